@@ -1,0 +1,265 @@
+// Oracle for decode-step top-k sparse attention -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, single-threaded CPU restatement of the four stages, written
+// for a reader to check by eye. Only the tests, the smoke check and the
+// benchmark's CPU-baseline leg load it; the library never calls it, and it
+// shares no code, header or table with the CUDA path.
+//
+// Sources (the pages give prose, no formulas or code):
+//   [DS]   "Support double sparsity" (sglang PR #1459): sections "Motivation",
+//          "Modifications" (a Triton sparse decode attention) and "Speedup
+//          Evaluation" (heavy channels, heavy tokens); the review thread's
+//          forward_extend traceback shows the label cache as a per-token,
+//          per-head gather of K channels (index [tokens, heads, channels]).
+//   [QSA]  sglang PR #43527 "QSA cache sharding": section "Distributed QSA
+//          execution" (scan, exact Top-K with deterministic global token-ID
+//          tie-breaking, owner-side sparse attention, FP32 log-sum-exp merge
+//          of partial outputs) and "CUDA Graph metadata" (page-table tails are
+//          not cleared; consumers stop at the sequence length).
+//   [PLG]  "QSA HiSparse - SGLang plugin", section "Supported versions": FP8
+//          E4M3 KV cache, page size 64.
+//   [CP]   sglang PR #39721, "Motivation": the QSA indexer scores and selects
+//          top-k; sparse_gqa attends over the selection.
+//
+// Readings taken where the pages are silent (each one is a choice):
+//   R1 proxy score of KV head g = sum over the query heads h of g's group of
+//      sum_c qp[b,h,c] * L[slot(b,t), gL, c]; no scale, no activation.
+//      gL = g for a per-head label cache, 0 for a shared index key.
+//   R2 GQA grouping is contiguous: query head h belongs to KV head h / G.
+//   R3 slot(b,t) = page_table[b][t / P] * P + t % P.
+//   R4 top-k order: larger score first, equal scores by smaller token index;
+//      NaN ranks below every number. Output ascending by token index, padded
+//      with -1 after min(k, T_b) entries.
+//   R5 attention scale is a caller argument (1/sqrt(D) by default); logs are
+//      natural logs.
+//   R6 split-KV: contiguous balanced chunks of the selected list, or chunk =
+//      logical page mod S (the page-owner placement); an empty chunk has
+//      lse = -inf and o = 0.
+//   R7 FP8 values are e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+//      bits, subnormals, S.1111.111 = NaN, no infinities) times one fp32 scale
+//      per physical page, separate for K and V.
+//
+// All arithmetic is in double; the scores are rounded to float once, at the
+// end (the top-k ranks float scores, as the CUDA path does).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <limits>
+#include <vector>
+
+namespace {
+
+// bfloat16 is the upper half of an IEEE binary32.
+double bf16_value(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// OCP FP8 E4M3 (reading R7), decoded from the bit fields.
+double e4m3_value(uint8_t byte) {
+  const int sign = (byte >> 7) & 1;
+  const int exp = (byte >> 3) & 0xF;
+  const int man = byte & 0x7;
+  double mag;
+  if (exp == 0xF && man == 0x7) return std::numeric_limits<double>::quiet_NaN();
+  if (exp == 0)
+    mag = std::ldexp(static_cast<double>(man) / 8.0, 1 - 7);        // subnormal
+  else
+    mag = std::ldexp(1.0 + static_cast<double>(man) / 8.0, exp - 7);  // normal
+  return sign ? -mag : mag;
+}
+
+long long slot_of(const int32_t* page_table, int max_pages, int page_size, int b, long long t) {
+  const long long page = page_table[static_cast<long long>(b) * max_pages + t / page_size];
+  return page * page_size + t % page_size;
+}
+
+}  // namespace
+
+extern "C" {
+
+double oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
+double oracle_e4m3_value(uint8_t byte) { return e4m3_value(byte); }
+
+// Stage 1, proxy scoring ([DS] label cache, [QSA]/[CP] index scan; R1-R3).
+//   qp      bf16 bits [B, Hq, C]
+//   label   bf16 bits [num_slots, HL, C], HL = Hkv (per-head label) or 1 (shared key)
+//   scores  float [B, Hkv, Tmax]; only t < seq_lens[b] is written.
+//   row_mask (may be null) uint8 [B, Hkv]: compute only rows with a nonzero mask.
+// Returns 0, or -1 on an argument outside the definition.
+int oracle_index_score(int B, int Hq, int Hkv, int HL, int C, int page_size, int max_pages,
+                       int Tmax, const uint16_t* qp, const uint16_t* label,
+                       const int32_t* page_table, const int32_t* seq_lens,
+                       const uint8_t* row_mask, float* scores) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || !(HL == Hkv || HL == 1)) return -1;
+  const int G = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    const long long T = seq_lens[b];
+    if (T < 0 || T > Tmax || T > static_cast<long long>(max_pages) * page_size) return -1;
+    for (int g = 0; g < Hkv; ++g) {
+      if (row_mask && !row_mask[b * Hkv + g]) continue;
+      const int gL = (HL == 1) ? 0 : g;
+      for (long long t = 0; t < T; ++t) {
+        const long long slot = slot_of(page_table, max_pages, page_size, b, t);
+        double s = 0.0;
+        for (int h = g * G; h < (g + 1) * G; ++h) {
+          for (int c = 0; c < C; ++c) {
+            const double qv = bf16_value(qp[(static_cast<long long>(b) * Hq + h) * C + c]);
+            const double lv = bf16_value(label[(slot * HL + gL) * C + c]);
+            s += qv * lv;
+          }
+        }
+        scores[(static_cast<long long>(b) * Hkv + g) * Tmax + t] = static_cast<float>(s);
+      }
+    }
+  }
+  return 0;
+}
+
+// Stage 2, exact top-k with lowest-token-index tie-breaking ([QSA] "Distributed
+// QSA execution"; R4). Sorts every token of the row by the total order, keeps
+// the first min(k, T_b), and writes them ascending by token index.
+//   scores float [B, Hkv, Tmax];  idx int32 [B, Hkv, k]
+int oracle_topk(int B, int Hkv, int Tmax, const float* scores, const int32_t* seq_lens, int k,
+                const uint8_t* row_mask, int32_t* idx) {
+  if (k < 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    const int T = seq_lens[b];
+    if (T < 0 || T > Tmax) return -1;
+    for (int g = 0; g < Hkv; ++g) {
+      if (row_mask && !row_mask[b * Hkv + g]) continue;
+      const float* s = scores + (static_cast<long long>(b) * Hkv + g) * Tmax;
+      std::vector<int32_t> order(T);
+      for (int t = 0; t < T; ++t) order[t] = t;
+      auto before = [s](int32_t x, int32_t y) {
+        const bool nx = std::isnan(s[x]), ny = std::isnan(s[y]);
+        if (nx != ny) return ny;             // a number ranks above NaN
+        if (!nx && s[x] != s[y]) return s[x] > s[y];
+        return x < y;                        // equal scores: smaller token index first
+      };
+      std::sort(order.begin(), order.end(), before);
+      const int keff = std::min(k, T);
+      std::vector<int32_t> chosen(order.begin(), order.begin() + keff);
+      std::sort(chosen.begin(), chosen.end());
+      int32_t* out = idx + (static_cast<long long>(b) * Hkv + g) * k;
+      for (int i = 0; i < k; ++i) out[i] = (i < keff) ? chosen[i] : -1;
+    }
+  }
+  return 0;
+}
+
+// Stage 3, sparse GQA decode attention over the selected tokens ([DS]
+// "Modifications", [CP] sparse_gqa, [PLG] paged FP8 KV; R2, R3, R5-R7).
+//   q        bf16 bits [B, Hq, D]
+//   k_cache  [num_slots, Hkv, D], bf16 bits (kv_fp8 == 0) or e4m3 bytes (kv_fp8 == 1)
+//   k_scale  float [num_pages] (FP8 only)
+//   idx      int32 [B, Hkv, k]: a prefix of valid token indices, then -1
+//   o_part   double [S, B, Hq, D]; lse_part double [S, B, Hq]
+// Chunk j of the valid list is positions [j*n/S, (j+1)*n/S) (split_mode 0), or
+// the tokens whose logical page mod S equals j (split_mode 1).
+int oracle_sparse_attn(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int kv_fp8,
+                       const uint16_t* q, const void* k_cache, const void* v_cache,
+                       const float* k_scale, const float* v_scale, const int32_t* page_table,
+                       const int32_t* seq_lens, const int32_t* idx, int k, double sm_scale,
+                       int num_splits, int split_mode, const uint8_t* row_mask,
+                       double* o_part, double* lse_part) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || num_splits < 1 || k < 0) return -1;
+  const int G = Hq / Hkv;
+  const int S = num_splits;
+  const double NEG_INF = -std::numeric_limits<double>::infinity();
+  auto kval = [&](long long slot, int g, int d) {
+    const long long e = (slot * Hkv + g) * D + d;
+    if (!kv_fp8) return bf16_value(static_cast<const uint16_t*>(k_cache)[e]);
+    return e4m3_value(static_cast<const uint8_t*>(k_cache)[e]) * k_scale[slot / page_size];
+  };
+  auto vval = [&](long long slot, int g, int d) {
+    const long long e = (slot * Hkv + g) * D + d;
+    if (!kv_fp8) return bf16_value(static_cast<const uint16_t*>(v_cache)[e]);
+    return e4m3_value(static_cast<const uint8_t*>(v_cache)[e]) * v_scale[slot / page_size];
+  };
+  for (int b = 0; b < B; ++b) {
+    const int T = seq_lens[b];
+    for (int g = 0; g < Hkv; ++g) {
+      if (row_mask && !row_mask[b * Hkv + g]) continue;
+      const int32_t* row = idx + (static_cast<long long>(b) * Hkv + g) * k;
+      int n = 0;
+      while (n < k && row[n] >= 0) ++n;
+      for (int i = 0; i < n; ++i)
+        if (row[i] >= T) return -1;
+      for (int h = g * G; h < (g + 1) * G; ++h) {
+        const uint16_t* qh = q + (static_cast<long long>(b) * Hq + h) * D;
+        for (int j = 0; j < S; ++j) {
+          std::vector<int32_t> chunk;
+          for (int i = 0; i < n; ++i) {
+            const bool mine = (split_mode == 0)
+                                  ? (i >= static_cast<long long>(j) * n / S &&
+                                     i < static_cast<long long>(j + 1) * n / S)
+                                  : ((row[i] / page_size) % S == j);
+            if (mine) chunk.push_back(row[i]);
+          }
+          double* o = o_part + ((static_cast<long long>(j) * B + b) * Hq + h) * D;
+          double& lse = lse_part[(static_cast<long long>(j) * B + b) * Hq + h];
+          for (int d = 0; d < D; ++d) o[d] = 0.0;
+          if (chunk.empty()) {
+            lse = NEG_INF;
+            continue;
+          }
+          std::vector<double> z(chunk.size());
+          double m = NEG_INF;
+          for (size_t i = 0; i < chunk.size(); ++i) {
+            const long long slot = slot_of(page_table, max_pages, page_size, b, chunk[i]);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += bf16_value(qh[d]) * kval(slot, g, d);
+            z[i] = sm_scale * dot;
+            m = std::max(m, z[i]);
+          }
+          double l = 0.0;
+          for (size_t i = 0; i < chunk.size(); ++i) {
+            const long long slot = slot_of(page_table, max_pages, page_size, b, chunk[i]);
+            const double w = std::exp(z[i] - m);
+            l += w;
+            for (int d = 0; d < D; ++d) o[d] += w * vval(slot, g, d);
+          }
+          for (int d = 0; d < D; ++d) o[d] /= l;
+          lse = m + std::log(l);
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+// Stage 4, log-sum-exp merge of split partials ([QSA] "Distributed QSA
+// execution": partial outputs merged with FP32 log-sum-exp normalisation; here
+// in double). lse = log sum_j exp(lse_j); o = sum_j exp(lse_j - lse) * o_j.
+//   o_part [S, rows, D]; lse_part [S, rows] -> out [rows, D]; lse [rows]
+int oracle_lse_merge(int S, long long rows, int D, const double* o_part, const double* lse_part,
+                     double* out, double* lse) {
+  if (S < 1) return -1;
+  const double NEG_INF = -std::numeric_limits<double>::infinity();
+  for (long long r = 0; r < rows; ++r) {
+    double m = NEG_INF;
+    for (int j = 0; j < S; ++j) m = std::max(m, lse_part[j * rows + r]);
+    double* o = out + r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (m == NEG_INF) {
+      lse[r] = NEG_INF;
+      continue;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < S; ++j) sum += std::exp(lse_part[j * rows + r] - m);
+    lse[r] = m + std::log(sum);
+    for (int j = 0; j < S; ++j) {
+      const double w = std::exp(lse_part[j * rows + r] - lse[r]);
+      if (w == 0.0) continue;
+      for (int d = 0; d < D; ++d) o[d] += w * o_part[(j * rows + r) * D + d];
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,291 @@
+"""Pins of the oracle against what the pages and the mathematics fix.
+
+None of these tests compares the oracle with a retyped copy of itself. Each
+one checks it against a library routine on a special case (torch matmul and
+scaled_dot_product_attention, torch's bf16 / e4m3 conversions), a closed form,
+an invariant the definition implies (GQA decomposition, page relocation,
+split/unsplit equality), or brute force on tiny inputs.
+"""
+import math
+
+import pytest
+import torch
+import torch.nn.functional as F
+
+import dsgen
+import oracle
+
+P = 64
+
+
+# ---------------------------------------------------------------- decoders
+
+def test_bf16_decoder_matches_torch_on_every_code():
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).double()
+    got = torch.tensor([oracle.bf16_value(int(b) & 0xFFFF) for b in bits.tolist()], dtype=torch.float64)
+    nan = torch.isnan(ref)
+    assert torch.equal(torch.isnan(got), nan)
+    assert torch.equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_matches_torch_on_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double()
+    got = torch.tensor([oracle.e4m3_value(c) for c in range(256)], dtype=torch.float64)
+    nan = torch.isnan(ref)
+    assert nan.sum() == 2                      # S.1111.111 only: the format has no infinities
+    assert torch.equal(torch.isnan(got), nan)
+    assert torch.equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x80] == 0.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def _paged(dense: torch.Tensor, page_table: torch.Tensor, num_pages: int) -> torch.Tensor:
+    """Scatter per-request rows dense[b, t, ...] into a page pool via the page table."""
+    B, T = dense.shape[:2]
+    pool = torch.zeros((num_pages * P,) + tuple(dense.shape[2:]), dtype=dense.dtype)
+    for b in range(B):
+        for t in range(T):
+            pool[int(page_table[b, t // P]) * P + t % P] = dense[b, t]
+    return pool
+
+
+def _shuffled_table(B, pages_per_req, seed):
+    total = B * pages_per_req
+    perm = dsgen.permutation(total, seed, 7)
+    return perm.view(B, pages_per_req).clone(), total
+
+
+def _ints(shape, lo, hi, seed, tid):
+    return dsgen.uniform_int(shape, lo, hi, seed, tid)
+
+
+# ---------------------------------------------------------------- stage 1: scores
+
+def test_score_is_matmul_when_label_is_the_key_and_group_is_one():
+    # With G = 1 and C = D, the label row of head g is K itself and qp is q:
+    # the proxy score is the plain dot product q . K_t, i.e. a matmul.
+    B, H, C, T = 2, 3, 16, 150
+    pt, npages = _shuffled_table(B, 3, 11)
+    dense = _ints((B, T, H, C), -8, 8, 11, 1)
+    label = _paged(dense, pt, npages)
+    qp = _ints((B, H, C), -4, 4, 11, 2)
+    seq = torch.tensor([150, 97], dtype=torch.int32)
+    s = oracle.index_score(qp, label, pt, seq, H, T)
+    for b in range(B):
+        Tb = int(seq[b])
+        ref = torch.matmul(dense[b, :Tb].double().permute(1, 0, 2), qp[b].double().unsqueeze(-1)).squeeze(-1)
+        assert torch.equal(s[b, :, :Tb].double(), ref)
+        assert torch.isnan(s[b, :, Tb:]).all()     # nothing written past the length
+
+
+def test_score_group_is_the_sum_of_its_query_heads():
+    # Contiguous GQA grouping: KV head g scores with query heads g*G .. g*G+G-1.
+    B, Hq, Hkv, C, T = 1, 8, 2, 32, 130
+    G = Hq // Hkv
+    pt, npages = _shuffled_table(B, 3, 12)
+    label = _ints((npages * P, Hkv, C), -8, 8, 12, 1)
+    qp = _ints((B, Hq, C), -4, 4, 12, 2)
+    seq = torch.tensor([T], dtype=torch.int32)
+    grouped = oracle.index_score(qp, label, pt, seq, Hkv, T)
+    per_head = oracle.index_score(qp, label.repeat_interleave(G, dim=1), pt, seq, Hq, T)
+    ref = per_head.view(B, Hkv, G, T).double().sum(2)
+    assert torch.equal(grouped.double(), ref)
+
+
+def test_shared_index_key_equals_a_replicated_per_head_label():
+    B, Hq, Hkv, C, T = 2, 8, 4, 64, 100
+    pt, npages = _shuffled_table(B, 2, 13)
+    keys = _ints((npages * P, 1, C), -8, 8, 13, 1)
+    qp = _ints((B, Hq, C), -4, 4, 13, 2)
+    seq = torch.tensor([100, 65], dtype=torch.int32)
+    shared = oracle.index_score(qp, keys, pt, seq, Hkv, T)
+    repl = oracle.index_score(qp, keys.expand(-1, Hkv, -1).contiguous(), pt, seq, Hkv, T)
+    assert torch.equal(torch.nan_to_num(shared, 7.5), torch.nan_to_num(repl, 7.5))
+
+
+def test_score_does_not_depend_on_where_pages_live():
+    B, Hq, Hkv, C, T = 2, 4, 2, 16, 200
+    pt, npages = _shuffled_table(B, 4, 14)
+    dense = _ints((B, T, Hkv, C), -8, 8, 14, 1)
+    qp = _ints((B, Hq, C), -4, 4, 14, 2)
+    seq = torch.tensor([200, 129], dtype=torch.int32)
+    a = oracle.index_score(qp, _paged(dense, pt, npages), pt, seq, Hkv, T)
+    pt2 = pt.flip(1).roll(1, 0).contiguous()        # another placement of the same pages
+    b = oracle.index_score(qp, _paged(dense, pt2, npages), pt2, seq, Hkv, T)
+    assert torch.equal(torch.nan_to_num(a, 7.5), torch.nan_to_num(b, 7.5))
+
+
+def test_score_worked_example_by_hand():
+    # One request, one KV head of two query heads, C = 2, pages of 64 with the
+    # request's single page stored at physical page 1. Token 0 has label
+    # (1, 2), token 1 has (-3, 4); queries (1, 1) and (2, -1) sum to (3, 0):
+    # scores 3*1 + 0*2 = 3 and 3*(-3) + 0*4 = -9.
+    label = torch.zeros((2 * P, 1, 2), dtype=torch.bfloat16)
+    label[P + 0, 0] = torch.tensor([1.0, 2.0])
+    label[P + 1, 0] = torch.tensor([-3.0, 4.0])
+    qp = torch.tensor([[[1.0, 1.0], [2.0, -1.0]]], dtype=torch.bfloat16)
+    pt = torch.tensor([[1]], dtype=torch.int32)
+    s = oracle.index_score(qp, label, pt, torch.tensor([2], dtype=torch.int32), 1, 2)
+    assert s[0, 0].tolist() == [3.0, -9.0]
+
+
+# ---------------------------------------------------------------- stage 2: top-k
+
+def _brute_topk(s, T, k):
+    keyed = sorted(range(T), key=lambda t: (-s[t], t))
+    return sorted(keyed[:min(k, T)]) + [-1] * (k - min(k, T))
+
+
+@pytest.mark.parametrize("T,k,lo,hi", [(1, 1, -2, 2), (17, 5, -2, 2), (64, 64, -1, 1), (100, 7, 0, 0),
+                                       (250, 40, -3, 3), (33, 50, -5, 5), (513, 128, -50, 50)])
+def test_topk_equals_brute_force_sort(T, k, lo, hi):
+    B, H = 2, 3
+    s = _ints((B, H, T), lo, hi, T * 31 + k, 1).float()
+    seq = torch.tensor([T, max(0, T - 9)], dtype=torch.int32)
+    idx = oracle.topk(s, seq, k)
+    for b in range(B):
+        for g in range(H):
+            assert idx[b, g].tolist() == _brute_topk(s[b, g].tolist(), int(seq[b]), k)
+
+
+def test_topk_all_ties_take_the_lowest_indices():
+    s = torch.full((1, 1, 1000), 3.0)
+    idx = oracle.topk(s, torch.tensor([1000], dtype=torch.int32), 10)
+    assert idx[0, 0].tolist() == list(range(10))
+
+
+def test_topk_negative_zero_ties_with_zero():
+    s = torch.tensor([[[-0.0, 0.0, -0.0, 1.0, -1.0]]])
+    idx = oracle.topk(s, torch.tensor([5], dtype=torch.int32), 3)
+    assert idx[0, 0].tolist() == [0, 1, 3]
+
+
+def test_topk_nan_ranks_last_and_empty_rows_pad():
+    s = torch.tensor([[[float("nan"), -100.0, float("nan"), 5.0]]])
+    assert oracle.topk(s, torch.tensor([4], dtype=torch.int32), 3)[0, 0].tolist() == [0, 1, 3]
+    assert oracle.topk(s, torch.tensor([0], dtype=torch.int32), 3)[0, 0].tolist() == [-1, -1, -1]
+    assert oracle.topk(s, torch.tensor([4], dtype=torch.int32), 0).shape == (1, 1, 0)
+
+
+# ---------------------------------------------------------------- stage 3: attention
+
+def _dequant(inp, cache, scale):
+    if cache.dtype == torch.uint8:
+        vals = cache.view(torch.float8_e4m3fn).double()
+        return vals * scale.double().repeat_interleave(P).view(-1, 1, 1)
+    return cache.double()
+
+
+def _sdpa_rows(q_bh, K_rows, V_rows, scale):
+    """Library attention of one query over given rows, with its lse."""
+    o = F.scaled_dot_product_attention(q_bh.view(1, 1, 1, -1), K_rows.unsqueeze(0).unsqueeze(0),
+                                       V_rows.unsqueeze(0).unsqueeze(0), scale=scale).view(-1)
+    lse = torch.logsumexp(scale * (K_rows @ q_bh), 0)
+    return o, lse
+
+
+def _small_workload(kv_dtype, B=2, Hq=8, Hkv=2, T=(300, 131), C=16, HL=None, k=40, shuffle=True):
+    return dsgen.Workload(name="pin", batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=32,
+                          seq_lens=list(T), proxy_dim=C, label_heads=Hkv if HL is None else HL,
+                          top_k=k, kv_dtype=kv_dtype, shuffle_pages=shuffle, seed=77,
+                          proxy_from_query=False)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_attention_with_k_at_least_T_is_dense_softmax_attention(kv_dtype):
+    w = _small_workload(kv_dtype)
+    inp = dsgen.make_inputs(w)
+    k = w.max_seq_len + 5
+    _, idx, out, lse = oracle.decode(inp, k=k)
+    Kd = _dequant(inp, inp.k_cache, inp.k_scale)
+    Vd = _dequant(inp, inp.v_cache, inp.v_scale)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    for b in range(w.batch):
+        Tb = w.seq_lens[b]
+        assert idx[b, :, :Tb].tolist() == [list(range(Tb))] * w.num_kv_heads
+        slots = inp.page_table[b, torch.arange(Tb) // P].long() * P + torch.arange(Tb) % P
+        for h in range(w.num_q_heads):
+            g = h // w.group
+            o_ref, lse_ref = _sdpa_rows(inp.q[b, h].double(), Kd[slots, g], Vd[slots, g], scale)
+            assert torch.allclose(out[b, h], o_ref, rtol=0, atol=1e-12)
+            assert abs(float(lse[b, h]) - float(lse_ref)) < 1e-12
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_sparse_attention_equals_library_attention_over_the_selected_rows(kv_dtype):
+    w = _small_workload(kv_dtype)
+    inp = dsgen.make_inputs(w)
+    _, idx, out, lse = oracle.decode(inp)
+    Kd = _dequant(inp, inp.k_cache, inp.k_scale)
+    Vd = _dequant(inp, inp.v_cache, inp.v_scale)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    for b in range(w.batch):
+        for h in range(w.num_q_heads):
+            g = h // w.group
+            sel = idx[b, g][idx[b, g] >= 0].long()
+            assert len(sel) == min(w.top_k, w.seq_lens[b])
+            slots = inp.page_table[b, sel // P].long() * P + sel % P
+            o_ref, lse_ref = _sdpa_rows(inp.q[b, h].double(), Kd[slots, g], Vd[slots, g], scale)
+            assert torch.allclose(out[b, h], o_ref, rtol=0, atol=1e-12)
+            assert abs(float(lse[b, h]) - float(lse_ref)) < 1e-12
+
+
+def test_single_selected_token_returns_its_value_row():
+    w = _small_workload("bf16", k=1)
+    inp = dsgen.make_inputs(w)
+    _, idx, out, _ = oracle.decode(inp)
+    for b in range(w.batch):
+        for h in range(w.num_q_heads):
+            t = int(idx[b, h // w.group, 0])
+            slot = int(inp.page_table[b, t // P]) * P + t % P
+            assert torch.equal(out[b, h], inp.v_cache[slot, h // w.group].double())
+
+
+def test_empty_rows_give_zero_output_and_minus_infinity_lse():
+    w = _small_workload("bf16", T=(0, 70))
+    inp = dsgen.make_inputs(w)
+    _, idx, out, lse = oracle.decode(inp)
+    assert (idx[0] == -1).all()
+    assert torch.equal(out[0], torch.zeros_like(out[0]))
+    assert torch.isinf(lse[0]).all() and (lse[0] < 0).all()
+    _, _, out0, lse0 = oracle.decode(inp, k=0)
+    assert torch.equal(out0, torch.zeros_like(out0)) and torch.isinf(lse0).all()
+
+
+# ---------------------------------------------------------------- stage 4: merge
+
+@pytest.mark.parametrize("S", [2, 3, 4, 16, 64])
+@pytest.mark.parametrize("split_mode", [0, 1])
+def test_merge_of_any_split_equals_the_unsplit_result(S, split_mode):
+    w = _small_workload("fp8_e4m3", T=(700, 45), k=90)
+    inp = dsgen.make_inputs(w)
+    _, idx, out1, lse1 = oracle.decode(inp)
+    o, l = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                              inp.page_table, inp.seq_lens, idx, None, S, split_mode)
+    if S > 45:
+        assert torch.isinf(l[:, 1]).any()               # some chunks of the short request are empty
+    out, lse = oracle.lse_merge(o, l)
+    assert torch.allclose(out, out1, rtol=0, atol=1e-12)
+    assert torch.allclose(lse, lse1, rtol=0, atol=1e-12)
+
+
+def test_merge_closed_form_two_partials():
+    # lse_1 = 0, lse_2 = ln 3: total lse = ln 4, weights 1/4 and 3/4.
+    o = torch.tensor([[[1.0, 0.0]], [[0.0, 2.0]]], dtype=torch.float64)
+    l = torch.tensor([[0.0], [math.log(3.0)]], dtype=torch.float64)
+    out, lse = oracle.lse_merge(o, l)
+    assert torch.allclose(out, torch.tensor([[0.25, 1.5]], dtype=torch.float64), atol=1e-15)
+    assert abs(float(lse[0]) - math.log(4.0)) < 1e-15
+
+
+def test_merge_single_split_is_identity_and_all_empty_is_empty():
+    o = torch.randn(1, 5, 8, dtype=torch.float64)
+    l = torch.randn(1, 5, dtype=torch.float64)
+    out, lse = oracle.lse_merge(o, l)
+    assert torch.allclose(out, o[0], atol=1e-15) and torch.allclose(lse, l[0], atol=1e-15)
+    out, lse = oracle.lse_merge(torch.zeros(3, 2, 4, dtype=torch.float64),
+                                torch.full((3, 2), -math.inf, dtype=torch.float64))
+    assert torch.equal(out, torch.zeros(2, 4, dtype=torch.float64)) and torch.isinf(lse).all()
