@@ -292,3 +292,11 @@ def _normal_at(seed, tensor_id, start, shape, device):
     u1 = (hash_u32(k1, start, n, device).to(torch.float32) + 0.5) * (1.0 / 4294967296.0)
     u2 = hash_u32(k2, start, n, device).to(torch.float32) * (1.0 / 4294967296.0)
     return (torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)).view(shape)
+
+
+def shape_kwargs(inp: Inputs) -> dict:
+    """Sizes of ``inp`` as keyword arguments of the library's ds_shape."""
+    w = inp.w
+    return dict(batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                page_size=w.page_size, max_pages_per_req=int(inp.page_table.shape[1]), num_pages=int(inp.num_pages),
+                max_seq_len=w.max_seq_len)

@@ -1,0 +1,221 @@
+/*
+ * ds_sparse.h -- C ABI of the decode-step top-k sparse attention library
+ * (libdssparse.so, CUDA, sm_103a).
+ *
+ * One decode step of Double-Sparsity / QSA-style attention runs in four stages:
+ *   1. ds_index_score        score every cached token with a cheap proxy
+ *   2. ds_topk_select        keep the exact top-k tokens per (request, KV head)
+ *   3. ds_sparse_decode_attn GQA attention over the kept tokens only, gathered
+ *                            from a paged bf16 or FP8-E4M3 KV cache
+ *   4. ds_lse_merge          merge split-KV partial outputs by log-sum-exp
+ * and ds_sparse_decode chains all four on one stream.
+ *
+ * Sources: "Support double sparsity" (sglang PR #1459: label cache of heavy
+ * channels, heavy-token selection, sparse decode attention); sglang PR #43527
+ * "QSA cache sharding", sections "Distributed QSA execution" (exact Top-K with
+ * deterministic global token-ID tie-breaking, owner-side sparse attention,
+ * FP32 log-sum-exp merge), "CUDA Graph buffers" and "CUDA Graph metadata";
+ * "QSA HiSparse - SGLang plugin", "Supported versions" (FP8 E4M3 KV cache,
+ * page size 64).
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers on the current device unless stated.
+ *    The caller owns all memory; the library never allocates or frees.
+ *  - Calls are asynchronous on `stream` and never synchronise the host.
+ *    Arguments are validated on the host before any launch; a call that
+ *    returns an error has launched nothing.
+ *  - Problems the host cannot see (a seq_len, page id or token index outside
+ *    its range) never cause an out-of-bounds access: the kernel skips the bad
+ *    element and sets a bit in a sticky device error word, read back with
+ *    ds_device_errors(). Results of such a call are unspecified.
+ *  - Tensor layouts are row-major and dense; base pointers are 16-byte aligned.
+ *  - GQA grouping is contiguous: query head h uses KV head h / (Hq / Hkv).
+ *  - Logical token t of request b lives in physical slot
+ *        page_table[b][t / page_size] * page_size + t % page_size.
+ *    Page-table entries at or past ceil(seq_lens[b] / page_size) are never read.
+ */
+#ifndef DS_SPARSE_H
+#define DS_SPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* ds_stream_t;
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = -1,   /* null pointer, negative size, misaligned pointer, too-small buffer */
+  DS_ERR_UNSUPPORTED = -2,   /* a size this build does not implement (head_dim, page_size, group, ...) */
+  DS_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+  DS_ERR_WORKSPACE = -4,     /* workspace too small (see the *_workspace_bytes queries) */
+  DS_ERR_DEVICE_CHECK = -5   /* ds_device_errors found a flagged element */
+} ds_status;
+
+typedef enum { DS_KV_BF16 = 0, DS_KV_FP8_E4M3 = 1 } ds_kv_dtype;
+
+/* How stage 3 cuts a row's selected tokens into num_splits chunks. */
+typedef enum {
+  DS_SPLIT_CONTIGUOUS = 0,       /* chunk j = positions [j*n/S, (j+1)*n/S) of the n selected tokens */
+  DS_SPLIT_PAGE_INTERLEAVED = 1  /* chunk j = selected tokens whose logical page % S == j (page owners) */
+} ds_split_mode;
+
+/* Bits of the device error word. */
+#define DS_DEVERR_SEQ_LEN   1u   /* seq_lens[b] < 0 or > min(max_seq_len, max_pages_per_req*page_size); clamped */
+#define DS_DEVERR_PAGE_ID   2u   /* a page-table entry outside [0, num_pages); its tokens were skipped */
+#define DS_DEVERR_TOKEN_IDX 4u   /* an index entry outside [0, seq_lens[b]) before the -1 padding; skipped */
+
+typedef struct {
+  int batch;             /* B, requests in the step (>= 0) */
+  int num_q_heads;       /* Hq, a multiple of num_kv_heads; Hq / Hkv in {1, 2, 4, 8} */
+  int num_kv_heads;      /* Hkv (>= 1) */
+  int head_dim;          /* D; this build supports 128 */
+  int page_size;         /* P; this build supports 64 */
+  int max_pages_per_req; /* row stride of page_table (>= 1) */
+  int num_pages;         /* physical pages in the pool; valid page ids are [0, num_pages) */
+  int max_seq_len;       /* Tmax, row stride of the score buffer; every seq_lens[b] must be <= it */
+} ds_shape;
+
+/*
+ * Stage 1: proxy scores ("Support double sparsity": the query's heavy channels
+ * against a label cache of heavy K channels; PR #39721 / #43527: the QSA
+ * indexer scans per-token index keys and scores them).
+ *
+ *   s[b, g, t] = sum over q-heads h of group g, sum_c qp[b, h, c] * label[slot(b,t), gL, c]
+ *
+ * for t < seq_lens[b], with gL = g when label_heads == Hkv (a per-head label
+ * cache) and gL = 0 when label_heads == 1 (one index key per token shared by
+ * all heads). Accumulated in fp32; exact whenever every partial sum is an
+ * integer below 2^24 in magnitude (e.g. integer-valued inputs).
+ *
+ *   qp          bf16  [B, Hq, proxy_dim]                      proxy query
+ *   proxy_dim   C in {16, 32, 64}
+ *   label       bf16  [num_pages * P, label_heads, proxy_dim] label cache / index keys
+ *   label_heads Hkv or 1
+ *   page_table  int32 [B, max_pages_per_req]
+ *   seq_lens    int32 [B]
+ *   scores      fp32  [B, Hkv, max_seq_len]; positions t >= seq_lens[b] are not written
+ */
+ds_status ds_index_score(const ds_shape* shape, const void* qp, int proxy_dim, const void* label,
+                         int label_heads, const int32_t* page_table, const int32_t* seq_lens,
+                         float* scores, ds_stream_t stream);
+
+/*
+ * Stage 2: exact top-k (PR #43527, "Distributed QSA execution": exact Top-K
+ * with deterministic token-ID tie-breaking; PR #1459 heavy-token count).
+ *
+ * For each row (b, g) keeps the K_eff = min(k, seq_lens[b]) tokens that come
+ * first in the order (score descending, token index ascending): equal scores
+ * go to the smaller token index, -0.0 equals +0.0, NaN ranks below every
+ * number. The result is unique. idx[b, g, :] holds the kept token indices in
+ * ascending order followed by -1 up to k. k == 0 or seq_lens[b] == 0 gives
+ * an all -1 row.
+ *
+ *   scores     fp32  [B, Hkv, max_seq_len] (only t < seq_lens[b] is read)
+ *   idx        int32 [B, Hkv, k]
+ *   workspace  device scratch of at least ds_topk_workspace_bytes(shape, k)
+ *              bytes, 256-byte aligned; its contents need no initialisation and
+ *              are overwritten. Two calls in flight at once need two workspaces.
+ */
+size_t ds_topk_workspace_bytes(const ds_shape* shape, int k);
+ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
+                         int32_t* idx, void* workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/*
+ * Stage 3: sparse GQA decode attention over the selected tokens (PR #1459
+ * sparse decode attention; PR #39721 sparse_gqa; FP8 E4M3 paged KV of the
+ * QSA HiSparse plugin).
+ *
+ * For query head h of request b, with g = h / G and I the valid entries of
+ * idx[b, g, :] (a prefix of token indices, then -1):
+ *   z_t = sm_scale * q[b,h,:] . K[slot(b,t), g, :]
+ *   o   = sum_{t in I} softmax(z)_t * V[slot(b,t), g, :],  lse = ln sum_{t in I} exp(z_t)
+ * FP8 values are e4m3 times one fp32 scale per physical page (k_scale for K,
+ * v_scale for V). Math is fp32.
+ *
+ * num_splits == 1: writes out (bf16 [B, Hq, D]) and lse (fp32 [B, Hq]).
+ * num_splits  > 1: cuts I into S chunks by split_mode and writes, per chunk j,
+ *   the normalised partial o_part[j] (fp32 [S, B, Hq, D]) and its
+ *   lse_part[j] (fp32 [S, B, Hq]); an empty chunk gives o = 0, lse = -inf.
+ *   out / lse are not touched (merge with ds_lse_merge).
+ * An empty row gives o = 0 and lse = -inf.
+ *
+ *   q         bf16 [B, Hq, D]
+ *   k_cache   [num_pages * P, Hkv, D], bf16 or e4m3 bytes per kv_dtype; v_cache likewise
+ *   k_scale   fp32 [num_pages] (FP8 only; NULL for bf16); v_scale likewise
+ *   idx       int32 [B, Hkv, k]
+ *   sm_scale  softmax scale, normally 1/sqrt(D)
+ */
+ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void* k_cache,
+                                const void* v_cache, ds_kv_dtype kv_dtype, const float* k_scale,
+                                const float* v_scale, const int32_t* page_table,
+                                const int32_t* seq_lens, const int32_t* idx, int k, float sm_scale,
+                                int num_splits, ds_split_mode split_mode, float* o_part,
+                                float* lse_part, void* out, float* lse, ds_stream_t stream);
+
+/*
+ * Stage 4: log-sum-exp merge of split partials (PR #43527: owner-side
+ * partial outputs merged with FP32 log-sum-exp normalisation).
+ *   lse = ln sum_j exp(lse_j);  out = sum_j exp(lse_j - lse) * o_j
+ * Chunks with lse_j = -inf weigh nothing; if all are -inf, out = 0 and
+ * lse = -inf.
+ *
+ *   o_part   fp32 [num_splits, rows, head_dim]; lse_part fp32 [num_splits, rows]
+ *   out      bf16 [rows, head_dim];             lse      fp32 [rows] (may be NULL)
+ *   head_dim a multiple of 4
+ */
+ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_part,
+                       const float* lse_part, void* out, float* lse, ds_stream_t stream);
+
+/* Arguments of the chained call (meanings as in the stages above). */
+typedef struct {
+  const void* q;             /* bf16 [B, Hq, D] */
+  const void* qp;            /* bf16 [B, Hq, proxy_dim] */
+  int proxy_dim;
+  const void* label;         /* bf16 [num_pages * P, label_heads, proxy_dim] */
+  int label_heads;
+  const void* k_cache;
+  const void* v_cache;
+  ds_kv_dtype kv_dtype;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int k;
+  float sm_scale;
+  int32_t* idx;              /* out: int32 [B, Hkv, k] selected tokens */
+  void* out;                 /* out: bf16 [B, Hq, D] */
+  float* lse;                /* out: fp32 [B, Hq] (may be NULL) */
+} ds_decode_args;
+
+/*
+ * The whole decode step: ds_index_score -> ds_topk_select ->
+ * ds_sparse_decode_attn (internal split-KV chosen for occupancy) ->
+ * ds_lse_merge, on one stream, with scores and partials in `workspace`
+ * (at least ds_decode_workspace_bytes bytes, 256-byte aligned, no
+ * initialisation needed). No host synchronisation and no allocation, so the
+ * call can be captured in a CUDA graph and replayed with new input contents.
+ */
+size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k);
+ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                           size_t workspace_bytes, ds_stream_t stream);
+
+/* Human-readable name of a status. */
+const char* ds_error_string(ds_status status);
+
+/*
+ * Synchronises the current device, returns the sticky device error word in
+ * *flags (DS_DEVERR_* bits) and clears it. Returns DS_ERR_DEVICE_CHECK when
+ * any bit was set, DS_OK otherwise.
+ */
+ds_status ds_device_errors(unsigned* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_SPARSE_H */

@@ -1,0 +1,100 @@
+"""The C ABI library loads, exports every entry point its header declares, and
+rejects bad arguments on the host (no GPU needed: none of these calls reaches
+a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds_sparse.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sparse_decode_label_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\*?\s+\**(ds_[a-z_]+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_four_stages_and_the_chain():
+    names = declared_functions()
+    for n in ("ds_index_score", "ds_topk_select", "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode",
+              "ds_topk_workspace_bytes", "ds_decode_workspace_bytes", "ds_error_string", "ds_device_errors"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def _shape(**kw):
+    import top_sparse_decode_label_gb300 as ds
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, max_pages_per_req=4,
+                num_pages=8, max_seq_len=256)
+    base.update(kw)
+    return ds.Shape(**base)
+
+
+def test_host_validation_without_a_gpu():
+    import top_sparse_decode_label_gb300 as ds
+    L = ds.lib()
+    P = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    # Null shape.
+    assert L.ds_index_score(None, P, 16, P, 2, P, P, P, None) == -1
+    # Group size 3 is not implemented.
+    assert L.ds_index_score(ctypes.byref(_shape(num_q_heads=6)), P, 16, P, 2, P, P, P, None) == -2
+    # Head dim 64 / page size 32 are not implemented.
+    assert L.ds_index_score(ctypes.byref(_shape(head_dim=64)), P, 16, P, 2, P, P, P, None) == -2
+    assert L.ds_index_score(ctypes.byref(_shape(page_size=32)), P, 16, P, 2, P, P, P, None) == -2
+    # Proxy width 24, label heads neither 1 nor Hkv.
+    assert L.ds_index_score(ctypes.byref(_shape()), P, 24, P, 2, P, P, P, None) == -2
+    assert L.ds_index_score(ctypes.byref(_shape()), P, 16, P, 3, P, P, P, None) == -1
+    # Hq not a multiple of Hkv; negative batch.
+    assert L.ds_index_score(ctypes.byref(_shape(num_q_heads=7)), P, 16, P, 2, P, P, P, None) == -1
+    assert L.ds_index_score(ctypes.byref(_shape(batch=-1)), P, 16, P, 2, P, P, P, None) == -1
+    # Negative k, too-small workspace.
+    assert L.ds_topk_select(ctypes.byref(_shape()), P, P, -1, P, P, 0, None) == -1
+    assert L.ds_topk_select(ctypes.byref(_shape()), P, P, 8, P, P, 0, None) == -4
+    # Bad split count / mode, null out for one split.
+    S = _shape()
+    assert L.ds_sparse_decode_attn(ctypes.byref(S), P, P, P, 0, None, None, P, P, P, 8, ctypes.c_float(0.1), 0,
+                                   0, None, None, P, None, None) == -1
+    assert L.ds_sparse_decode_attn(ctypes.byref(S), P, P, P, 0, None, None, P, P, P, 8, ctypes.c_float(0.1), 2,
+                                   7, P, P, None, None, None) == -1
+    assert L.ds_sparse_decode_attn(ctypes.byref(S), P, P, P, 0, None, None, P, P, P, 8, ctypes.c_float(0.1), 1,
+                                   0, None, None, None, None, None) == -1
+    # FP8 without scales.
+    assert L.ds_sparse_decode_attn(ctypes.byref(S), P, P, P, 1, None, None, P, P, P, 8, ctypes.c_float(0.1), 1,
+                                   0, None, None, P, None, None) == -1
+    # Merge: head_dim not a multiple of 4, zero splits.
+    assert L.ds_lse_merge(2, 4, 126, P, P, P, None, None) == -1
+    assert L.ds_lse_merge(0, 4, 128, P, P, P, None, None) == -1
+    # Misaligned query pointer.
+    assert L.ds_sparse_decode_attn(ctypes.byref(S), ctypes.c_void_p(18), P, P, 0, None, None, P, P, P, 8,
+                                   ctypes.c_float(0.1), 1, 0, None, None, P, None, None) == -1
+
+
+def test_workspace_queries_are_host_only_and_grow_with_the_problem():
+    import top_sparse_decode_label_gb300 as ds
+    a = ds.ds_topk_workspace_bytes(_shape(), 16)
+    b = ds.ds_topk_workspace_bytes(_shape(max_seq_len=4096), 16)
+    assert 0 < a < b and a % 256 == 0
+    c = ds.ds_decode_workspace_bytes(_shape(max_seq_len=4096), 16, 300)
+    assert c > b
+    assert ds.ds_topk_workspace_bytes(_shape(head_dim=64), 16) == 0
+
+
+def test_error_strings():
+    import top_sparse_decode_label_gb300 as ds
+    for st in (0, -1, -2, -3, -4, -5):
+        assert ds.lib().ds_error_string(st).startswith(b"DS_")

@@ -1,0 +1,278 @@
+// C ABI of libdssparse: argument validation, workspace layout and the chained
+// decode step. Every entry point validates on the host and then only enqueues
+// work on the caller's stream; nothing here allocates or synchronises, except
+// ds_device_errors which is documented to synchronise.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ds_sparse.h"
+#include "internal.h"
+
+// Sticky device error word (DS_DEVERR_* bits), one per device.
+static __device__ unsigned g_ds_device_errors;
+
+namespace ds {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Device address of the error word on the current device (resolved once).
+unsigned* error_word() {
+  static unsigned* ptrs[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ds_device_errors) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+ds_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DS_OK;
+  if (e == cudaErrorNotSupported) return DS_ERR_UNSUPPORTED;
+  return DS_ERR_CUDA;
+}
+
+ds_status check_shape(const ds_shape* s) {
+  if (!s) return DS_ERR_INVALID_ARG;
+  if (s->batch < 0 || s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->max_pages_per_req <= 0 ||
+      s->num_pages <= 0 || s->max_seq_len < 0 || s->head_dim <= 0 || s->page_size <= 0)
+    return DS_ERR_INVALID_ARG;
+  if (s->num_q_heads % s->num_kv_heads) return DS_ERR_INVALID_ARG;
+  const int G = s->num_q_heads / s->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return DS_ERR_UNSUPPORTED;
+  if (s->head_dim != kHeadDimSupported || s->page_size != kPageSupported) return DS_ERR_UNSUPPORTED;
+  // Slot and element offsets are 64-bit; page ids and token indices are int32.
+  if (static_cast<long long>(s->num_pages) * s->page_size > 0x7fffffffLL) return DS_ERR_UNSUPPORTED;
+  return DS_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+  static int counts[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  if (!counts[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+// Internal split count of the chained call: enough (request, KV head, split)
+// CTAs to cover the GPU about twice, at least 64 selected tokens per split.
+int decode_splits(const ds_shape* s, int k) {
+  const long long rows = static_cast<long long>(s->batch) * s->num_kv_heads;
+  if (rows <= 0 || k <= 64) return 1;
+  long long want = (kDecodeTargetCtas + rows - 1) / rows;
+  long long cap = (k + 63) / 64;
+  if (want > cap) want = cap;
+  if (want > 64) want = 64;
+  return want < 1 ? 1 : static_cast<int>(want);
+}
+
+}  // namespace ds
+
+using namespace ds;
+
+extern "C" {
+
+const char* ds_error_string(ds_status status) {
+  switch (status) {
+    case DS_OK: return "DS_OK";
+    case DS_ERR_INVALID_ARG: return "DS_ERR_INVALID_ARG: null, negative, misaligned or inconsistent argument";
+    case DS_ERR_UNSUPPORTED: return "DS_ERR_UNSUPPORTED: size not implemented by this build";
+    case DS_ERR_CUDA: return "DS_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case DS_ERR_WORKSPACE: return "DS_ERR_WORKSPACE: workspace too small or misaligned";
+    case DS_ERR_DEVICE_CHECK: return "DS_ERR_DEVICE_CHECK: a kernel flagged an out-of-range element";
+  }
+  return "unknown ds_status";
+}
+
+ds_status ds_device_errors(unsigned* flags) {
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DS_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_ds_device_errors, sizeof v) != cudaSuccess) return DS_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_ds_device_errors, &zero, sizeof zero) != cudaSuccess) return DS_ERR_CUDA;
+  if (flags) *flags = v;
+  return v ? DS_ERR_DEVICE_CHECK : DS_OK;
+}
+
+ds_status ds_index_score(const ds_shape* shape, const void* qp, int proxy_dim, const void* label,
+                         int label_heads, const int32_t* page_table, const int32_t* seq_lens,
+                         float* scores, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (proxy_dim != 16 && proxy_dim != 32 && proxy_dim != 64) return DS_ERR_UNSUPPORTED;
+  if (label_heads != 1 && label_heads != shape->num_kv_heads) return DS_ERR_INVALID_ARG;
+  if (!index_score_supported(proxy_dim, label_heads, shape->num_kv_heads,
+                             shape->num_q_heads / shape->num_kv_heads))
+    return DS_ERR_UNSUPPORTED;
+  if (shape->batch == 0 || shape->max_seq_len == 0) return DS_OK;
+  if (!qp || !label || !page_table || !seq_lens || !scores) return DS_ERR_INVALID_ARG;
+  if (!aligned(qp, 16) || !aligned(label, 16) || !aligned(scores, 4)) return DS_ERR_INVALID_ARG;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  ScoreArgs a{qp, label, page_table, seq_lens, scores, err, shape->batch, shape->num_q_heads,
+              shape->num_kv_heads, label_heads, proxy_dim, shape->max_pages_per_req, shape->num_pages,
+              shape->max_seq_len};
+  return from_cuda(launch_index_score(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t ds_topk_workspace_bytes(const ds_shape* shape, int k) {
+  if (check_shape(shape) != DS_OK || k < 0) return 0;
+  return topk_workspace_bytes(shape->batch, shape->num_kv_heads, shape->max_seq_len, k);
+}
+
+ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
+                         int32_t* idx, void* workspace, size_t workspace_bytes, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (k < 0) return DS_ERR_INVALID_ARG;
+  if (shape->batch == 0 || k == 0) return DS_OK;
+  if (!seq_lens || !idx || (shape->max_seq_len > 0 && !scores)) return DS_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || (scores && !aligned(scores, 4))) return DS_ERR_INVALID_ARG;
+  const size_t need = topk_workspace_bytes(shape->batch, shape->num_kv_heads, shape->max_seq_len, k);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
+             shape->max_pages_per_req * shape->page_size, k, workspace};
+  return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static ds_status attn_common(const ds_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                             ds_kv_dtype kv_dtype, const float* k_scale, const float* v_scale,
+                             const int32_t* page_table, const int32_t* seq_lens, const int32_t* idx, int k,
+                             float sm_scale, int num_splits, int split_mode, float* o_part, float* lse_part,
+                             void* out, float* lse, int n_from_seq_len, cudaStream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (kv_dtype != DS_KV_BF16 && kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
+  if (k < 0 || num_splits < 1 || (split_mode != DS_SPLIT_CONTIGUOUS && split_mode != DS_SPLIT_PAGE_INTERLEAVED))
+    return DS_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return DS_ERR_INVALID_ARG;
+  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads)) return DS_ERR_UNSUPPORTED;
+  if (shape->batch == 0) return DS_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || (k > 0 && !idx)) return DS_ERR_INVALID_ARG;
+  if (kv_dtype == DS_KV_FP8_E4M3 && (!k_scale || !v_scale)) return DS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return DS_ERR_INVALID_ARG;
+  if (num_splits == 1) {
+    if (!out || !aligned(out, 4)) return DS_ERR_INVALID_ARG;
+  } else {
+    if (!o_part || !lse_part || !aligned(o_part, 4)) return DS_ERR_INVALID_ARG;
+  }
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  AttnArgs a{q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx, o_part, lse_part, out, lse, err,
+             shape->batch, shape->num_q_heads, shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
+             shape->max_seq_len, k, num_splits, split_mode, kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, sm_scale,
+             n_from_seq_len};
+  return from_cuda(launch_sparse_attn(a, stream));
+}
+
+ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void* k_cache,
+                                const void* v_cache, ds_kv_dtype kv_dtype, const float* k_scale,
+                                const float* v_scale, const int32_t* page_table,
+                                const int32_t* seq_lens, const int32_t* idx, int k, float sm_scale,
+                                int num_splits, ds_split_mode split_mode, float* o_part,
+                                float* lse_part, void* out, float* lse, ds_stream_t stream) {
+  return attn_common(shape, q, k_cache, v_cache, kv_dtype, k_scale, v_scale, page_table, seq_lens, idx, k,
+                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, 0,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_part, const float* lse_part,
+                       void* out, float* lse, ds_stream_t stream) {
+  if (num_splits < 1 || rows < 0 || head_dim <= 0 || head_dim % 4) return DS_ERR_INVALID_ARG;
+  if (rows == 0) return DS_OK;
+  if (!o_part || !lse_part || !out) return DS_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(out, 8) || !aligned(lse_part, 4)) return DS_ERR_INVALID_ARG;
+  return from_cuda(launch_lse_merge(num_splits, rows, head_dim, o_part, lse_part, out, lse,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+struct DecodeLayout {
+  float* scores;
+  void* topk_ws;
+  size_t topk_bytes;
+  float* o_part;
+  float* lse_part;
+  size_t bytes;
+};
+
+DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
+  DecodeLayout L;
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  L.scores = reinterpret_cast<float*>(p + off);
+  off = align256(off + static_cast<size_t>(s->batch) * s->num_kv_heads * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
+  L.topk_ws = p + off;
+  L.topk_bytes = topk_workspace_bytes(s->batch, s->num_kv_heads, s->max_seq_len, k);
+  off = align256(off + L.topk_bytes);
+  const int S = decode_splits(s, k);
+  L.o_part = reinterpret_cast<float*>(p + off);
+  if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * s->head_dim * 4);
+  L.lse_part = reinterpret_cast<float*>(p + off);
+  if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * 4);
+  L.bytes = off;
+  return L;
+}
+
+}  // namespace
+
+size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k) {
+  (void)proxy_dim;
+  if (check_shape(shape) != DS_OK || k < 0) return 0;
+  return decode_layout(shape, k, nullptr).bytes;
+}
+
+ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                           size_t workspace_bytes, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (!args) return DS_ERR_INVALID_ARG;
+  if (args->k < 0) return DS_ERR_INVALID_ARG;
+  if (shape->batch == 0) return DS_OK;
+  if (!args->idx || !args->out) return DS_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(shape, args->k, workspace);
+  if (!workspace || workspace_bytes < L.bytes || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int S = decode_splits(shape, args->k);
+  st = ds_index_score(shape, args->qp, args->proxy_dim, args->label, args->label_heads, args->page_table,
+                      args->seq_lens, L.scores, stream);
+  if (st != DS_OK) return st;
+  st = ds_topk_select(shape, L.scores, args->seq_lens, args->k, args->idx, L.topk_ws, L.topk_bytes, stream);
+  if (st != DS_OK) return st;
+  if (S == 1)
+    return attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
+                       args->page_table, args->seq_lens, args->idx, args->k, args->sm_scale, 1,
+                       DS_SPLIT_CONTIGUOUS, nullptr, nullptr, args->out, args->lse, 1, s);
+  st = attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
+                   args->page_table, args->seq_lens, args->idx, args->k, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
+                   L.o_part, L.lse_part, nullptr, nullptr, 1, s);
+  if (st != DS_OK) return st;
+  return ds_lse_merge(S, shape->batch * shape->num_q_heads, shape->head_dim, L.o_part, L.lse_part, args->out,
+                      args->lse, stream);
+}
+
+}  // extern "C"

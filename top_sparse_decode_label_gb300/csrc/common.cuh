@@ -1,0 +1,118 @@
+// Device helpers shared by the kernels of libdssparse (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace ds {
+
+constexpr int kPage = 64;       // tokens per KV page
+constexpr int kHeadDim = 128;   // D
+constexpr unsigned kFull = 0xffffffffu;
+
+// bf16 pair packed in one 32-bit word -> two fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two e4m3 bytes (low 16 bits of w) -> two fp32 through CUDA's FP8 conversion.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t w) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// 16-byte read-only load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ uint4 ld_nc_na_16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_nc_na_8(const void* p) {
+  uint2 r;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_nc_na_4(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// Order-preserving map float -> uint32: a > b  <=>  key(a) > key(b).
+// -0.0 and +0.0 share one key; every NaN maps to 0, below every number.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  if (x != x) return 0u;
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;                     // -0.0 -> +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Inclusive warp prefix sum.
+__device__ __forceinline__ unsigned warp_incl_scan(unsigned v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned n = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// Exclusive block prefix sum over blockDim.x threads (a multiple of 32, <= 1024).
+// `sh` needs 33 words of shared memory. Returns the exclusive prefix; *total the sum.
+__device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* sh, unsigned* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned inc = warp_incl_scan(v);
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned s = (lane < nw) ? sh[lane] : 0u;
+    unsigned si = warp_incl_scan(s);
+    if (lane < nw) sh[lane] = si - s;
+    if (lane == 31) sh[32] = si;
+  }
+  __syncthreads();
+  unsigned r = sh[warp] + inc - v;
+  if (total) *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+// Transposed butterfly reduction over groups of L consecutive lanes (L a power
+// of two <= 32). Each lane holds N partial sums v[0..N) of the same N
+// quantities; afterwards lane j (= lane % L) holds the full sums of
+// quantities [j*N/L, (j+1)*N/L) in v[0..N/L) when N >= L, or of quantity
+// j*N/L in v[0] when N < L. Each step halves the values a lane keeps, so the
+// shuffle count is about N instead of N*log2(L).
+template <int L, int N>
+__device__ __forceinline__ void transposed_reduce(float (&v)[N]) {
+  const int j = threadIdx.x & (L - 1);
+  int n = N;
+#pragma unroll
+  for (int o = L / 2; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool upper = (j & o) != 0;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < h) {
+          float keep = upper ? v[i + h] : v[i];
+          float send = upper ? v[i] : v[i + h];
+          v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], o);
+    }
+  }
+}
+
+}  // namespace ds

@@ -1,0 +1,65 @@
+// Host-side launchers shared between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ds {
+
+constexpr int kHeadDimSupported = 128;
+constexpr int kPageSupported = 64;
+constexpr long long kDecodeTargetCtas = 320;  // attention CTAs the chained call aims for
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+struct ScoreArgs {
+  const void* qp;          // bf16 [B, Hq, C]
+  const void* label;       // bf16 [slots, HL, C]
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  float* scores;           // [B, Hkv, Tmax]
+  unsigned* err;
+  int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
+};
+// Returns a cudaError_t; cudaErrorNotSupported for shapes without a kernel.
+cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream);
+bool index_score_supported(int C, int HL, int Hkv, int G);
+
+struct TopkArgs {
+  const float* scores;     // [B, Hkv, Tmax]
+  const int32_t* seq_lens;
+  int32_t* idx;            // [B, Hkv, k]
+  unsigned* err;
+  int B, Hkv, Tmax, maxp_tokens, k;
+  void* ws;
+};
+size_t topk_workspace_bytes(int B, int Hkv, int Tmax, int k);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  const void* q;           // bf16 [B, Hq, D]
+  const void* k_cache;     // [slots, Hkv, D]
+  const void* v_cache;
+  const float* k_scale;    // [num_pages] (fp8)
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* idx;      // [B, Hkv, k]
+  float* o_part;           // [S, B, Hq, D] (S > 1)
+  float* lse_part;         // [S, B, Hq]
+  void* out;               // bf16 [B, Hq, D] (S == 1)
+  float* lse;              // [B, Hq] (S == 1, may be null)
+  unsigned* err;
+  int B, Hq, Hkv, maxp, num_pages, Tmax, k, S, split_mode, fp8;
+  float sm_scale;
+  int n_from_seq_len;      // 1: each idx row holds exactly min(k, seq_len) valid entries (top-k output)
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+bool sparse_attn_supported(int G);
+
+cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const float* lse_part,
+                             void* out, float* lse, cudaStream_t stream);
+
+}  // namespace ds
