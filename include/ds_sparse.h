@@ -204,6 +204,13 @@ size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k);
 ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
                            size_t workspace_bytes, ds_stream_t stream);
 
+/*
+ * Kernel launches one ds_sparse_decode call makes for this shape and k (not
+ * counting the one cudaMemsetAsync of the top-k counters); 0 when the
+ * arguments are invalid or there is nothing to do. Host-only query.
+ */
+int ds_decode_kernel_launches(const ds_shape* shape, int k);
+
 /* Human-readable name of a status. */
 const char* ds_error_string(ds_status status);
 

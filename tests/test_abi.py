@@ -9,12 +9,13 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "ds_sparse.h")
+pytestmark = pytest.mark.usefixtures("lib")
 
 
 @pytest.fixture(scope="module")
 def lib():
-    from top_sparse_decode_label_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 

@@ -189,7 +189,7 @@ def test_attention_with_padded_and_empty_rows():
     w = workload("pad", 3, 8, 2, [100, 0, 37], 32, 2, 64)
     inp = dsgen.make_inputs(w)
     _, idx, _, _ = oracle.decode(inp)
-    assert (idx[0] == -1).any() and (idx[1] == -1).all()
+    assert (idx[2] == -1).any() and (idx[1] == -1).all() and not (idx[0] == -1).any()
     g = inp.to(DEV)
     out = torch.full((3, 8, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.full((3, 8), float("nan"), device=DEV)

@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_workspace_bytes",
     "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes",
-    "ds_device_errors", "lib", "LIB_PATH",
+    "ds_device_errors", "ds_decode_kernel_launches", "lib", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdssparse.so")
@@ -73,6 +73,8 @@ def lib():
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
         L.ds_decode_workspace_bytes.restype = Z
         L.ds_sparse_decode.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P]
+        L.ds_decode_kernel_launches.argtypes = [SP, I]
+        L.ds_decode_kernel_launches.restype = I
         L.ds_error_string.argtypes = [I]
         L.ds_error_string.restype = ctypes.c_char_p
         L.ds_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -172,6 +174,11 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().ds_sparse_decode(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes, _stream(stream)),
            "ds_sparse_decode")
+
+
+def ds_decode_kernel_launches(shape: Shape, k: int) -> int:
+    """Kernel launches one chained call makes (host-only query)."""
+    return lib().ds_decode_kernel_launches(ctypes.byref(shape), k)
 
 
 def ds_device_errors() -> int:

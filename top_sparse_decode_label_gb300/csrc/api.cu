@@ -246,6 +246,16 @@ size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k) {
   return decode_layout(shape, k, nullptr).bytes;
 }
 
+int ds_decode_kernel_launches(const ds_shape* shape, int k) {
+  if (check_shape(shape) != DS_OK || k < 0 || shape->batch == 0) return 0;
+  int n = 0;
+  if (shape->max_seq_len > 0) n += 1;                 // scoring
+  if (k > 0) n += (shape->max_seq_len > 0 ? 2 : 0) + 1;  // histogram, filter, select
+  n += 1;                                             // attention
+  if (decode_splits(shape, k) > 1) n += 1;            // merge
+  return n;
+}
+
 ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
                            size_t workspace_bytes, ds_stream_t stream) {
   ds_status st = check_shape(shape);
