@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step of top-k sparse attention on GB300.
+
+A step is one call of the chained C entry point ds_sparse_decode (score every
+cached token -> exact top-k -> sparse GQA attention over the selected tokens ->
+log-sum-exp merge) over one batch of seeded synthetic inputs that are already
+resident in HBM. The default workload is the Llama-3.1-8B-shaped
+Double-Sparsity decode (batch 3, 32 query / 8 KV heads, 60000 tokens per
+request, 32 K-channel label cache, top-k 3000, bf16 KV); --config selects
+another one of dsgen.WORKLOADS.
+
+Printed: one JSON line with calls/s (value), the achieved HBM bandwidth of the
+step and of its dominant kernel against the measured copy bandwidth, the
+end-to-end number through the C ABI with host<->device copies, the oracle's CPU
+time on a bounded sample, clocks sampled during the timed region, and the
+number of kernel launches.
+
+Timing: W untimed warm-up steps, then exactly K timed steps; L2 is flushed
+(a 256 MiB device write) before every timed step, outside the CUDA events
+that bracket each step on the launching stream. Under torchrun each rank runs
+its own replica (weak scaling, no collective on the data path) and the
+slowest rank's time is used.
+
+`--impl reference` times the oracle (plain single-threaded C++ on the host
+cores) on the same workload instead, one (request, KV head) row per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import dsgen  # noqa: E402
+
+METRIC = "sparse-decode attn calls/s + achieved HBM GB/s vs ~8 TB/s roofline, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="index into dsgen.WORKLOADS")
+    ap.add_argument("--flush-mib", type=int, default=256)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle time budget of the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def alg_bytes(w: dsgen.Workload) -> dict:
+    """Algorithmic bytes of one call: what the method must move, per stage."""
+    elt = 1 if w.kv_dtype == "fp8_e4m3" else 2
+    scan = sum(T * w.label_heads * w.proxy_dim * 2 for T in w.seq_lens)
+    pages = sum(-(-T // w.page_size) * 4 for T in w.seq_lens)
+    keff = [min(w.top_k, T) for T in w.seq_lens]
+    kv = sum(k * w.num_kv_heads * w.head_dim * elt * 2 for k in keff)
+    scales = sum(k * w.num_kv_heads * 8 for k in keff) if elt == 1 else 0
+    q = w.batch * w.num_q_heads * (w.head_dim + w.proxy_dim) * 2
+    out = w.batch * w.num_q_heads * (w.head_dim * 2 + 4) + w.batch * w.num_kv_heads * w.top_k * 4
+    return dict(scan=scan, page_table=pages, kv_rows=kv + scales, q=q, out=out,
+                total=scan + pages + kv + scales + q + out)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def traffic_record(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "top_sparse_decode_label_gb300", "csrc", kernel_file)
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload, {}).get(kernel_file)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if rec and rec.get("source_sha") == sha:
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, timestamped on arrival."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]),
+                                     [n for n, v in zip(self.NAMES, parts[4:8]) if v.lower().startswith("active")]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        use = inside
+        if len(inside) < 3:
+            use = [s for s in self.samples if s[0] <= t1]
+            window = "soak+timed (timed region shorter than the sampling interval)"
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        reasons = sorted({r for s in use for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": max(s[2] for s in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_row_seconds(inp_cpu, budget_s: float, max_rows: int = None):
+    """Time the oracle on whole (request, KV head) rows until the budget is spent.
+
+    Returns (mean seconds per row, rows timed, threads used).
+    """
+    import oracle
+    w = inp_cpu.w
+    rows = [(b, g) for b in range(w.batch) for g in range(w.num_kv_heads)]
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    times = []
+    try:
+        i = 0
+        t_start = time.perf_counter()
+        while True:
+            b, g = rows[i % len(rows)]
+            mask = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.uint8)
+            mask[b, g] = 1
+            t0 = time.perf_counter()
+            oracle.decode(inp_cpu, row_mask=mask)
+            times.append(time.perf_counter() - t0)
+            i += 1
+            if max_rows is not None and i >= max_rows:
+                break
+            if time.perf_counter() - t_start >= budget_s and i >= 1:
+                break
+    finally:
+        torch.set_num_threads(prev)
+    return sum(times) / len(times), len(times), 1
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    import oracle
+    w = dsgen.WORKLOADS[args.config]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = dsgen.make_inputs(w, device=dev).to("cpu")
+    rows_per_call = w.batch * w.num_kv_heads
+    rows = [(b, g) for b in range(w.batch) for g in range(w.num_kv_heads)]
+    torch.set_num_threads(1)
+
+    def step(i):
+        b, g = rows[i % len(rows)]
+        mask = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.uint8)
+        mask[b, g] = 1
+        oracle.decode(inp, row_mask=mask)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    calls_per_s = args.steps / dt / rows_per_call
+    sample = (f"{args.steps} steps, each one (request, KV head) row of the call ({rows_per_call} rows per call): "
+              f"proxy scores of the row, its top-k, attention of its {w.group} query heads, merge")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.max_seq_len, "top_k": w.top_k},
+        "cpu_baseline": {"value": calls_per_s, "unit": "calls/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": calls_per_s, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import top_sparse_decode_label_gb300 as ds
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = dsgen.WORKLOADS[args.config]
+    inp = dsgen.make_inputs(w, device=dev)
+    shape = ds.Shape(**dsgen.shape_kwargs(inp))
+    k = w.top_k
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    stream = torch.cuda.current_stream(dev)
+
+    idx = torch.empty((B, Hkv, k), dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(ds.ds_decode_workspace_bytes(shape, w.proxy_dim, k), dtype=torch.uint8, device=dev)
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        ds.ds_sparse_decode(shape, inp.q, inp.qp, inp.label, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                            inp.page_table, inp.seq_lens, k, idx, out, lse, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ds.ds_device_errors() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = "GPU-" + str(props.uuid) if getattr(props, "uuid", None) is not None else str(local)
+    sampler = ClockSampler(gpu_id)
+    # Untimed soak so that the clock record covers the timed region even when it is short.
+    t_soak = time.time()
+    while time.time() - t_soak < 1.0:
+        for _ in range(50):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K chained calls, L2 flushed before each.
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    calls_per_s = world * args.steps / total_s
+    ms_per_step = total_s / args.steps * 1e3
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if ds.ds_device_errors() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # ---- per-stage breakdown: the same kernels through the four stage entry points.
+    S = ds.ds_decode_num_splits(shape, k)
+    scores = torch.empty((B, Hkv, w.max_seq_len), dtype=torch.float32, device=dev)
+    tws = torch.empty(max(1, ds.ds_topk_workspace_bytes(shape, k)), dtype=torch.uint8, device=dev)
+    o_part = torch.empty((S, B, Hq, D), dtype=torch.float32, device=dev) if S > 1 else None
+    l_part = torch.empty((S, B, Hq), dtype=torch.float32, device=dev) if S > 1 else None
+    nstage = min(args.steps, 500)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nstage)]
+    for i in range(nstage):
+        flush.zero_()
+        e = evs[i]
+        e[0].record(stream)
+        ds.ds_index_score(shape, inp.qp, inp.label, inp.page_table, inp.seq_lens, scores, stream=stream)
+        e[1].record(stream)
+        ds.ds_topk_select(shape, scores, inp.seq_lens, k, idx, tws, stream=stream)
+        e[2].record(stream)
+        if S > 1:
+            ds.ds_sparse_decode_attn(shape, inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                                     inp.page_table, inp.seq_lens, idx, num_splits=S, o_part=o_part,
+                                     lse_part=l_part, stream=stream)
+            e[3].record(stream)
+            ds.ds_lse_merge(o_part, l_part, out, lse, stream=stream)
+        else:
+            ds.ds_sparse_decode_attn(shape, inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                                     inp.page_table, inp.seq_lens, idx, out=out, lse=lse, stream=stream)
+            e[3].record(stream)
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    stage_us = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nstage)) * 1e3
+                for j, name in enumerate(["index_score", "topk_select", "sparse_attn", "lse_merge"])}
+
+    # ---- end to end through the C ABI: per-step inputs from pinned host memory, results back.
+    h_q = inp.q.cpu().pin_memory()
+    h_qp = inp.qp.cpu().pin_memory()
+    h_pt = inp.page_table.cpu().pin_memory()
+    h_sl = inp.seq_lens.cpu().pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h_lse = torch.empty_like(lse, device="cpu").pin_memory()
+    h_idx = torch.empty_like(idx, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qp, h_pt, h_sl))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_idx))
+    ee0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ee0[i].record(stream)
+        inp.q.copy_(h_q, non_blocking=True)
+        inp.qp.copy_(h_qp, non_blocking=True)
+        inp.page_table.copy_(h_pt, non_blocking=True)
+        inp.seq_lens.copy_(h_sl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        ee1[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(ee0, ee1)) / 1e3, world)
+    e2e_value = world * args.steps / e2e_s
+
+    # ---- roofline
+    peak, peak_src = measured_peak()
+    ab = alg_bytes(w)
+    step_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
+    dominant = max(stage_us, key=stage_us.get)
+    if dominant == "index_score":
+        dom_bytes = ab["scan"] + ab["page_table"] + w.batch * w.num_q_heads * w.proxy_dim * 2
+        dom_file = "score.cu"
+    elif dominant == "sparse_attn":
+        dom_bytes = ab["kv_rows"] + ab["q"] + w.batch * w.num_kv_heads * w.top_k * 4
+        dom_file = "attn.cu"
+    else:
+        dom_bytes = 2 * sum(T * 4 for T in w.seq_lens) * w.num_kv_heads
+        dom_file = "topk.cu"
+    dom_gbs = dom_bytes / (stage_us[dominant] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                "frac": dom_gbs / peak, "traffic": traffic_record(dom_file, w.name),
+                "alg_bytes_per_launch": dom_bytes, "avg_launch_us": stage_us[dominant], "peak_source": peak_src}
+
+    line = {
+        "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "seq_len": w.max_seq_len, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "proxy_dim": w.proxy_dim, "label_heads": w.label_heads,
+                   "top_k": k, "kv_dtype": w.kv_dtype, "page_size": w.page_size,
+                   "l2": f"flushed ({args.flush_mib} MiB device write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": calls_per_s * B, "scanned_tokens_per_s": calls_per_s * sum(w.seq_lens),
+        "step_hbm": {"alg_bytes_per_call": ab["total"], "bytes_breakdown": ab, "achieved_gbs": step_gbs,
+                     "frac_of_peak": step_gbs / peak},
+        "stage_us": stage_us, "internal_splits": S,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "what": "H2D of q, qp, page_table, seq_lens from pinned host memory; the chained call; "
+                        "D2H of out, lse, idx; KV and label caches stay resident"},
+        "clocks": clocks,
+        "gpu_launches": args.steps * ds.ds_decode_kernel_launches(shape, k),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec_row, nrows, cores = oracle_row_seconds(inp.to("cpu"), args.cpu_budget_s)
+        rows_per_call = B * Hkv
+        line["cpu_baseline"] = {"value": 1.0 / (sec_row * rows_per_call), "unit": "calls/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{nrows} (request, KV head) rows of the {rows_per_call}-row call, "
+                                          f"each scored, top-k selected and attended by the oracle; "
+                                          f"{sec_row * 1e3:.1f} ms per row"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -211,6 +211,12 @@ ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, vo
  */
 int ds_decode_kernel_launches(const ds_shape* shape, int k);
 
+/*
+ * Split-KV count the chained call uses internally for this shape and k (so a
+ * caller running the four stages one by one can reproduce it). Host-only.
+ */
+int ds_decode_num_splits(const ds_shape* shape, int k);
+
 /* Human-readable name of a status. */
 const char* ds_error_string(ds_status status);
 

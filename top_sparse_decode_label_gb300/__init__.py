@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_workspace_bytes",
     "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes",
-    "ds_device_errors", "ds_decode_kernel_launches", "lib", "LIB_PATH",
+    "ds_device_errors", "ds_decode_kernel_launches", "ds_decode_num_splits", "lib", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdssparse.so")
@@ -73,6 +73,8 @@ def lib():
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
         L.ds_decode_workspace_bytes.restype = Z
         L.ds_sparse_decode.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P]
+        L.ds_decode_num_splits.argtypes = [SP, I]
+        L.ds_decode_num_splits.restype = I
         L.ds_decode_kernel_launches.argtypes = [SP, I]
         L.ds_decode_kernel_launches.restype = I
         L.ds_error_string.argtypes = [I]
@@ -179,6 +181,11 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
 def ds_decode_kernel_launches(shape: Shape, k: int) -> int:
     """Kernel launches one chained call makes (host-only query)."""
     return lib().ds_decode_kernel_launches(ctypes.byref(shape), k)
+
+
+def ds_decode_num_splits(shape: Shape, k: int) -> int:
+    """Split-KV count the chained call uses internally (host-only query)."""
+    return lib().ds_decode_num_splits(ctypes.byref(shape), k)
 
 
 def ds_device_errors() -> int:

@@ -246,6 +246,11 @@ size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k) {
   return decode_layout(shape, k, nullptr).bytes;
 }
 
+int ds_decode_num_splits(const ds_shape* shape, int k) {
+  if (check_shape(shape) != DS_OK || k < 0) return 0;
+  return decode_splits(shape, k);
+}
+
 int ds_decode_kernel_launches(const ds_shape* shape, int k) {
   if (check_shape(shape) != DS_OK || k < 0 || shape->batch == 0) return 0;
   int n = 0;
