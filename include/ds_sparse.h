@@ -126,6 +126,29 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
                          int32_t* idx, void* workspace, size_t workspace_bytes, ds_stream_t stream);
 
 /*
+ * ds_topk_select without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin whose host framework owns every device
+ * allocation and passes in only the call's tensors, code running while a CUDA
+ * graph is being captured around it (where entering an allocator is not
+ * allowed), or a latency-critical serving thread that must not wait on an
+ * allocator lock. The pages describe no such entry point; it exists for
+ * these callers only. Same arguments and results as ds_topk_select.
+ *
+ * Scratch comes from an array of DS_TOPK_STATIC_SCRATCH_BYTES (16 MiB)
+ * compiled into the library; each GPU that loads the library holds one until
+ * the process exits. A (shape, k) needing more scratch than that (see
+ * ds_topk_workspace_bytes) returns DS_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the one array, so calls whose work overlaps on the
+ * GPU (other streams, other host threads) race and corrupt each other's
+ * results: serialise them. Nothing is allocated or freed.
+ */
+#define DS_TOPK_STATIC_SCRATCH_BYTES (16u << 20)
+ds_status ds_topk_select_static(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
+                                int32_t* idx, ds_stream_t stream);
+
+/*
  * Stage 3: sparse GQA decode attention over the selected tokens (PR #1459
  * sparse decode attention; PR #39721 sparse_gqa; FP8 E4M3 paged KV of the
  * QSA HiSparse plugin).

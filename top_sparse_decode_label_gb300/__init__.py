@@ -16,7 +16,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_workspace_bytes",
+    "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_select_static", "ds_topk_workspace_bytes",
     "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes",
     "ds_device_errors", "ds_decode_kernel_launches", "ds_decode_num_splits", "lib", "LIB_PATH",
 ]
@@ -68,6 +68,8 @@ def lib():
         L.ds_topk_workspace_bytes.argtypes = [SP, I]
         L.ds_topk_workspace_bytes.restype = Z
         L.ds_topk_select.argtypes = [SP, P, P, I, P, P, Z, P]
+        L.ds_topk_select_static.argtypes = [SP, P, P, I, P, P]
+        L.ds_topk_select_static.restype = I
         L.ds_sparse_decode_attn.argtypes = [SP, P, P, P, I, P, P, P, P, P, I, ctypes.c_float, I, I, P, P, P, P, P]
         L.ds_lse_merge.argtypes = [I, I, I, P, P, P, P, P]
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
@@ -135,6 +137,17 @@ def ds_topk_select(shape: Shape, scores, seq_lens, k: int, idx, workspace, strea
     _check(lib().ds_topk_select(ctypes.byref(shape), _p(scores), _p(seq_lens), k, _p(idx), _p(workspace),
                                 workspace.numel() * workspace.element_size() if workspace is not None else 0,
                                 _stream(stream)), "ds_topk_select")
+
+
+def ds_topk_select_static(shape: Shape, scores, seq_lens, k: int, idx, stream=None) -> None:
+    """ds_topk_select with the library's fixed 16 MiB device scratch instead of a workspace.
+
+    For callers that cannot allocate device memory. Calls that overlap on the
+    GPU share the scratch and race; the first call on a device should come
+    before any stream capture.
+    """
+    _check(lib().ds_topk_select_static(ctypes.byref(shape), _p(scores), _p(seq_lens), k, _p(idx), _stream(stream)),
+           "ds_topk_select_static")
 
 
 def ds_sparse_decode_attn(shape: Shape, q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx,
