@@ -219,13 +219,27 @@ typedef struct {
  * The whole decode step: ds_index_score -> ds_topk_select ->
  * ds_sparse_decode_attn (internal split-KV chosen for occupancy) ->
  * ds_lse_merge, on one stream, with scores and partials in `workspace`
- * (at least ds_decode_workspace_bytes bytes, 256-byte aligned, no
- * initialisation needed). No host synchronisation and no allocation, so the
- * call can be captured in a CUDA graph and replayed with new input contents.
+ * (at least ds_decode_workspace_bytes bytes, 256-byte aligned). The
+ * workspace holds completion counters and histograms that must be zero
+ * before its first use (e.g. cudaMemsetAsync(workspace, 0, bytes) once);
+ * every call leaves them zero again, so it is reused without clearing. Calls
+ * sharing one workspace must not overlap on the GPU. No host synchronisation
+ * and no allocation, so the call can be captured in a CUDA graph and replayed
+ * with new input contents.
  */
 size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k);
 ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
                            size_t workspace_bytes, ds_stream_t stream);
+
+/*
+ * ds_sparse_decode, instrumented: when `events` is not NULL it must hold four
+ * created cudaEvent_t handles, recorded on `stream` before the scoring stage,
+ * after it, after the top-k stage and after the attention stage (which
+ * includes the fused merge), so a caller can time each stage of the very
+ * same launches. Results and requirements are those of ds_sparse_decode.
+ */
+ds_status ds_sparse_decode_profiled(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                                    size_t workspace_bytes, ds_stream_t stream, void* const* events);
 
 /*
  * Kernel launches one ds_sparse_decode call makes for this shape and k (not

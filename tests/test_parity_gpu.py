@@ -258,7 +258,7 @@ def test_replay_after_input_mutation_reuses_workspace():
     b = dsgen.make_inputs(w, seed=22)
     ga = a.to(DEV)
     shape = shape_of(a)
-    ws = torch.empty(_ds().ds_decode_workspace_bytes(shape, w.proxy_dim, w.top_k), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(_ds().ds_decode_workspace_bytes(shape, w.proxy_dim, w.top_k), dtype=torch.uint8, device=DEV)
     idx = torch.empty((w.batch, w.num_kv_heads, w.top_k), dtype=torch.int32, device=DEV)
     out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((w.batch, w.num_q_heads), device=DEV)

@@ -75,6 +75,8 @@ def lib():
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
         L.ds_decode_workspace_bytes.restype = Z
         L.ds_sparse_decode.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P]
+        L.ds_sparse_decode_profiled.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P, ctypes.POINTER(P)]
+        L.ds_sparse_decode_profiled.restype = ctypes.c_int
         L.ds_decode_num_splits.argtypes = [SP, I]
         L.ds_decode_num_splits.restype = I
         L.ds_decode_kernel_launches.argtypes = [SP, I]
@@ -178,8 +180,14 @@ def ds_decode_workspace_bytes(shape: Shape, proxy_dim: int, k: int) -> int:
 
 def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
                      k: int, idx, out, lse=None, workspace=None, sm_scale: Optional[float] = None,
-                     stream=None) -> None:
-    """The chained decode step (ds_sparse_decode): idx, out and lse from the caches and queries."""
+                     stream=None, events=None) -> None:
+    """The chained decode step (ds_sparse_decode): idx, out and lse from the caches and queries.
+
+    ``workspace`` must be zero-filled before its first use (torch.zeros); the
+    call leaves it zero-filled again. With ``events`` (four recorded
+    torch.cuda.Event objects) the instrumented entry point records them before
+    scoring and after scoring, top-k and attention.
+    """
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(shape.head_dim)
     a = DecodeArgs(q=_p(q), qp=_p(qp), proxy_dim=qp.shape[-1], label=_p(label), label_heads=label.shape[1],
@@ -187,13 +195,13 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
                    v_scale=_p(v_scale), page_table=_p(page_table), seq_lens=_p(seq_lens), k=k,
                    sm_scale=float(sm_scale), idx=_p(idx), out=_p(out), lse=_p(lse))
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().ds_sparse_decode(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes, _stream(stream)),
-           "ds_sparse_decode")
-
-
-def ds_decode_kernel_launches(shape: Shape, k: int) -> int:
-    """Kernel launches one chained call makes (host-only query)."""
-    return lib().ds_decode_kernel_launches(ctypes.byref(shape), k)
+    if events is None:
+        st = lib().ds_sparse_decode(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes, _stream(stream))
+    else:
+        handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        st = lib().ds_sparse_decode_profiled(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes,
+                                             _stream(stream), handles)
+    _check(st, "ds_sparse_decode")
 
 
 def ds_decode_num_splits(shape: Shape, k: int) -> int:

@@ -138,7 +138,7 @@ ds_status ds_index_score(const ds_shape* shape, const void* qp, int proxy_dim, c
 
 size_t ds_topk_workspace_bytes(const ds_shape* shape, int k) {
   if (check_shape(shape) != DS_OK || k < 0) return 0;
-  return topk_workspace_bytes(shape->batch, shape->num_kv_heads, shape->max_seq_len, k);
+  return topk_layout(nullptr, shape->batch * shape->num_kv_heads, shape->max_seq_len).bytes;
 }
 
 ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
@@ -149,12 +149,12 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
   if (shape->batch == 0 || k == 0) return DS_OK;
   if (!seq_lens || !idx || (shape->max_seq_len > 0 && !scores)) return DS_ERR_INVALID_ARG;
   if (!aligned(idx, 4) || (scores && !aligned(scores, 4))) return DS_ERR_INVALID_ARG;
-  const size_t need = topk_workspace_bytes(shape->batch, shape->num_kv_heads, shape->max_seq_len, k);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  const TopkLayout L = topk_layout(workspace, shape->batch * shape->num_kv_heads, shape->max_seq_len);
+  if (!workspace || workspace_bytes < L.bytes || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-             shape->max_pages_per_req * shape->page_size, k, workspace};
+             shape->max_pages_per_req * shape->page_size, k, L, false};
   return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -162,7 +162,8 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
                              ds_kv_dtype kv_dtype, const float* k_scale, const float* v_scale,
                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* idx, int k,
                              float sm_scale, int num_splits, int split_mode, float* o_part, float* lse_part,
-                             void* out, float* lse, int n_from_seq_len, cudaStream_t stream) {
+                             void* out, float* lse, int n_from_seq_len, unsigned* merge_done,
+                             cudaStream_t stream) {
   ds_status st = check_shape(shape);
   if (st != DS_OK) return st;
   if (kv_dtype != DS_KV_BF16 && kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
@@ -174,9 +175,10 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || (k > 0 && !idx)) return DS_ERR_INVALID_ARG;
   if (kv_dtype == DS_KV_FP8_E4M3 && (!k_scale || !v_scale)) return DS_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return DS_ERR_INVALID_ARG;
-  if (num_splits == 1) {
+  if (num_splits == 1 || merge_done) {
     if (!out || !aligned(out, 4)) return DS_ERR_INVALID_ARG;
-  } else {
+  }
+  if (num_splits > 1) {
     if (!o_part || !lse_part || !aligned(o_part, 4)) return DS_ERR_INVALID_ARG;
   }
   unsigned* err = error_word();
@@ -184,7 +186,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   AttnArgs a{q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx, o_part, lse_part, out, lse, err,
              shape->batch, shape->num_q_heads, shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
              shape->max_seq_len, k, num_splits, split_mode, kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, sm_scale,
-             n_from_seq_len};
+             n_from_seq_len, merge_done};
   return from_cuda(launch_sparse_attn(a, stream));
 }
 
@@ -195,7 +197,7 @@ ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void
                                 int num_splits, ds_split_mode split_mode, float* o_part,
                                 float* lse_part, void* out, float* lse, ds_stream_t stream) {
   return attn_common(shape, q, k_cache, v_cache, kv_dtype, k_scale, v_scale, page_table, seq_lens, idx, k,
-                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, 0,
+                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, 0, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -211,29 +213,34 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
 
 namespace {
 
+// Workspace of the chained call. The top-k counters and histograms and the
+// merge counters must be zero before the first call; every call leaves them
+// zero again.
 struct DecodeLayout {
   float* scores;
-  void* topk_ws;
-  size_t topk_bytes;
+  TopkLayout topk;
   float* o_part;
   float* lse_part;
+  unsigned* merge_done;
   size_t bytes;
 };
 
 DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
   DecodeLayout L;
   char* p = static_cast<char*>(base);
+  const int R = s->batch * s->num_kv_heads;
   size_t off = 0;
   L.scores = reinterpret_cast<float*>(p + off);
-  off = align256(off + static_cast<size_t>(s->batch) * s->num_kv_heads * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
-  L.topk_ws = p + off;
-  L.topk_bytes = topk_workspace_bytes(s->batch, s->num_kv_heads, s->max_seq_len, k);
-  off = align256(off + L.topk_bytes);
+  off = align256(off + static_cast<size_t>(R) * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
+  L.topk = topk_layout(p + off, R, s->max_seq_len);
+  off = align256(off + L.topk.bytes);
   const int S = decode_splits(s, k);
   L.o_part = reinterpret_cast<float*>(p + off);
   if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * s->head_dim * 4);
   L.lse_part = reinterpret_cast<float*>(p + off);
   if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * 4);
+  L.merge_done = reinterpret_cast<unsigned*>(p + off);
+  off = align256(off + static_cast<size_t>(R) * 4);
   L.bytes = off;
   return L;
 }
@@ -254,40 +261,68 @@ int ds_decode_num_splits(const ds_shape* shape, int k) {
 int ds_decode_kernel_launches(const ds_shape* shape, int k) {
   if (check_shape(shape) != DS_OK || k < 0 || shape->batch == 0) return 0;
   int n = 0;
-  if (shape->max_seq_len > 0) n += 1;                 // scoring
-  if (k > 0) n += (shape->max_seq_len > 0 ? 2 : 0) + 1;  // histogram, filter, select
-  n += 1;                                             // attention
-  if (decode_splits(shape, k) > 1) n += 1;            // merge
+  if (shape->max_seq_len > 0) n += 1;  // scoring (with the level-1 histograms)
+  if (k > 0) n += 1;                   // filter + select
+  n += 1;                              // attention (with the merge when split)
   return n;
 }
 
-ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
-                           size_t workspace_bytes, ds_stream_t stream) {
+static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                             size_t workspace_bytes, ds_stream_t stream, void* const* events) {
   ds_status st = check_shape(shape);
   if (st != DS_OK) return st;
   if (!args) return DS_ERR_INVALID_ARG;
   if (args->k < 0) return DS_ERR_INVALID_ARG;
   if (shape->batch == 0) return DS_OK;
-  if (!args->idx || !args->out) return DS_ERR_INVALID_ARG;
+  if (!args->idx || !args->out || !aligned(args->idx, 4)) return DS_ERR_INVALID_ARG;
   const DecodeLayout L = decode_layout(shape, args->k, workspace);
   if (!workspace || workspace_bytes < L.bytes || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  const int pd = args->proxy_dim;
+  if (pd != 16 && pd != 32 && pd != 64) return DS_ERR_UNSUPPORTED;
+  if (args->label_heads != 1 && args->label_heads != shape->num_kv_heads) return DS_ERR_INVALID_ARG;
+  if (!index_score_supported(pd, args->label_heads, shape->num_kv_heads, shape->num_q_heads / shape->num_kv_heads))
+    return DS_ERR_UNSUPPORTED;
+  if (!args->qp || !args->label || !args->page_table || !args->seq_lens) return DS_ERR_INVALID_ARG;
+  if (!aligned(args->qp, 16) || !aligned(args->label, 16)) return DS_ERR_INVALID_ARG;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int S = decode_splits(shape, args->k);
-  st = ds_index_score(shape, args->qp, args->proxy_dim, args->label, args->label_heads, args->page_table,
-                      args->seq_lens, L.scores, stream);
-  if (st != DS_OK) return st;
-  st = ds_topk_select(shape, L.scores, args->seq_lens, args->k, args->idx, L.topk_ws, L.topk_bytes, stream);
-  if (st != DS_OK) return st;
-  if (S == 1)
-    return attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
-                       args->page_table, args->seq_lens, args->idx, args->k, args->sm_scale, 1,
-                       DS_SPLIT_CONTIGUOUS, nullptr, nullptr, args->out, args->lse, 1, s);
+  const int k = args->k;
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  if (mark(0) != cudaSuccess) return DS_ERR_CUDA;
+  if (shape->max_seq_len > 0) {
+    ScoreArgs sa{args->qp, args->label, args->page_table, args->seq_lens, L.scores, err, shape->batch,
+                 shape->num_q_heads, shape->num_kv_heads, args->label_heads, pd, shape->max_pages_per_req,
+                 shape->num_pages, shape->max_seq_len, k > 0 ? &L.topk : nullptr, k};
+    st = from_cuda(launch_index_score(sa, s));
+    if (st != DS_OK) return st;
+  }
+  if (mark(1) != cudaSuccess) return DS_ERR_CUDA;
+  if (k > 0) {
+    TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
+                shape->max_pages_per_req * shape->page_size, k, L.topk, true};
+    st = from_cuda(launch_topk(ta, s));
+    if (st != DS_OK) return st;
+  }
+  if (mark(2) != cudaSuccess) return DS_ERR_CUDA;
   st = attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
-                   args->page_table, args->seq_lens, args->idx, args->k, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
-                   L.o_part, L.lse_part, nullptr, nullptr, 1, s);
+                   args->page_table, args->seq_lens, args->idx, k, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
+                   L.o_part, L.lse_part, args->out, args->lse, 1, S > 1 ? L.merge_done : nullptr, s);
   if (st != DS_OK) return st;
-  return ds_lse_merge(S, shape->batch * shape->num_q_heads, shape->head_dim, L.o_part, L.lse_part, args->out,
-                      args->lse, stream);
+  return mark(3) == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                           size_t workspace_bytes, ds_stream_t stream) {
+  return decode_impl(shape, args, workspace, workspace_bytes, stream, nullptr);
+}
+
+ds_status ds_sparse_decode_profiled(const ds_shape* shape, const ds_decode_args* args, void* workspace,
+                                    size_t workspace_bytes, ds_stream_t stream, void* const* events) {
+  return decode_impl(shape, args, workspace, workspace_bytes, stream, events);
 }
 
 }  // extern "C"

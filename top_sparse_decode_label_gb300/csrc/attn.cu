@@ -1,25 +1,28 @@
 // Stage 3: sparse GQA decode attention over the selected tokens, gathered
-// from a paged bf16 or FP8-E4M3 KV cache.
+// from a paged bf16 or FP8-E4M3 KV cache, with the log-sum-exp merge of the
+// split partials optionally fused into the last CTA of each (request, KV head).
 //
 // "Support double sparsity" (sglang PR #1459): attention over the heavy
 // tokens only. sglang PR #39721: sparse_gqa over the indexer's selection.
 // "QSA HiSparse - SGLang plugin", "Supported versions": FP8 E4M3 KV cache with
 // page size 64 (here with one fp32 scale per physical page for K and for V).
-// sglang PR #43527, "Distributed QSA execution": owner-side partial outputs,
-// merged later by log-sum-exp.
+// sglang PR #43527, "Distributed QSA execution": owner-side partial outputs
+// merged with FP32 log-sum-exp normalisation.
 //
-// One CTA per (request b, KV head g, split j); 4 warps. Each warp takes tiles
-// of 32 selected positions: lane l resolves the slot of position l (index ->
-// page table -> slot), then the warp walks the tile in sub-tiles of J tokens.
-// A K or V row (D = 128) is read by the whole warp in one coalesced
-// instruction (8 B bf16 or 4 B e4m3 per lane: dims 4l..4l+3). The G query
-// heads of the group are in registers (4 dims per lane, pre-scaled by
-// sm_scale * log2 e), so a lane forms J x G partial dot products; a transposed
-// butterfly leaves one finished logit per lane. Online softmax keeps per-head
-// running max and sum; P.V accumulates into 4 dims x G heads per lane. At the
-// end the warps' states are combined in shared memory (the same log-sum-exp
-// merge as stage 4) and the CTA writes either the final bf16 output (one
-// split) or fp32 partials.
+// One CTA per (request b, KV head g, split j), 4 warps. The CTA first
+// resolves the physical slot (index -> page table -> slot) of every selected
+// token of its chunk into shared memory, in order, with one prefix sum. The
+// K and V rows of those slots are then gathered in tiles of 32 tokens
+// through a ring of cp.async stages (16-byte copies; a bf16 row is 256 B,
+// an e4m3 row 128 B), so the gather keeps many rows in flight per SM. Each
+// warp takes 8 tokens of a tile: one K or V row is read by the whole warp in
+// one conflict-free shared-memory instruction (dims 4l..4l+3 in lane l); the
+// G query heads of the group are in registers (pre-scaled by sm_scale*log2 e),
+// a transposed butterfly turns the J x G partial dot products into one logit
+// per lane, and online softmax accumulates P.V into 4 dims x G heads per lane.
+// The warps' states are combined in shared memory; the CTA writes the final
+// bf16 output (one split) or fp32 partials, and with a fused merge the CTA
+// that finishes a (b, g) last merges all splits.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -30,6 +33,9 @@ namespace ds {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 32;     // tokens per gather stage
+constexpr int kSeg = 512;     // selected positions resolved at a time
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -47,25 +53,36 @@ struct AttnParams {
   __nv_bfloat16* out;
   float* lse;
   unsigned* err;
-  int B, Hq, Hkv, maxp, num_pages, lim, k, S, split_mode, n_known;
+  unsigned* merge_done;
+  int B, Hq, Hkv, maxp, num_pages, lim, k, S, split_mode, n_known, nst;
   float qscale;  // sm_scale * log2(e)
 };
 
 template <int G, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams p) {
   constexpr int J = (G >= 4) ? 32 / G : 8;   // tokens per sub-tile
   constexpr int V = J * G;                   // logits per sub-tile (<= 32)
   constexpr int SH = (V >= 32) ? 0 : (V == 16 ? 1 : (V == 8 ? 2 : 3));  // lane -> value shift
-  constexpr int NSUB = 32 / J;
   constexpr int ROWB = FP8 ? kHeadDim : kHeadDim * 2;  // bytes per K/V row
+  constexpr int CPR = ROWB / 16;                        // 16-byte copies per row
+  constexpr int STAGE = 2 * kTile * ROWB;               // K tile then V tile
+  constexpr int CPT = 2 * kTile * CPR / kThreads;       // copies per thread per stage
+  constexpr int WTOK = kTile / kWarps;                  // tokens per warp per tile (8)
 
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  int* sl = reinterpret_cast<int*>(smem + static_cast<size_t>(p.nst) * STAGE);   // [kSeg] slots
+  float2* sc = reinterpret_cast<float2*>(sl + kSeg);                             // [kSeg] (kscale, vscale)
   __shared__ float sm_m[kWarps][G];
   __shared__ float sm_l[kWarps][G];
   __shared__ float sm_o[kWarps][G][kHeadDim];
+  __shared__ unsigned sh_scan[33];
   __shared__ unsigned sh_cnt[kWarps];
+  __shared__ int sh_last;
 
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
   const int j = blockIdx.x % p.S;
   const int bg = blockIdx.x / p.S;
   const int g = bg % p.Hkv;
@@ -75,14 +92,12 @@ __global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnPara
   int T = p.seq_lens[b];
   if (T < 0 || T > p.lim) T = T < 0 ? 0 : p.lim;  // flagged by the scoring / top-k stages
 
-  // Number of valid (leading, non-negative) entries of the index row: known
-  // from the length when the row comes from the top-k stage, else counted.
   int n;
   if (p.n_known) {
     n = min(p.k, T);
   } else {
     unsigned cnt = 0;
-    for (int i = threadIdx.x; i < p.k; i += blockDim.x) cnt += row[i] >= 0;
+    for (int i = tid; i < p.k; i += kThreads) cnt += row[i] >= 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
     if (lane == 0) sh_cnt[warp] = cnt;
@@ -91,21 +106,17 @@ __global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnPara
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) n += sh_cnt[w];
   }
-
-  int p0, p1;
+  int p0 = 0, p1 = n;
   if (p.split_mode == 0) {
     p0 = static_cast<int>(static_cast<long long>(j) * n / p.S);
     p1 = static_cast<int>(static_cast<long long>(j + 1) * n / p.S);
-  } else {
-    p0 = 0;
-    p1 = n;
   }
 
   // Query heads g*G .. g*G+G-1, dims 4*lane .. 4*lane+3, scaled to log2 units.
   float qf[G][4];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p.q + (static_cast<long long>(b) * p.Hq + g * G + h) * kHeadDim + lane * 4);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.q + (static_cast<long long>(b) * p.Hq + g * G + h) * kHeadDim + lane * 4));
     qf[h][0] = bf16_lo(w.x) * p.qscale;
     qf[h][1] = bf16_hi(w.x) * p.qscale;
     qf[h][2] = bf16_lo(w.y) * p.qscale;
@@ -123,127 +134,167 @@ __global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnPara
   const int my_h = my_v % G;
   const int my_j = my_v / G;
 
-  for (int tb = p0 + warp * 32; tb < p1; tb += kWarps * 32) {
-    const int pos = tb + lane;
-    bool valid = pos < p1;
-    int t = valid ? row[pos] : -1;
-    valid = valid && t >= 0;
-    if (valid && t >= T) {
-      flag_error(p.err, 4u);
-      valid = false;
-    }
-    if (valid && p.split_mode == 1 && (t / kPage) % p.S != j) valid = false;
-    int pid = 0;
-    if (valid) {
-      pid = p.page_table[static_cast<long long>(b) * p.maxp + t / kPage];
-      if (pid < 0 || pid >= p.num_pages) {
-        flag_error(p.err, 2u);
-        valid = false;
-        pid = 0;
-      }
-    }
-    const long long rowoff = ((static_cast<long long>(pid) * kPage + (t & (kPage - 1))) * p.Hkv + g) * ROWB;
-    float kscale = 1.f, vscale = 1.f;
-    if (FP8 && valid) {
-      kscale = p.ks[pid];
-      vscale = p.vs[pid];
-    }
-    const unsigned vmask = __ballot_sync(kFull, valid);
-    if (!vmask) continue;
+  const long long head_off = static_cast<long long>(g) * ROWB;
+  const long long slot_stride = static_cast<long long>(p.Hkv) * ROWB;
 
-#pragma unroll 2
-    for (int sub = 0; sub < NSUB; ++sub) {
-      const unsigned smask = (vmask >> (sub * J)) & ((J == 32) ? kFull : ((1u << J) - 1u));
-      if (!smask) continue;
-      // Gather J K rows and J V rows, one coalesced warp instruction each.
-      uint2 kx[J], vx[J];
+  for (int sb = p0; sb < p1; sb += kSeg) {
+    const int se = min(p1, sb + kSeg);
+    // ---- resolve the slots of this segment, in order
+    constexpr int PPT = kSeg / kThreads;
+    int slot_v[PPT];
+    float2 sc_v[PPT];
+    unsigned cnt = 0;
 #pragma unroll
-      for (int jj = 0; jj < J; ++jj) {
-        const long long ro = __shfl_sync(kFull, rowoff, sub * J + jj);
-        if ((smask >> jj) & 1u) {
-          if (FP8) {
-            kx[jj].x = ld_nc_na_4(p.kc + ro + lane * 4);
-            vx[jj].x = ld_nc_na_4(p.vc + ro + lane * 4);
+    for (int i = 0; i < PPT; ++i) {
+      const int pos = sb + tid * PPT + i;
+      slot_v[i] = -1;
+      sc_v[i] = make_float2(1.f, 1.f);
+      if (pos < se) {
+        const int t = row[pos];
+        bool ok = t >= 0;
+        if (ok && t >= T) {
+          flag_error(p.err, 4u);
+          ok = false;
+        }
+        if (ok && p.split_mode == 1 && (t / kPage) % p.S != j) ok = false;
+        if (ok) {
+          const int pid = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + t / kPage);
+          if (pid < 0 || pid >= p.num_pages) {
+            flag_error(p.err, 2u);
           } else {
-            kx[jj] = ld_nc_na_8(p.kc + ro + lane * 8);
-            vx[jj] = ld_nc_na_8(p.vc + ro + lane * 8);
+            slot_v[i] = pid * kPage + (t & (kPage - 1));
+            if (FP8) sc_v[i] = make_float2(__ldg(p.ks + pid), __ldg(p.vs + pid));
+            ++cnt;
           }
-        } else {
-          kx[jj] = make_uint2(0u, 0u);
-          vx[jj] = make_uint2(0u, 0u);
-        }
-      }
-      float part[V];
-#pragma unroll
-      for (int jj = 0; jj < J; ++jj) {
-        float k0, k1, k2, k3;
-        if (FP8) {
-          const float2 a = e4m3x2_to_float2(kx[jj].x);
-          const float2 c = e4m3x2_to_float2(kx[jj].x >> 16);
-          k0 = a.x; k1 = a.y; k2 = c.x; k3 = c.y;
-        } else {
-          k0 = bf16_lo(kx[jj].x); k1 = bf16_hi(kx[jj].x); k2 = bf16_lo(kx[jj].y); k3 = bf16_hi(kx[jj].y);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float a = qf[h][0] * k0;
-          a = fmaf(qf[h][1], k1, a);
-          a = fmaf(qf[h][2], k2, a);
-          a = fmaf(qf[h][3], k3, a);
-          part[jj * G + h] = a;
-        }
-      }
-      transposed_reduce<32, V>(part);
-      // This lane now holds the logit of (token my_j, head my_h) of the sub-tile.
-      const int src = sub * J + my_j;
-      const bool tv = (smask >> my_j) & 1u;
-      const float ksrc = FP8 ? __shfl_sync(kFull, kscale, src) : 1.f;
-      float z = tv ? part[0] * ksrc : -INFINITY;
-      // Sub-tile max per head: reduce over lanes of other tokens.
-      float zm = z;
-#pragma unroll
-      for (int off = (1 << SH) * G; off < 32; off <<= 1) zm = fmaxf(zm, __shfl_xor_sync(kFull, zm, off));
-      float mnew[G], corr[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float tm = __shfl_sync(kFull, zm, h << SH);
-        mnew[h] = fmaxf(m[h], tm);
-        corr[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
-        m[h] = mnew[h];
-      }
-      float my_m = mnew[0], my_corr = corr[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h) {
-        my_m = (my_h == h) ? mnew[h] : my_m;
-        my_corr = (my_h == h) ? corr[h] : my_corr;
-      }
-      const float pw = (z == -INFINITY) ? 0.f : exp2f(z - my_m);
-      lsum = lsum * my_corr + pw;
-      const float pv = FP8 ? pw * __shfl_sync(kFull, vscale, src) : pw;
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[h][i] *= corr[h];
-#pragma unroll
-      for (int jj = 0; jj < J; ++jj) {
-        float v0, v1, v2, v3;
-        if (FP8) {
-          const float2 a = e4m3x2_to_float2(vx[jj].x);
-          const float2 c = e4m3x2_to_float2(vx[jj].x >> 16);
-          v0 = a.x; v1 = a.y; v2 = c.x; v3 = c.y;
-        } else {
-          v0 = bf16_lo(vx[jj].x); v1 = bf16_hi(vx[jj].x); v2 = bf16_lo(vx[jj].y); v3 = bf16_hi(vx[jj].y);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pj = __shfl_sync(kFull, pv, (jj * G + h) << SH);
-          o[h][0] = fmaf(pj, v0, o[h][0]);
-          o[h][1] = fmaf(pj, v1, o[h][1]);
-          o[h][2] = fmaf(pj, v2, o[h][2]);
-          o[h][3] = fmaf(pj, v3, o[h][3]);
         }
       }
     }
+    unsigned nseg;
+    unsigned wpos = block_excl_scan(cnt, sh_scan, &nseg);
+#pragma unroll
+    for (int i = 0; i < PPT; ++i) {
+      if (slot_v[i] >= 0) {
+        sl[wpos] = slot_v[i];
+        if (FP8) sc[wpos] = sc_v[i];
+        ++wpos;
+      }
+    }
+    __syncthreads();
+    const int ntile = (static_cast<int>(nseg) + kTile - 1) / kTile;
+
+    auto issue = [&](int tile, int stage) {
+      unsigned char* dst = ring + stage * STAGE;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        const int id = c * kThreads + tid;          // 0 .. 2*kTile*CPR-1
+        const int kv = id / (kTile * CPR);          // 0: K, 1: V
+        const int r = (id / CPR) % kTile;
+        const int part = id % CPR;
+        const int e = tile * kTile + r;
+        const bool ok = e < static_cast<int>(nseg);
+        const uint8_t* base = kv ? p.vc : p.kc;
+        const uint8_t* src = ok ? base + sl[e] * slot_stride + head_off + part * 16 : base;
+        cp_async16(dst + id * 16, src, ok);
+      }
+    };
+
+    for (int s = 0; s < p.nst; ++s) {
+      if (s < ntile) issue(s, s);
+      cp_async_commit();
+    }
+    for (int tile = 0; tile < ntile; ++tile) {
+      const int stage = tile % p.nst;
+      cp_async_wait_dyn(p.nst - 1);
+      __syncthreads();
+      const unsigned char* kt = ring + stage * STAGE;
+      const unsigned char* vt = kt + kTile * ROWB;
+      const int tok_base = tile * kTile + warp * WTOK;   // entry index of this warp's first token
+#pragma unroll
+      for (int sub = 0; sub < WTOK / J; ++sub) {
+        const int r0 = warp * WTOK + sub * J;           // row within the tile
+        const int e0 = tok_base + sub * J;              // entry index
+        const int nvalid = min(J, static_cast<int>(nseg) - e0);
+        if (nvalid <= 0) break;
+        float part[V];
+#pragma unroll
+        for (int jj = 0; jj < J; ++jj) {
+          float k0, k1, k2, k3;
+          if (FP8) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + (r0 + jj) * ROWB + lane * 4);
+            const float2 a = e4m3x2_to_float2(w);
+            const float2 c = e4m3x2_to_float2(w >> 16);
+            k0 = a.x; k1 = a.y; k2 = c.x; k3 = c.y;
+          } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(kt + (r0 + jj) * ROWB + lane * 8);
+            k0 = bf16_lo(w.x); k1 = bf16_hi(w.x); k2 = bf16_lo(w.y); k3 = bf16_hi(w.y);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float a = qf[h][0] * k0;
+            a = fmaf(qf[h][1], k1, a);
+            a = fmaf(qf[h][2], k2, a);
+            a = fmaf(qf[h][3], k3, a);
+            part[jj * G + h] = a;
+          }
+        }
+        transposed_reduce<32, V>(part);
+        // This lane now holds the logit of (token my_j, head my_h) of the sub-tile.
+        const bool tv = my_j < nvalid;
+        float2 scl = make_float2(1.f, 1.f);
+        if (FP8 && tv) scl = sc[e0 + my_j];
+        const float z = tv ? part[0] * scl.x : -INFINITY;
+        float zm = z;
+#pragma unroll
+        for (int off = (1 << SH) * G; off < 32; off <<= 1) zm = fmaxf(zm, __shfl_xor_sync(kFull, zm, off));
+        float mnew[G], corr[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float tm = __shfl_sync(kFull, zm, h << SH);
+          mnew[h] = fmaxf(m[h], tm);
+          corr[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
+          m[h] = mnew[h];
+        }
+        float my_m = mnew[0], my_corr = corr[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) {
+          my_m = (my_h == h) ? mnew[h] : my_m;
+          my_corr = (my_h == h) ? corr[h] : my_corr;
+        }
+        const float pw = (z == -INFINITY) ? 0.f : exp2f(z - my_m);
+        lsum = lsum * my_corr + pw;
+        const float pv = FP8 ? pw * scl.y : pw;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[h][i] *= corr[h];
+#pragma unroll
+        for (int jj = 0; jj < J; ++jj) {
+          float v0, v1, v2, v3;
+          if (FP8) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + (r0 + jj) * ROWB + lane * 4);
+            const float2 a = e4m3x2_to_float2(w);
+            const float2 c = e4m3x2_to_float2(w >> 16);
+            v0 = a.x; v1 = a.y; v2 = c.x; v3 = c.y;
+          } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(vt + (r0 + jj) * ROWB + lane * 8);
+            v0 = bf16_lo(w.x); v1 = bf16_hi(w.x); v2 = bf16_lo(w.y); v3 = bf16_hi(w.y);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float pj = __shfl_sync(kFull, pv, (jj * G + h) << SH);
+            o[h][0] = fmaf(pj, v0, o[h][0]);
+            o[h][1] = fmaf(pj, v1, o[h][1]);
+            o[h][2] = fmaf(pj, v2, o[h][2]);
+            o[h][3] = fmaf(pj, v3, o[h][3]);
+          }
+        }
+      }
+      __syncthreads();
+      if (tile + p.nst < ntile) issue(tile + p.nst, stage);
+      cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
   }
 
   // Per-head sums of this warp: add the lanes of the other tokens.
@@ -262,7 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnPara
   __syncthreads();
 
   // Combine the warps: the log-sum-exp merge of kWarps partial states.
-  for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x) {
+  for (int e = tid; e < G * kHeadDim; e += kThreads) {
     const int h = e / kHeadDim;
     const int d = e % kHeadDim;
     float M = -INFINITY;
@@ -289,6 +340,43 @@ __global__ void __launch_bounds__(kWarps * 32) sparse_attn_kernel(const AttnPara
       if (d == 0) p.lse_part[prow] = lse;
     }
   }
+  if (p.S == 1 || !p.merge_done) return;
+
+  // ---- fused merge: the CTA that finishes (b, g) last merges its S splits.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = (atomicAdd(p.merge_done + bg, 1u) + 1 == static_cast<unsigned>(p.S));
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  const long long rows = static_cast<long long>(p.B) * p.Hq;
+  const long long qrow0 = static_cast<long long>(b) * p.Hq + g * G;
+  // Per-head log-sum-exp over the splits (kept in sm_l[0]).
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int s = 0; s < p.S; ++s) M = fmaxf(M, __ldcg(p.lse_part + s * rows + qrow0 + tid));
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int s = 0; s < p.S; ++s) L += expf(__ldcg(p.lse_part + s * rows + qrow0 + tid) - M);
+    sm_l[0][tid] = (M == -INFINITY) ? -INFINITY : M + logf(L);
+  }
+  __syncthreads();
+  for (int e = tid; e < G * kHeadDim; e += kThreads) {
+    const int h = e / kHeadDim;
+    const int d = e % kHeadDim;
+    const float lse = sm_l[0][h];
+    float acc = 0.f;
+    if (lse != -INFINITY) {
+      for (int s = 0; s < p.S; ++s) {
+        const float ls = __ldcg(p.lse_part + s * rows + qrow0 + h);
+        if (ls == -INFINITY) continue;
+        acc = fmaf(expf(ls - lse), __ldcg(p.o_part + (s * rows + qrow0 + h) * kHeadDim + d), acc);
+      }
+    }
+    p.out[(qrow0 + h) * kHeadDim + d] = __float2bfloat16_rn(acc);
+    if (d == 0 && p.lse) p.lse[qrow0 + h] = lse;
+  }
+  if (tid == 0) atomicExch(p.merge_done + bg, 0u);
 }
 
 using KernelFn = void (*)(const AttnParams);
@@ -304,6 +392,19 @@ KernelFn pick(int G) {
   return nullptr;
 }
 
+cudaError_t allow_smem(KernelFn fn, int bytes) {
+  struct Entry { KernelFn fn; int dev; int bytes; };
+  static Entry done[64];
+  static int n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < n; ++i)
+    if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n < 64) done[n++] = Entry{fn, dev, bytes};
+  return e;
+}
+
 }  // namespace
 
 bool sparse_attn_supported(int G) { return pick<false>(G) != nullptr; }
@@ -314,7 +415,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (!fn) return cudaErrorNotSupported;
   const long long blocks = static_cast<long long>(a.B) * a.Hkv * a.S;
   if (blocks == 0) return cudaSuccess;
-  AttnParams p;
+  AttnParams p{};
   p.q = static_cast<const uint16_t*>(a.q);
   p.kc = static_cast<const uint8_t*>(a.k_cache);
   p.vc = static_cast<const uint8_t*>(a.v_cache);
@@ -328,6 +429,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.err = a.err;
+  p.merge_done = a.merge_done;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -339,7 +441,13 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.split_mode = a.split_mode;
   p.qscale = a.sm_scale * kLog2e;
   p.n_known = a.n_from_seq_len;
-  fn<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(p);
+  const int rowb = a.fp8 ? kHeadDim : kHeadDim * 2;
+  const int stage = 2 * kTile * rowb;
+  p.nst = a.fp8 ? 6 : 4;
+  const int smem = p.nst * stage + kSeg * (a.fp8 ? 4 + 8 : 4);
+  cudaError_t e = allow_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  fn<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

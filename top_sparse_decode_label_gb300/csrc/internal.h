@@ -9,10 +9,26 @@ namespace ds {
 
 constexpr int kHeadDimSupported = 128;
 constexpr int kPageSupported = 64;
-constexpr long long kDecodeTargetCtas = 320;  // attention CTAs the chained call aims for
+constexpr long long kDecodeTargetCtas = 456;  // attention CTAs the chained call aims for (3 per SM)
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+
+// Scratch of the exact top-k for R rows of up to Tmax scores. The first
+// `zero_bytes` bytes (histograms and completion counters) must be zero when a
+// top-k starts; every completed top-k leaves them zero again.
+struct TopkLayout {
+  void* ghist;       // u32 [R, 2048]
+  void* done1;       // u32 [R]
+  void* done2;       // u32 [R]
+  void* row_state;   // uint2 [R]
+  void* counts;      // u32 [R, nch]
+  void* list;        // uint2 [R, Tmax]
+  int nch;
+  size_t zero_bytes;
+  size_t bytes;
+};
+TopkLayout topk_layout(void* base, int R, int Tmax);
 
 struct ScoreArgs {
   const void* qp;          // bf16 [B, Hq, C]
@@ -22,6 +38,8 @@ struct ScoreArgs {
   float* scores;           // [B, Hkv, Tmax]
   unsigned* err;
   int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
+  const TopkLayout* topk;  // non-null: also build the level-1 top-k histograms for this k
+  int k;
 };
 // Returns a cudaError_t; cudaErrorNotSupported for shapes without a kernel.
 cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream);
@@ -33,9 +51,9 @@ struct TopkArgs {
   int32_t* idx;            // [B, Hkv, k]
   unsigned* err;
   int B, Hkv, Tmax, maxp_tokens, k;
-  void* ws;
+  TopkLayout L;
+  bool histogram_done;     // level-1 thresholds already computed by the scoring kernel
 };
-size_t topk_workspace_bytes(int B, int Hkv, int Tmax, int k);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
@@ -49,12 +67,13 @@ struct AttnArgs {
   const int32_t* idx;      // [B, Hkv, k]
   float* o_part;           // [S, B, Hq, D] (S > 1)
   float* lse_part;         // [S, B, Hq]
-  void* out;               // bf16 [B, Hq, D] (S == 1)
-  float* lse;              // [B, Hq] (S == 1, may be null)
+  void* out;               // bf16 [B, Hq, D] (S == 1, or S > 1 with a fused merge)
+  float* lse;              // [B, Hq] (may be null)
   unsigned* err;
   int B, Hq, Hkv, maxp, num_pages, Tmax, k, S, split_mode, fp8;
   float sm_scale;
   int n_from_seq_len;      // 1: each idx row holds exactly min(k, seq_len) valid entries (top-k output)
+  unsigned* merge_done;    // non-null (S > 1): [B, Hkv] zeroed counters; the last split CTA merges into out
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 bool sparse_attn_supported(int G);

@@ -36,15 +36,27 @@ lse_merge_kernel(int S, int rows, int D, const float* __restrict__ o_part, const
   for (int d4 = lane; d4 < D / 4; d4 += 32) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float ls = lse_part[static_cast<long long>(s) * rows + r];
-        if (ls == -INFINITY) continue;
-        const float w = expf(ls - lse);
-        const float4 v = *reinterpret_cast<const float4*>(o_part + (static_cast<long long>(s) * rows + r) * D + d4 * 4);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+      // Eight splits per step, loads issued before use so they overlap.
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        float ls[8];
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ls[i] = -INFINITY;
+          if (s0 + i < S) {
+            ls[i] = lse_part[static_cast<long long>(s0 + i) * rows + r];
+            v[i] = *reinterpret_cast<const float4*>(o_part + (static_cast<long long>(s0 + i) * rows + r) * D + d4 * 4);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (ls[i] == -INFINITY) continue;
+          const float w = expf(ls[i] - lse);
+          acc.x = fmaf(w, v[i].x, acc.x);
+          acc.y = fmaf(w, v[i].y, acc.y);
+          acc.z = fmaf(w, v[i].z, acc.z);
+          acc.w = fmaf(w, v[i].w, acc.w);
+        }
       }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);

@@ -6,67 +6,37 @@
 // token-ID tie-breaking. "Support double sparsity" (PR #1459): keep the
 // heavy-token count of tokens per head.
 //
-// Scores are mapped to order-preserving 32-bit keys (-0.0 == +0.0, NaN
-// lowest). Let K_eff = min(k, T). Three launches, all multi-CTA except the last:
-//   hist    : 2048-bin histogram of key >> 21 per row (shared-memory
-//             histogram per 4096-score chunk, flushed with global atomics).
-//   filter  : every CTA finds the bin b1 holding the K_eff-th largest key from
-//             the row histogram, then streams its chunk: keys in bins above b1
-//             are certainly kept ("sure" list), keys in b1 are candidates.
-//   select  : one CTA per row refines the threshold key among the candidates
-//             with two more radix digits (11 + 10 bits), giving the exact
-//             K_eff-th key `thr` and how many tokens with key == thr to keep.
-//             Kept tokens are marked in a shared-memory bitmap over token
-//             positions; the first r ties in token order are found with a
-//             popcount prefix over the bitmap, and a second popcount prefix
-//             writes the kept tokens ascending. Rows longer than the bitmap
-//             window are processed window by window.
-// The score buffer is read twice (hist, filter); everything else touches only
-// the candidates, typically a few thousand per row.
+// Scores map to order-preserving 32-bit keys (-0.0 == +0.0, NaN lowest).
+// With K_eff = min(k, T), rows with 0 < K_eff < T go through three radix
+// digits (11 + 11 + 10 bits):
+//   level 1 (histogram): a 2048-bin histogram of key >> 21 per row, built by
+//     the scoring kernel in the chained call or by topk_hist_kernel here; the
+//     CTA that completes a row's histogram finds the bin b1 holding the
+//     K_eff-th largest key and the count above it.
+//   filter: one CTA per 4096-score chunk keeps every (key, token) with
+//     key >> 21 >= b1, in token order, in the chunk's slot of the row's list
+//     (one block-wide prefix sum, no atomics per element).
+//   select: the CTA that completes a row's filter refines the threshold key
+//     over the kept entries whose top bits equal b1 (two more digits in shared
+//     memory), giving the exact K_eff-th key `thr` and the number r of tokens
+//     with key == thr to keep. Walking the list in token order with two
+//     block-wide prefix sums (rank among ties, then output position) writes
+//     the kept tokens -- key > thr, or key == thr and tie rank < r --
+//     ascending. The list is typically K_eff plus a few thousand entries.
+// Completion is detected with per-row counters (the last CTA continues);
+// nothing waits on another CTA.
 #include "common.cuh"
 #include "internal.h"
+#include "topk_common.cuh"
 
 namespace ds {
 
 namespace {
 
-constexpr int kBins1 = 2048;          // top 11 bits
-constexpr int kChunk = 4096;          // scores per hist/filter CTA
-constexpr int kChunkThreads = 256;
-constexpr int kSelThreads = 1024;
-constexpr int kWindow = 1 << 20;      // tokens per bitmap window (128 KB of shared memory)
-
-struct Layout {
-  unsigned* hist;    // [R, 2048]
-  unsigned* state;   // [R, 4]: sure count, candidate count
-  int32_t* sure;     // [R, k]
-  uint32_t* ckey;    // [R, Tmax]
-  int32_t* ctok;     // [R, Tmax]
-  size_t bytes;
-  size_t clear_bytes;  // hist + state, zeroed per call
-};
+constexpr int kElems = kChunk / kChunkThreads;   // 16 scores per thread
+constexpr int kMaxChunks = 4096;                 // rows of up to 16M tokens
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-Layout make_layout(void* base, int R, int Tmax, int k) {
-  Layout L;
-  char* p = static_cast<char*>(base);
-  size_t off = 0;
-  L.hist = reinterpret_cast<unsigned*>(p + off);
-  off += static_cast<size_t>(R) * kBins1 * 4;
-  L.state = reinterpret_cast<unsigned*>(p + off);
-  off += static_cast<size_t>(R) * 16;
-  L.clear_bytes = off;
-  off = align256(off);
-  L.sure = reinterpret_cast<int32_t*>(p + off);
-  off = align256(off + static_cast<size_t>(R) * (k > 0 ? k : 1) * 4);
-  L.ckey = reinterpret_cast<uint32_t*>(p + off);
-  off = align256(off + static_cast<size_t>(R) * (Tmax > 0 ? Tmax : 1) * 4);
-  L.ctok = reinterpret_cast<int32_t*>(p + off);
-  off = align256(off + static_cast<size_t>(R) * (Tmax > 0 ? Tmax : 1) * 4);
-  L.bytes = off;
-  return L;
-}
 
 struct TopkParams {
   const float* scores;
@@ -74,7 +44,7 @@ struct TopkParams {
   int32_t* idx;
   unsigned* err;
   int Hkv, Tmax, lim, k;
-  Layout L;
+  TopkWs w;
 };
 
 __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
@@ -86,229 +56,266 @@ __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
   return T;
 }
 
-// Scanning `hist` from its highest bin down, finds the bin where the running
-// count first reaches `need` (1 <= need <= total). Writes out[0] = bin,
-// out[1] = count in the bins above it. nbins must be a multiple of blockDim.x.
-__device__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned need, unsigned* sh_scan,
-                                   unsigned* out) {
-  const int per = nbins / blockDim.x;
-  const int hi = nbins - per * threadIdx.x;
-  if (threadIdx.x == 0) {  // defined result even if `need` were out of range
-    out[0] = 0;
-    out[1] = 0;
-  }
-  unsigned c = 0;
-  for (int i = 1; i <= per; ++i) c += hist[hi - i];
-  unsigned total;
-  const unsigned before = block_excl_scan(c, sh_scan, &total);
-  if (before < need && before + c >= need) {
-    unsigned run = before;
-    for (int i = 1; i <= per; ++i) {
-      const unsigned h = hist[hi - i];
-      if (run + h >= need) {
-        out[0] = hi - i;
-        out[1] = run;
-        break;
-      }
-      run += h;
-    }
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ unsigned warp_append(bool pred, unsigned* counter) {
-  const int lane = threadIdx.x & 31;
-  const unsigned mask = __ballot_sync(kFull, pred);
-  unsigned base = 0;
-  const int leader = mask ? __ffs(mask) - 1 : 0;
-  if (mask && lane == leader) base = atomicAdd(counter, __popc(mask));
-  base = __shfl_sync(kFull, base, leader);
-  return base + __popc(mask & ((1u << lane) - 1u));
-}
-
+// Level 1 on its own (the scores were produced elsewhere).
 __global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const TopkParams p) {
   __shared__ unsigned h[kBins1];
+  __shared__ unsigned sh_scan[33];
+  __shared__ unsigned sh_res[2];
+  __shared__ int sh_last;
   const int row = blockIdx.y;
   const int b = row / p.Hkv;
   const int T = row_len(p, b, blockIdx.x == 0 && threadIdx.x == 0 && row % p.Hkv == 0);
-  const int keff = min(p.k, T);
-  const int c0 = blockIdx.x * kChunk;
-  if (keff == 0 || keff == T || c0 >= T) return;
+  if (!needs_selection(p.k, T)) return;
+  const int nch = (T + kChunk - 1) / kChunk;
+  if (static_cast<int>(blockIdx.x) >= nch) return;
   for (int i = threadIdx.x; i < kBins1; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
+  const int c0 = blockIdx.x * kChunk;
   const int c1 = min(T, c0 + kChunk);
   for (int t = c0 + threadIdx.x; t < c1; t += blockDim.x) atomicAdd(&h[order_key(s[t]) >> 21], 1u);
   __syncthreads();
-  unsigned* g = p.L.hist + static_cast<size_t>(row) * kBins1;
+  unsigned* g = p.w.ghist + static_cast<size_t>(row) * kBins1;
   for (int i = threadIdx.x; i < kBins1; i += blockDim.x)
     if (h[i]) atomicAdd(&g[i], h[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sh_last = (atomicAdd(p.w.done1 + row, 1u) + 1 == static_cast<unsigned>(nch));
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  level1_threshold(p.w, row, p.k, sh_scan, sh_res);
+  if (threadIdx.x == 0) atomicExch(p.w.done1 + row, 0u);
 }
 
-__global__ void __launch_bounds__(kChunkThreads) topk_filter_kernel(const TopkParams p) {
-  __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_res[2];
-  const int row = blockIdx.y;
-  const int b = row / p.Hkv;
-  const int T = row_len(p, b, false);
-  const int keff = min(p.k, T);
-  const int c0 = blockIdx.x * kChunk;
-  if (keff == 0 || keff == T || c0 >= T) return;
-  find_threshold_bin(p.L.hist + static_cast<size_t>(row) * kBins1, kBins1, keff, sh_scan, sh_res);
-  const unsigned b1 = sh_res[0];
-  const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-  unsigned* st = p.L.state + static_cast<size_t>(row) * 4;
-  int32_t* sure = p.L.sure + static_cast<size_t>(row) * p.k;
-  uint32_t* ckey = p.L.ckey + static_cast<size_t>(row) * p.Tmax;
-  int32_t* ctok = p.L.ctok + static_cast<size_t>(row) * p.Tmax;
-  const int c1 = min(T, c0 + kChunk);
-  // Uniform trip count so whole warps take part in the appends.
-  for (int base = c0; base < c1; base += blockDim.x) {
-    const int t = base + threadIdx.x;
-    uint32_t key = 0;
-    if (t < c1) key = order_key(s[t]);
-    const unsigned bin = key >> 21;
-    const bool is_sure = t < c1 && bin > b1;
-    const bool is_cand = t < c1 && bin == b1;
-    const unsigned ps = warp_append(is_sure, &st[0]);
-    const unsigned pc = warp_append(is_cand, &st[1]);
-    if (is_sure) sure[ps] = t;
-    if (is_cand) {
-      ckey[pc] = key;
-      ctok[pc] = t;
+// Walks entries [e, ...) of a row's list (chunk slots concatenated).
+struct ListWalker {
+  const uint2* base;   // row's list
+  const unsigned* pref;  // shared: chunk prefix, nch + 1 entries
+  int ci, off;
+  __device__ void seek(int e, int nch) {
+    int lo = 0, hi = nch - 1;  // largest ci with pref[ci] <= e
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pref[mid] <= static_cast<unsigned>(e)) lo = mid; else hi = mid - 1;
     }
+    ci = lo;
+    off = e - static_cast<int>(pref[ci]);
   }
-}
+  __device__ uint2 next() {
+    while (static_cast<unsigned>(off) >= pref[ci + 1] - pref[ci]) {
+      ++ci;
+      off = 0;
+    }
+    const uint2 v = __ldcg(base + static_cast<size_t>(ci) * kChunk + off);
+    ++off;
+    return v;
+  }
+};
 
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkParams p, int win_words) {
-  extern __shared__ unsigned bitmap[];
+__global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const TopkParams p) {
   __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_hist[kBins1];
   __shared__ unsigned sh_res[2];
-  const int row = blockIdx.x;
+  __shared__ int sh_last;
+  __shared__ unsigned sh_hist[kBins1];
+  __shared__ unsigned sh_pref[kMaxChunks + 1];
+  const int tid = threadIdx.x;
+  const int row = blockIdx.y;
   const int b = row / p.Hkv;
   const int T = row_len(p, b, false);
   const int keff = min(p.k, T);
   int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
-  const int tid = threadIdx.x;
-
-  if (keff == 0 || keff == T) {
-    for (int i = tid; i < p.k; i += blockDim.x) out[i] = (i < keff) ? i : -1;
+  if (!needs_selection(p.k, T)) {
+    if (blockIdx.x == 0)
+      for (int i = tid; i < p.k; i += blockDim.x) out[i] = (i < keff) ? i : -1;
     return;
   }
-  // Level 1: the bin of the top 11 bits (same histogram the filter used).
-  find_threshold_bin(p.L.hist + static_cast<size_t>(row) * kBins1, kBins1, keff, sh_scan, sh_res);
-  const unsigned b1 = sh_res[0];
-  const unsigned need = keff - sh_res[1];
-  const unsigned* st = p.L.state + static_cast<size_t>(row) * 4;
-  const int nsure = st[0];
-  const int ncand = st[1];
-  const uint32_t* ckey = p.L.ckey + static_cast<size_t>(row) * p.Tmax;
-  const int32_t* ctok = p.L.ctok + static_cast<size_t>(row) * p.Tmax;
-  const int32_t* sure = p.L.sure + static_cast<size_t>(row) * p.k;
+  const int nch = (T + kChunk - 1) / kChunk;
+  const int c = blockIdx.x;
+  if (c >= nch) return;
+  const uint2 st = __ldcg(p.w.row_state + row);
+  const unsigned b1 = st.x;
+  const unsigned above1 = st.y;
 
-  // Level 2: bits 10..20 among the candidates.
+  // ---- filter: keep key >> 21 >= b1 of this chunk, in token order
+  const int c0 = c * kChunk;
+  const int c1 = min(T, c0 + kChunk);
+  const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
+  const int t0 = c0 + tid * kElems;
+  uint32_t keys[kElems];
+  unsigned flags = 0, cnt = 0;
+  const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1);
+  if (vec) {
+#pragma unroll
+    for (int i = 0; i < kElems; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(s + t0 + i);
+      keys[i] = order_key(v.x);
+      keys[i + 1] = order_key(v.y);
+      keys[i + 2] = order_key(v.z);
+      keys[i + 3] = order_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < kElems; ++i) {
+    if (t0 + i < c1 && (keys[i] >> 21) >= b1) {
+      flags |= 1u << i;
+      ++cnt;
+    }
+  }
+  unsigned total;
+  unsigned pos = block_excl_scan(cnt, sh_scan, &total);
+  uint2* lst = p.w.list + static_cast<size_t>(row) * p.Tmax + c0;
+#pragma unroll
+  for (int i = 0; i < kElems; ++i)
+    if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
+  if (tid == 0) p.w.counts[static_cast<size_t>(row) * p.w.nch + c] = total;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = (atomicAdd(p.w.done2 + row, 1u) + 1 == static_cast<unsigned>(nch));
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+
+  // ---- select: this CTA completed the row
+  const unsigned* counts = p.w.counts + static_cast<size_t>(row) * p.w.nch;
+  const int cpt = (nch + kChunkThreads - 1) / kChunkThreads;
+  {
+    unsigned mine = 0;
+    for (int i = tid * cpt; i < min(nch, (tid + 1) * cpt); ++i) mine += __ldcg(counts + i);
+    unsigned tot;
+    unsigned run = block_excl_scan(mine, sh_scan, &tot);
+    for (int i = tid * cpt; i < min(nch, (tid + 1) * cpt); ++i) {
+      sh_pref[i] = run;
+      run += __ldcg(counts + i);
+    }
+    if (tid == 0) sh_pref[nch] = tot;
+  }
+  __syncthreads();
+  const int M = static_cast<int>(sh_pref[nch]);
+  const uint2* base = p.w.list + static_cast<size_t>(row) * p.Tmax;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const unsigned need = static_cast<unsigned>(keff) - above1;
+
+  // Level 2: bits 10..20 of the entries in bin b1.
   for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
-  for (int i = tid; i < ncand; i += blockDim.x) atomicAdd(&sh_hist[(ckey[i] >> 10) & 2047u], 1u);
+  for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
+    const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
+    for (int j = lane; j < n; j += 32) {
+      const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+      if ((key >> 21) == b1) atomicAdd(&sh_hist[(key >> 10) & 2047u], 1u);
+    }
+  }
   __syncthreads();
-  find_threshold_bin(sh_hist, kBins1, need, sh_scan, sh_res);
+  find_threshold_bin<false>(sh_hist, kBins1, need, sh_scan, sh_res);
   const unsigned d2 = sh_res[0];
   const unsigned need2 = need - sh_res[1];
-  // Level 3: bits 0..9 among the candidates that match so far.
+  // Level 3: bits 0..9 of the entries that match so far.
+  const uint32_t hi22 = (b1 << 11) | d2;
   for (int i = tid; i < 1024; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
-  for (int i = tid; i < ncand; i += blockDim.x) {
-    const uint32_t key = ckey[i];
-    if (((key >> 10) & 2047u) == d2) atomicAdd(&sh_hist[key & 1023u], 1u);
+  for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
+    const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
+    for (int j = lane; j < n; j += 32) {
+      const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+      if ((key >> 10) == hi22) atomicAdd(&sh_hist[key & 1023u], 1u);
+    }
   }
   __syncthreads();
-  find_threshold_bin(sh_hist, 1024, need2, sh_scan, sh_res);
+  find_threshold_bin<false>(sh_hist, 1024, need2, sh_scan, sh_res);
   const unsigned d3 = sh_res[0];
-  const unsigned r_eq = need2 - sh_res[1];          // ties to keep, in token order
+  const unsigned r_eq = need2 - sh_res[1];
   const unsigned eq_total = sh_hist[d3];
-  const uint32_t thr = (b1 << 21) | (d2 << 10) | d3;
+  const uint32_t thr = (hi22 << 10) | d3;
   __syncthreads();
 
-  const bool prune = eq_total > r_eq;
-  unsigned eq_before = 0;   // ties kept in earlier windows
-  unsigned out_off = 0;
-  const int win = win_words * 32;
-  for (int w0 = 0; w0 < T; w0 += win) {
-    const int wl = min(win, T - w0);
-    const int nwords = (wl + 31) >> 5;
-    const int per = (nwords + blockDim.x - 1) / blockDim.x;
-    const int wb = tid * per;
-    const int we = min(nwords, wb + per);
-    for (int i = tid; i < nwords; i += blockDim.x) bitmap[i] = 0;
-    __syncthreads();
-    // Ties at the threshold key.
-    for (int i = tid; i < ncand; i += blockDim.x) {
-      const int t = ctok[i] - w0;
-      if (ckey[i] == thr && t >= 0 && t < wl) atomicOr(&bitmap[t >> 5], 1u << (t & 31));
+  // Ordered output over the list: thread segments, prefix sums across threads.
+  const int seg = (M + kChunkThreads - 1) / kChunkThreads;
+  const int e0 = min(M, tid * seg);
+  const int e1 = min(M, e0 + seg);
+  ListWalker wk{base, sh_pref, 0, 0};
+  unsigned eq_base = 0;
+  if (eq_total > r_eq) {
+    unsigned eqc = 0;
+    if (e0 < e1) {
+      wk.seek(e0, nch);
+      for (int e = e0; e < e1; ++e) eqc += (wk.next().x == thr);
     }
-    __syncthreads();
-    if (prune) {
-      unsigned c = 0;
-      for (int i = wb; i < we; ++i) c += __popc(bitmap[i]);
-      unsigned total;
-      unsigned before = block_excl_scan(c, sh_scan, &total) + eq_before;
-      for (int i = wb; i < we; ++i) {
-        unsigned w = bitmap[i];
-        unsigned keepw = 0;
-        while (w) {
-          const unsigned bit = w & (0u - w);
-          if (before < r_eq) keepw |= bit;
-          ++before;
-          w ^= bit;
-        }
-        bitmap[i] = keepw;
-      }
-      eq_before += total;
-      __syncthreads();
-    }
-    // Everything strictly above the threshold.
-    for (int i = tid; i < ncand; i += blockDim.x) {
-      const int t = ctok[i] - w0;
-      if (ckey[i] > thr && t >= 0 && t < wl) atomicOr(&bitmap[t >> 5], 1u << (t & 31));
-    }
-    for (int i = tid; i < nsure; i += blockDim.x) {
-      const int t = sure[i] - w0;
-      if (t >= 0 && t < wl) atomicOr(&bitmap[t >> 5], 1u << (t & 31));
-    }
-    __syncthreads();
-    // Ascending compaction.
-    unsigned c = 0;
-    for (int i = wb; i < we; ++i) c += __popc(bitmap[i]);
-    unsigned total;
-    unsigned pos = out_off + block_excl_scan(c, sh_scan, &total);
-    for (int i = wb; i < we; ++i) {
-      unsigned w = bitmap[i];
-      while (w) {
-        const int bit = __ffs(w) - 1;
-        if (pos < static_cast<unsigned>(p.k)) out[pos] = w0 + i * 32 + bit;
-        ++pos;
-        w &= w - 1;
+    unsigned tot;
+    eq_base = block_excl_scan(eqc, sh_scan, &tot);
+  }
+  unsigned selc = 0;
+  if (e0 < e1) {
+    wk.seek(e0, nch);
+    unsigned eq = eq_base;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = wk.next().x;
+      if (key > thr) {
+        ++selc;
+      } else if (key == thr) {
+        selc += (eq < r_eq);
+        ++eq;
       }
     }
-    out_off += total;
-    __syncthreads();
+  }
+  unsigned tot_sel;
+  unsigned opos = block_excl_scan(selc, sh_scan, &tot_sel);
+  if (e0 < e1) {
+    wk.seek(e0, nch);
+    unsigned eq = eq_base;
+    for (int e = e0; e < e1; ++e) {
+      const uint2 v = wk.next();
+      bool keep = v.x > thr;
+      if (v.x == thr) {
+        keep = eq < r_eq;
+        ++eq;
+      }
+      if (keep) {
+        if (opos < static_cast<unsigned>(p.k)) out[opos] = static_cast<int32_t>(v.y);
+        ++opos;
+      }
+    }
   }
   for (int i = keff + tid; i < p.k; i += blockDim.x) out[i] = -1;
+  if (tid == 0) atomicExch(p.w.done2 + row, 0u);
 }
 
 }  // namespace
 
-size_t topk_workspace_bytes(int B, int Hkv, int Tmax, int k) {
-  return make_layout(nullptr, B * Hkv, Tmax, k).bytes;
+TopkLayout topk_layout(void* base, int R, int Tmax) {
+  TopkLayout L;
+  char* p = static_cast<char*>(base);
+  const int T1 = Tmax > 0 ? Tmax : 1;
+  L.nch = (T1 + kChunk - 1) / kChunk;
+  size_t off = 0;
+  L.ghist = p + off;
+  off += static_cast<size_t>(R) * kBins1 * 4;
+  L.done1 = p + off;
+  off += static_cast<size_t>(R) * 4;
+  L.done2 = p + off;
+  off += static_cast<size_t>(R) * 4;
+  L.zero_bytes = off;
+  off = align256(off);
+  L.row_state = p + off;
+  off = align256(off + static_cast<size_t>(R) * 8);
+  L.counts = p + off;
+  off = align256(off + static_cast<size_t>(R) * L.nch * 4);
+  L.list = p + off;
+  off = align256(off + static_cast<size_t>(R) * T1 * 8);
+  L.bytes = off;
+  return L;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   const int R = a.B * a.Hkv;
-  if (R == 0 || a.k == 0) {
-    return cudaSuccess;
-  }
-  TopkParams p;
+  if (R == 0 || a.k == 0) return cudaSuccess;
+  const int T1 = a.Tmax > 0 ? a.Tmax : 1;
+  if ((T1 + kChunk - 1) / kChunk > kMaxChunks) return cudaErrorNotSupported;
+  TopkParams p{};
   p.scores = a.scores;
   p.seq_lens = a.seq_lens;
   p.idx = a.idx;
@@ -317,22 +324,14 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.Tmax = a.Tmax;
   p.lim = a.maxp_tokens < a.Tmax ? a.maxp_tokens : a.Tmax;
   p.k = a.k;
-  p.L = make_layout(a.ws, R, a.Tmax, a.k);
-  cudaError_t e = cudaMemsetAsync(p.L.hist, 0, p.L.clear_bytes, stream);
-  if (e != cudaSuccess) return e;
-  if (a.Tmax > 0) {
-    dim3 grid((a.Tmax + kChunk - 1) / kChunk, R);
-    topk_hist_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
-    topk_filter_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
+  p.w = topk_ws_view(a.L);
+  dim3 grid(a.L.nch, R);
+  if (!a.histogram_done) {
+    cudaError_t e = cudaMemsetAsync(a.L.ghist, 0, a.L.zero_bytes, stream);
+    if (e != cudaSuccess) return e;
+    if (a.Tmax > 0) topk_hist_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
   }
-  int tw = a.Tmax < kWindow ? a.Tmax : kWindow;
-  int win_words = (tw + 31) / 32;
-  if (win_words < 1) win_words = 1;
-  const size_t smem = static_cast<size_t>(win_words) * 4;
-  e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  topk_select_kernel<<<R, kSelThreads, smem, stream>>>(p, win_words);
+  topk_filter_select_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
