@@ -99,3 +99,9 @@ def test_error_strings():
     import top_sparse_decode_label_gb300 as ds
     for st in (0, -1, -2, -3, -4, -5):
         assert ds.lib().ds_error_string(st).startswith(b"DS_")
+
+
+def test_binding_exports_every_name_it_lists():
+    import top_sparse_decode_label_gb300 as ds
+    for n in ds.__all__:
+        assert hasattr(ds, n), n

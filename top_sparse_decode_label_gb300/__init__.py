@@ -204,6 +204,11 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
     _check(st, "ds_sparse_decode")
 
 
+def ds_decode_kernel_launches(shape: Shape, k: int) -> int:
+    """Kernel launches one chained call makes (host-only query)."""
+    return lib().ds_decode_kernel_launches(ctypes.byref(shape), k)
+
+
 def ds_decode_num_splits(shape: Shape, k: int) -> int:
     """Split-KV count the chained call uses internally (host-only query)."""
     return lib().ds_decode_num_splits(ctypes.byref(shape), k)

@@ -16,7 +16,7 @@
 // 512-byte block of heads of each token (per-head label with many heads). A
 // persistent grid gives each CTA a contiguous range of units; the CTA streams
 // them through a ring of cp.async stages (16-byte copies, L1 bypassed, L2
-// evict-first, zero-fill past the request's length), so 64-128 KB per SM are
+// zero-fill past the request's length), so 64-128 KB per SM are
 // in flight without holding registers. Each of the 8 warps then reads 4
 // consecutive 512-byte pieces of a unit from shared memory: C/8 lanes hold one
 // C-wide row, every lane keeps the same (head, channel chunk) for the whole
@@ -98,7 +98,6 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
   const int G = p.Hq / p.Hkv;
   const long long u0 = blockIdx.x * p.units / gridDim.x;
   const long long u1 = (blockIdx.x + 1) * p.units / gridDim.x;
-  const uint64_t pol = l2_evict_first_policy();
 
   if (p.hist)
     for (int i = tid; i < RB * 1024; i += kScoreThreads) hist[i] = 0;
@@ -123,7 +122,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
         if (ok)
           src = p.label + ((static_cast<long long>(pid) * kPage + (t & (kPage - 1))) * p.HL + hb * HPB) * (C * 2) + byte;
       }
-      cp_async16_hint(dst + ch * 16, src, ok, pol);
+      cp_async16(dst + ch * 16, src, ok);
     }
   };
 
