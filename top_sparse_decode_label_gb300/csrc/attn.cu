@@ -351,30 +351,41 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   __threadfence();
   const long long rows = static_cast<long long>(p.B) * p.Hq;
   const long long qrow0 = static_cast<long long>(b) * p.Hq + g * G;
-  // Per-head log-sum-exp over the splits (kept in sm_l[0]).
+  // All split lse values of the group's heads in one round of loads, then the
+  // merge weights exp(lse_s - lse) in shared memory (reusing the ring).
+  float* sw = reinterpret_cast<float*>(ring);          // [S][G] weights
+  float* slse = sw + p.S * G;                          // [G] merged lse
+  for (int i = tid; i < p.S * G; i += kThreads) sw[i] = __ldcg(p.lse_part + (i / G) * rows + qrow0 + (i % G));
+  __syncthreads();
   if (tid < G) {
     float M = -INFINITY;
-    for (int s = 0; s < p.S; ++s) M = fmaxf(M, __ldcg(p.lse_part + s * rows + qrow0 + tid));
+    for (int s = 0; s < p.S; ++s) M = fmaxf(M, sw[s * G + tid]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int s = 0; s < p.S; ++s) L += expf(__ldcg(p.lse_part + s * rows + qrow0 + tid) - M);
-    sm_l[0][tid] = (M == -INFINITY) ? -INFINITY : M + logf(L);
+      for (int s = 0; s < p.S; ++s) L += expf(sw[s * G + tid] - M);
+    const float lse = (M == -INFINITY) ? -INFINITY : M + logf(L);
+    slse[tid] = lse;
+    for (int s = 0; s < p.S; ++s) {
+      const float ls = sw[s * G + tid];
+      sw[s * G + tid] = (ls == -INFINITY) ? 0.f : expf(ls - lse);
+    }
   }
   __syncthreads();
   for (int e = tid; e < G * kHeadDim; e += kThreads) {
     const int h = e / kHeadDim;
     const int d = e % kHeadDim;
-    const float lse = sm_l[0][h];
     float acc = 0.f;
-    if (lse != -INFINITY) {
-      for (int s = 0; s < p.S; ++s) {
-        const float ls = __ldcg(p.lse_part + s * rows + qrow0 + h);
-        if (ls == -INFINITY) continue;
-        acc = fmaf(expf(ls - lse), __ldcg(p.o_part + (s * rows + qrow0 + h) * kHeadDim + d), acc);
-      }
+    for (int s0 = 0; s0 < p.S; s0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = (s0 + i < p.S) ? __ldcg(p.o_part + ((s0 + i) * rows + qrow0 + h) * kHeadDim + d) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (s0 + i < p.S) acc = fmaf(sw[(s0 + i) * G + h], v[i], acc);
     }
     p.out[(qrow0 + h) * kHeadDim + d] = __float2bfloat16_rn(acc);
-    if (d == 0 && p.lse) p.lse[qrow0 + h] = lse;
+    if (d == 0 && p.lse) p.lse[qrow0 + h] = slse[h];
   }
   if (tid == 0) atomicExch(p.merge_done + bg, 0u);
 }

@@ -48,7 +48,7 @@ struct ScoreParams {
   float* scores;
   unsigned* err;
   int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb, k;
-  long long units;  // B * nhb * upb
+  int units;        // B * nhb * upb (< 2^31, checked on the host)
   int upb;          // units per (request, head block)
   int nst;          // cp.async ring stages
   int hist;         // build level-1 top-k histograms
@@ -62,8 +62,8 @@ __device__ __forceinline__ int clamp_len(const ScoreParams& p, int b) {
 }
 
 // Index of the CTA whose unit range holds unit i (ranges [c*U/n, (c+1)*U/n)).
-__device__ __forceinline__ long long cta_of(long long i, long long units, long long n) {
-  return ((i + 1) * n + units - 1) / units - 1;
+__device__ __forceinline__ int cta_of(long long i, long long units, long long n) {
+  return static_cast<int>(((i + 1) * n + units - 1) / units - 1);
 }
 
 // C: proxy width; NGR: groups fed by one label row (1 for a per-head label,
@@ -84,8 +84,6 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* ring = smem;
   unsigned* hist = reinterpret_cast<unsigned*>(smem + static_cast<size_t>(p.nst) * kUnitBytes);
-  __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_res[2];
   __shared__ int sh_last;
 
   const int tid = threadIdx.x;
@@ -96,18 +94,19 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
   const int tok_off = rin / HPB;
   const int hin = rin % HPB;
   const int G = p.Hq / p.Hkv;
-  const long long u0 = blockIdx.x * p.units / gridDim.x;
-  const long long u1 = (blockIdx.x + 1) * p.units / gridDim.x;
+  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.units / gridDim.x);
+  const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.units / gridDim.x);
 
   if (p.hist)
     for (int i = tid; i < RB * 1024; i += kScoreThreads) hist[i] = 0;
 
-  auto issue = [&](long long u, int stage) {
-    const long long bh = u / p.upb;
-    const int ui = static_cast<int>(u - bh * p.upb);
-    const int b = static_cast<int>(bh / p.nhb);
-    const int hb = static_cast<int>(bh - static_cast<long long>(b) * p.nhb);
+  // Copies unit (bh, ui) into ring stage `stage`.
+  auto issue = [&](int bh, int ui, int stage) {
+    const int b = (p.nhb == 1) ? bh : bh / p.nhb;
+    const int hb = bh - b * p.nhb;
     const int T = clamp_len(p, b);
+    const int* pt = p.page_table + b * p.maxp;
+    const long long head0 = static_cast<long long>(hb) * HPB * (C * 2);
     unsigned char* dst = ring + stage * kUnitBytes;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
@@ -117,17 +116,19 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
       bool ok = t < T;
       const uint8_t* src = p.label;
       if (ok) {
-        const int pid = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + (t >> 6));
+        const int pid = __ldg(pt + (t >> 6));
         ok = pid >= 0 && pid < p.num_pages;
-        if (ok)
-          src = p.label + ((static_cast<long long>(pid) * kPage + (t & (kPage - 1))) * p.HL + hb * HPB) * (C * 2) + byte;
+        if (ok) {
+          const int slot = pid * kPage + (t & (kPage - 1));
+          src = p.label + static_cast<long long>(slot) * (p.HL * C * 2) + head0 + byte;
+        }
       }
       cp_async16(dst + ch * 16, src, ok);
     }
   };
 
-  long long cur = -1;
-  long long flushed_at = 0;  // unit of the last histogram flush (16-bit counters must not overflow)
+  int cur = -1;
+  int flushed_at = 0;  // unit of the last histogram flush (16-bit counters must not overflow)
   int b = 0, hb = 0, T = 0, hl = 0;
   bool sel = false;
   float q[NGR][8];
@@ -156,43 +157,50 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
       __threadfence();
       __syncthreads();
       if (tid == 0) {
-        const long long s = cur * p.upb;
-        const long long expected = cta_of(s + p.upb - 1, p.units, gridDim.x) - cta_of(s, p.units, gridDim.x) + 1;
+        const long long s = static_cast<long long>(cur) * p.upb;
+        const int expected = cta_of(s + p.upb - 1, p.units, gridDim.x) - cta_of(s, p.units, gridDim.x) + 1;
         const unsigned prev = atomicAdd(p.tw.done1 + cur, 1u);
-        sh_last = (prev + 1 == expected);
+        sh_last = (prev + 1 == static_cast<unsigned>(expected));
       }
       __syncthreads();
       if (sh_last) {
         __threadfence();
-        for (int r = 0; r < RB; ++r) {
+        for (int r = warp; r < RB; r += kWarps) {
           const int g = (NGR == 1) ? hb * HPB + r : r;
-          level1_threshold(p.tw, b * p.Hkv + g, p.k, sh_scan, sh_res);
+          level1_threshold_warp(p.tw, b * p.Hkv + g, p.k);
         }
         if (tid == 0) atomicExch(p.tw.done1 + cur, 0u);
       }
     }
   };
 
+  // Compute cursor (bh, ui) and issue cursor, advanced without divisions.
+  int c_bh = u0 / p.upb;
+  int c_ui = u0 - c_bh * p.upb;
+  int i_bh = c_bh, i_ui = c_ui;
   for (int s = 0; s < p.nst; ++s) {
-    if (u0 + s < u1) issue(u0 + s, s);
+    if (u0 + s < u1) {
+      issue(i_bh, i_ui, s);
+      if (++i_ui == p.upb) { i_ui = 0; ++i_bh; }
+    }
     cp_async_commit();
   }
 
-  for (long long u = u0; u < u1; ++u) {
-    const int stage = static_cast<int>((u - u0) % p.nst);
+  int stage = 0;
+  for (int u = u0; u < u1; ++u) {
     cp_async_wait_dyn(p.nst - 1);
     __syncthreads();
-    const long long bh = u / p.upb;
+    const int bh = c_bh;
     if (bh != cur) {
       if (cur >= 0 && p.hist) finish();
       cur = bh;
       flushed_at = u;
-      b = static_cast<int>(bh / p.nhb);
-      hb = static_cast<int>(bh - static_cast<long long>(b) * p.nhb);
+      b = (p.nhb == 1) ? bh : bh / p.nhb;
+      hb = bh - b * p.nhb;
       hl = hb * HPB + hin;
       T = clamp_len(p, b);
       sel = p.hist && needs_selection(p.k, T);
-      if (tid == 0 && hb == 0 && u == bh * p.upb) {
+      if (tid == 0 && hb == 0 && c_ui == 0) {
         const int raw = __ldg(p.seq_lens + b);
         if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
       }
@@ -210,7 +218,6 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
         }
       }
     }
-
     if (sel && (u - flushed_at) * TPU > 60000) {
       flush_hist();
       __syncthreads();
@@ -218,8 +225,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
     }
 
     // ---- dot products of this unit
-    const int ui = static_cast<int>(u - bh * p.upb);
-    const int tbase = ui * TPU;
+    const int tbase = c_ui * TPU;
     if (tbase < T) {
       const unsigned char* src = ring + stage * kUnitBytes + (warp * U) * 512 + lane * 16;
       float acc[V];
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
         const int g = (NGR == 1) ? hl : n;
         if (writer && t < T) {
           float sc = acc[kk];
-          const int pid = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + (t >> 6));
+          const int pid = __ldg(p.page_table + b * p.maxp + (t >> 6));
           if (pid < 0 || pid >= p.num_pages) {
             sc = __int_as_float(0x7fc00000);
             flag_error(p.err, 2u);
@@ -263,8 +269,13 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
       }
     }
     __syncthreads();
-    if (u + p.nst < u1) issue(u + p.nst, stage);
+    if (u + p.nst < u1) {
+      issue(i_bh, i_ui, stage);
+      if (++i_ui == p.upb) { i_ui = 0; ++i_bh; }
+    }
     cp_async_commit();
+    if (++c_ui == p.upb) { c_ui = 0; ++c_bh; }
+    if (++stage == p.nst) stage = 0;
   }
   if (cur >= 0 && p.hist) finish();
   cp_async_wait<0>();
@@ -367,8 +378,11 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.Tmax = a.Tmax;
   p.nhb = nhb;
   p.k = a.k;
-  p.upb = static_cast<int>((static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu);
-  p.units = static_cast<long long>(a.B) * nhb * p.upb;
+  const long long upb = (static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu;
+  const long long units = static_cast<long long>(a.B) * nhb * upb;
+  if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;
+  p.upb = static_cast<int>(upb);
+  p.units = static_cast<int>(units);
   p.hist = a.topk != nullptr;
   if (p.hist) p.tw = topk_ws_view(*a.topk);
   const int hist_bytes = p.hist ? rb * 4096 : 0;

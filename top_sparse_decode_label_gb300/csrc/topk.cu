@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kElems = kChunk / kChunkThreads;   // 16 scores per thread
 constexpr int kMaxChunks = 4096;                 // rows of up to 16M tokens
+constexpr int kListCap = 8192;                   // kept entries selected from shared memory (64 KB)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -43,7 +44,7 @@ struct TopkParams {
   const int32_t* seq_lens;
   int32_t* idx;
   unsigned* err;
-  int Hkv, Tmax, lim, k;
+  int Hkv, Tmax, lim, k, R;
   TopkWs w;
 };
 
@@ -113,74 +114,19 @@ struct ListWalker {
   }
 };
 
-__global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const TopkParams p) {
-  __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_res[2];
-  __shared__ int sh_last;
-  __shared__ unsigned sh_hist[kBins1];
-  __shared__ unsigned sh_pref[kMaxChunks + 1];
+// Select phase of one row, run by the CTA that completed the row's filter.
+// `lst` holds the kept entries of the row in token order when M <= cap
+// (copied to shared memory); otherwise they are walked in global memory.
+__device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigned b1, unsigned above1,
+                           uint2* sm_list, int cap, unsigned* sh_pref, unsigned* sh_hist, unsigned* sh_scan,
+                           unsigned* sh_res) {
   const int tid = threadIdx.x;
-  const int row = blockIdx.y;
-  const int b = row / p.Hkv;
-  const int T = row_len(p, b, false);
   const int keff = min(p.k, T);
   int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
-  if (!needs_selection(p.k, T)) {
-    if (blockIdx.x == 0)
-      for (int i = tid; i < p.k; i += blockDim.x) out[i] = (i < keff) ? i : -1;
-    return;
-  }
-  const int nch = (T + kChunk - 1) / kChunk;
-  const int c = blockIdx.x;
-  if (c >= nch) return;
-  const uint2 st = __ldcg(p.w.row_state + row);
-  const unsigned b1 = st.x;
-  const unsigned above1 = st.y;
-
-  // ---- filter: keep key >> 21 >= b1 of this chunk, in token order
-  const int c0 = c * kChunk;
-  const int c1 = min(T, c0 + kChunk);
-  const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-  const int t0 = c0 + tid * kElems;
-  uint32_t keys[kElems];
-  unsigned flags = 0, cnt = 0;
-  const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1);
-  if (vec) {
-#pragma unroll
-    for (int i = 0; i < kElems; i += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(s + t0 + i);
-      keys[i] = order_key(v.x);
-      keys[i + 1] = order_key(v.y);
-      keys[i + 2] = order_key(v.z);
-      keys[i + 3] = order_key(v.w);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
-  }
-#pragma unroll
-  for (int i = 0; i < kElems; ++i) {
-    if (t0 + i < c1 && (keys[i] >> 21) >= b1) {
-      flags |= 1u << i;
-      ++cnt;
-    }
-  }
-  unsigned total;
-  unsigned pos = block_excl_scan(cnt, sh_scan, &total);
-  uint2* lst = p.w.list + static_cast<size_t>(row) * p.Tmax + c0;
-#pragma unroll
-  for (int i = 0; i < kElems; ++i)
-    if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
-  if (tid == 0) p.w.counts[static_cast<size_t>(row) * p.w.nch + c] = total;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh_last = (atomicAdd(p.w.done2 + row, 1u) + 1 == static_cast<unsigned>(nch));
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-
-  // ---- select: this CTA completed the row
   const unsigned* counts = p.w.counts + static_cast<size_t>(row) * p.w.nch;
+  const uint2* base = p.w.list + static_cast<size_t>(row) * p.Tmax;
+
+  // Chunk prefix of the list lengths.
   const int cpt = (nch + kChunkThreads - 1) / kChunkThreads;
   {
     unsigned mine = 0;
@@ -195,19 +141,50 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   }
   __syncthreads();
   const int M = static_cast<int>(sh_pref[nch]);
-  const uint2* base = p.w.list + static_cast<size_t>(row) * p.Tmax;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
+  const bool in_smem = M <= cap;
+  if (in_smem) {
+    // Gather the list into shared memory, 8 independent loads in flight per thread.
+    for (int e0 = tid; e0 < M; e0 += 8 * kChunkThreads) {
+      uint2 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = e0 + i * kChunkThreads;
+        if (e < M) {
+          int lo = 0, hi = nch - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sh_pref[mid] <= static_cast<unsigned>(e)) lo = mid; else hi = mid - 1;
+          }
+          v[i] = __ldcg(base + static_cast<size_t>(lo) * kChunk + (e - static_cast<int>(sh_pref[lo])));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = e0 + i * kChunkThreads;
+        if (e < M) sm_list[e] = v[i];
+      }
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int e, ListWalker& wk) -> uint2 { return in_smem ? sm_list[e] : wk.next(); };
   const unsigned need = static_cast<unsigned>(keff) - above1;
 
   // Level 2: bits 10..20 of the entries in bin b1.
   for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
-  for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
-    const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-    for (int j = lane; j < n; j += 32) {
-      const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+  if (in_smem) {
+    for (int e = tid; e < M; e += kChunkThreads) {
+      const uint32_t key = sm_list[e].x;
       if ((key >> 21) == b1) atomicAdd(&sh_hist[(key >> 10) & 2047u], 1u);
+    }
+  } else {
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
+      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
+      for (int j = lane; j < n; j += 32) {
+        const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+        if ((key >> 21) == b1) atomicAdd(&sh_hist[(key >> 10) & 2047u], 1u);
+      }
     }
   }
   __syncthreads();
@@ -218,11 +195,19 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   const uint32_t hi22 = (b1 << 11) | d2;
   for (int i = tid; i < 1024; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
-  for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
-    const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-    for (int j = lane; j < n; j += 32) {
-      const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+  if (in_smem) {
+    for (int e = tid; e < M; e += kChunkThreads) {
+      const uint32_t key = sm_list[e].x;
       if ((key >> 10) == hi22) atomicAdd(&sh_hist[key & 1023u], 1u);
+    }
+  } else {
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
+      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
+      for (int j = lane; j < n; j += 32) {
+        const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
+        if ((key >> 10) == hi22) atomicAdd(&sh_hist[key & 1023u], 1u);
+      }
     }
   }
   __syncthreads();
@@ -233,7 +218,7 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   const uint32_t thr = (hi22 << 10) | d3;
   __syncthreads();
 
-  // Ordered output over the list: thread segments, prefix sums across threads.
+  // Ordered output: thread segments in token order, prefix sums across threads.
   const int seg = (M + kChunkThreads - 1) / kChunkThreads;
   const int e0 = min(M, tid * seg);
   const int e1 = min(M, e0 + seg);
@@ -241,19 +226,17 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   unsigned eq_base = 0;
   if (eq_total > r_eq) {
     unsigned eqc = 0;
-    if (e0 < e1) {
-      wk.seek(e0, nch);
-      for (int e = e0; e < e1; ++e) eqc += (wk.next().x == thr);
-    }
+    if (!in_smem && e0 < e1) wk.seek(e0, nch);
+    for (int e = e0; e < e1; ++e) eqc += (key_at(e, wk).x == thr);
     unsigned tot;
     eq_base = block_excl_scan(eqc, sh_scan, &tot);
   }
   unsigned selc = 0;
-  if (e0 < e1) {
-    wk.seek(e0, nch);
+  {
+    if (!in_smem && e0 < e1) wk.seek(e0, nch);
     unsigned eq = eq_base;
     for (int e = e0; e < e1; ++e) {
-      const uint32_t key = wk.next().x;
+      const uint32_t key = key_at(e, wk).x;
       if (key > thr) {
         ++selc;
       } else if (key == thr) {
@@ -264,11 +247,11 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   }
   unsigned tot_sel;
   unsigned opos = block_excl_scan(selc, sh_scan, &tot_sel);
-  if (e0 < e1) {
-    wk.seek(e0, nch);
+  {
+    if (!in_smem && e0 < e1) wk.seek(e0, nch);
     unsigned eq = eq_base;
     for (int e = e0; e < e1; ++e) {
-      const uint2 v = wk.next();
+      const uint2 v = key_at(e, wk);
       bool keep = v.x > thr;
       if (v.x == thr) {
         keep = eq < r_eq;
@@ -281,7 +264,95 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
     }
   }
   for (int i = keff + tid; i < p.k; i += blockDim.x) out[i] = -1;
-  if (tid == 0) atomicExch(p.w.done2 + row, 0u);
+  __syncthreads();
+}
+
+// Persistent filter: CTAs walk (row, chunk) work items; the CTA that completes
+// a row's last chunk selects the row.
+__global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const TopkParams p, int cap) {
+  extern __shared__ __align__(16) unsigned char dsmem[];
+  uint2* sm_list = reinterpret_cast<uint2*>(dsmem);                         // [cap]
+  unsigned* sh_pref = reinterpret_cast<unsigned*>(dsmem + static_cast<size_t>(cap) * 8);  // [nch + 1]
+  __shared__ unsigned sh_scan[33];
+  __shared__ unsigned sh_res[2];
+  __shared__ int sh_last;
+  __shared__ unsigned sh_hist[kBins1];
+  const int tid = threadIdx.x;
+  const int nitems = p.R * p.w.nch;
+  const int w0 = static_cast<int>(static_cast<long long>(blockIdx.x) * nitems / gridDim.x);
+  const int w1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * nitems / gridDim.x);
+  for (int item = w0; item < w1; ++item) {
+    const int row = item / p.w.nch;
+    const int c = item - row * p.w.nch;
+    const int b = row / p.Hkv;
+    const int T = row_len(p, b, false);
+    const int keff = min(p.k, T);
+    if (!needs_selection(p.k, T)) {
+      if (c == 0) {
+        int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
+        for (int i = tid; i < p.k; i += blockDim.x) out[i] = (i < keff) ? i : -1;
+      }
+      continue;
+    }
+    const int nch = (T + kChunk - 1) / kChunk;
+    if (c >= nch) continue;
+    const uint2 st = __ldcg(p.w.row_state + row);
+    const unsigned b1 = st.x;
+
+    // ---- filter: keep key >> 21 >= b1 of this chunk, in token order
+    const int c0 = c * kChunk;
+    const int c1 = min(T, c0 + kChunk);
+    const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
+    const int t0 = c0 + tid * kElems;
+    uint32_t keys[kElems];
+    unsigned flags = 0, cnt = 0;
+    const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1);
+    if (vec) {
+#pragma unroll
+      for (int i = 0; i < kElems; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(s + t0 + i);
+        keys[i] = order_key(v.x);
+        keys[i + 1] = order_key(v.y);
+        keys[i + 2] = order_key(v.z);
+        keys[i + 3] = order_key(v.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < kElems; ++i) {
+      if (t0 + i < c1 && (keys[i] >> 21) >= b1) {
+        flags |= 1u << i;
+        ++cnt;
+      }
+    }
+    unsigned total;
+    unsigned pos = block_excl_scan(cnt, sh_scan, &total);
+    uint2* lst = p.w.list + static_cast<size_t>(row) * p.Tmax + c0;
+#pragma unroll
+    for (int i = 0; i < kElems; ++i)
+      if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
+    if (tid == 0) p.w.counts[static_cast<size_t>(row) * p.w.nch + c] = total;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sh_last = (atomicAdd(p.w.done2 + row, 1u) + 1 == static_cast<unsigned>(nch));
+    __syncthreads();
+    if (!sh_last) continue;
+    __threadfence();
+    select_row(p, row, T, nch, b1, st.y, sm_list, cap, sh_pref, sh_hist, sh_scan, sh_res);
+    if (tid == 0) atomicExch(p.w.done2 + row, 0u);
+  }
+}
+
+cudaError_t allow_select_smem(int bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(topk_filter_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  return e;
 }
 
 }  // namespace
@@ -325,13 +396,24 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.lim = a.maxp_tokens < a.Tmax ? a.maxp_tokens : a.Tmax;
   p.k = a.k;
   p.w = topk_ws_view(a.L);
-  dim3 grid(a.L.nch, R);
+  p.R = R;
   if (!a.histogram_done) {
     cudaError_t e = cudaMemsetAsync(a.L.ghist, 0, a.L.zero_bytes, stream);
     if (e != cudaSuccess) return e;
-    if (a.Tmax > 0) topk_hist_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
+    if (a.Tmax > 0) topk_hist_kernel<<<dim3(a.L.nch, R), kChunkThreads, 0, stream>>>(p);
   }
-  topk_filter_select_kernel<<<grid, kChunkThreads, 0, stream>>>(p);
+  // Shared memory: the selected row's kept list (up to kListCap entries) and the chunk prefix.
+  const int smem = kListCap * 8 + (a.L.nch + 1) * 4;
+  cudaError_t e = allow_select_smem(smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_filter_select_kernel, kChunkThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  long long blocks = static_cast<long long>(sm_count()) * per_sm;
+  const long long items = static_cast<long long>(R) * a.L.nch;
+  if (items < blocks) blocks = items;
+  topk_filter_select_kernel<<<static_cast<unsigned>(blocks), kChunkThreads, smem, stream>>>(p, kListCap);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,45 @@ __device__ __forceinline__ void level1_threshold(const TopkWs& w, int row, int k
   __syncthreads();
 }
 
+// Level-1 epilogue of one row run by a single warp: lane l holds bins
+// [2048 - 64(l+1), 2048 - 64 l) in registers (one round of loads), a warp
+// prefix over lanes from the top finds the lane holding the K_eff-th key,
+// which scans its bins. Records (b1, above) and clears the histogram.
+__device__ __forceinline__ void level1_threshold_warp(const TopkWs& w, int row, int keff) {
+  const int lane = threadIdx.x & 31;
+  unsigned* h = w.ghist + static_cast<size_t>(row) * kBins1 + (kBins1 - 64 * (lane + 1));
+  uint4 v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __ldcg(reinterpret_cast<const uint4*>(h) + i);
+  unsigned c = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c += v[i].x + v[i].y + v[i].z + v[i].w;
+  const unsigned inc = warp_incl_scan(c);
+  const unsigned before = inc - c;
+  const unsigned need = static_cast<unsigned>(keff);
+  if (before < need && inc >= need) {
+    unsigned run = before;
+    unsigned bin = 0, above = 0;
+    bool found = false;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+      const unsigned e[4] = {v[i].w, v[i].z, v[i].y, v[i].x};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!found && run + e[q] >= need) {
+          found = true;
+          bin = kBins1 - 64 * (lane + 1) + 4 * i + (3 - q);
+          above = run;
+        }
+        run += e[q];
+      }
+    }
+    w.row_state[row] = make_uint2(bin, above);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) __stcg(reinterpret_cast<uint4*>(h) + i, make_uint4(0u, 0u, 0u, 0u));
+}
+
 // Rows that need a selection at all: 0 < K_eff < T.
 __device__ __forceinline__ bool needs_selection(int k, int T) { return k > 0 && k < T; }
 
