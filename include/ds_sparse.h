@@ -68,6 +68,7 @@ typedef enum {
 #define DS_DEVERR_SEQ_LEN   1u   /* seq_lens[b] < 0 or > min(max_seq_len, max_pages_per_req*page_size); clamped */
 #define DS_DEVERR_PAGE_ID   2u   /* a page-table entry outside [0, num_pages); its tokens were skipped */
 #define DS_DEVERR_TOKEN_IDX 4u   /* an index entry outside [0, seq_lens[b]) before the -1 padding; skipped */
+#define DS_DEVERR_TIMEOUT   8u   /* a bounded wait for an asynchronous copy gave up; the call's results are invalid */
 
 typedef struct {
   int batch;             /* B, requests in the step (>= 0) */

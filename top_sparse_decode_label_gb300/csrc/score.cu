@@ -14,14 +14,17 @@
 // HBM-bound scan. The label cache is cut into 16 KB units: consecutive tokens
 // of one request, either whole token rows (HL*C*2 bytes <= 512) or one
 // 512-byte block of heads of each token (per-head label with many heads). A
-// persistent grid gives each CTA a contiguous range of units; the CTA streams
-// them through a ring of cp.async stages (16-byte copies, L1 bypassed, L2
-// zero-fill past the request's length), so 64-128 KB per SM are
-// in flight without holding registers. Each of the 8 warps then reads 4
-// consecutive 512-byte pieces of a unit from shared memory: C/8 lanes hold one
-// C-wide row, every lane keeps the same (head, channel chunk) for the whole
-// unit, its slice of the summed query sits in registers, and the partial dot
-// products of a lane group are combined by a transposed butterfly.
+// persistent grid gives each CTA a contiguous range of units. In each CTA a
+// producer warp streams the units into a ring of shared-memory stages with
+// bulk (TMA) copies -- one per page span or head block -- that complete on the
+// stage's mbarrier; eight consumer warps wait on it, compute, and release the
+// stage through a second mbarrier, so copies run ahead by the ring depth with
+// no CTA-wide barrier per unit. Each consumer warp reads 4 consecutive
+// 512-byte pieces of a unit: C/8 lanes hold one C-wide row, every lane keeps
+// the same (head, channel chunk) for the whole unit, its slice of the summed
+// query sits in registers, packed fp32 FMAs form the partial dot products, and
+// a transposed butterfly combines them across the row's lanes. Every mbarrier
+// wait is bounded: on timeout it sets DS_DEVERR_TIMEOUT and carries on.
 //
 // With a top-k to follow, the kernel also builds each row's histogram of the
 // top 11 bits of the order-preserving score key in shared memory (two 16-bit
@@ -36,9 +39,12 @@ namespace ds {
 
 namespace {
 
-constexpr int kScoreThreads = 256;
-constexpr int kUnitBytes = 16384;               // 32 warp instructions of 512 B
-constexpr int kWarps = kScoreThreads / 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kScoreThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kUnitBytes = 16384;                     // 32 pieces of 512 B
+constexpr int kMaxStages = 12;
+constexpr uint32_t kWaitLimit = 1u << 22;             // bounded mbarrier polls
 
 struct ScoreParams {
   const uint16_t* qp;
@@ -50,7 +56,7 @@ struct ScoreParams {
   int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb, k;
   int units;        // B * nhb * upb (< 2^31, checked on the host)
   int upb;          // units per (request, head block)
-  int nst;          // cp.async ring stages
+  int nst;          // ring stages
   int hist;         // build level-1 top-k histograms
   TopkWs tw;
 };
@@ -69,73 +75,120 @@ __device__ __forceinline__ int cta_of(long long i, long long units, long long n)
 // C: proxy width; NGR: groups fed by one label row (1 for a per-head label,
 // Hkv for a shared index key); TPI: tokens covered by one 512-byte piece.
 template <int C, int NGR, int TPI>
-__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreParams p) {
-  constexpr int LPR = C / 8;                    // lanes per C-wide row
-  constexpr int RPI = 32 / LPR;                 // rows per 512-byte piece
-  constexpr int HPB = RPI / TPI;                // label heads per piece
-  constexpr int BR = 512 / TPI;                 // bytes of one token's block
-  constexpr int TPU = kUnitBytes / BR;          // tokens per unit
-  constexpr int U = kUnitBytes / 512 / kWarps;  // pieces per warp per unit (4)
-  constexpr int V = U * NGR;                    // partial sums per lane
-  constexpr int PER = V >= LPR ? V / LPR : 1;   // finished sums per lane
-  constexpr int RB = (NGR == 1) ? HPB : NGR;    // histogram rows of a (request, head block)
-  constexpr int CPT = kUnitBytes / 16 / kScoreThreads;
+__global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score_kernel(const ScoreParams p) {
+  constexpr int LPR = C / 8;                             // lanes per C-wide row
+  constexpr int RPI = 32 / LPR;                          // rows per 512-byte piece
+  constexpr int HPB = RPI / TPI;                         // label heads per piece
+  constexpr int BR = 512 / TPI;                          // bytes of one token's block
+  constexpr int TPU = kUnitBytes / BR;                   // tokens per unit
+  constexpr int U = kUnitBytes / 512 / kConsumerWarps;   // pieces per consumer warp per unit (4)
+  constexpr int V = U * NGR;                             // partial sums per lane
+  constexpr int PER = V >= LPR ? V / LPR : 1;            // finished sums per lane
+  constexpr int RB = (NGR == 1) ? HPB : NGR;             // histogram rows of a (request, head block)
 
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   unsigned* hist = reinterpret_cast<unsigned*>(smem + static_cast<size_t>(p.nst) * kUnitBytes);
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ int sh_last;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int chunk = lane % LPR;
-  const int rin = lane / LPR;
-  const int tok_off = rin / HPB;
-  const int hin = rin % HPB;
-  const int G = p.Hq / p.Hkv;
   const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.units / gridDim.x);
   const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.units / gridDim.x);
 
-  if (p.hist)
-    for (int i = tid; i < RB * 1024; i += kScoreThreads) hist[i] = 0;
+  if (tid == 0) {
+    for (int s = 0; s < p.nst; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  if (p.hist && tid < kConsumerThreads)
+    for (int i = tid; i < RB * 1024; i += kConsumerThreads) hist[i] = 0;
+  __syncthreads();
 
-  // Copies unit (bh, ui) into ring stage `stage`.
-  auto issue = [&](int bh, int ui, int stage) {
-    const int b = (p.nhb == 1) ? bh : bh / p.nhb;
-    const int hb = bh - b * p.nhb;
-    const int T = clamp_len(p, b);
-    const int* pt = p.page_table + b * p.maxp;
-    const long long head0 = static_cast<long long>(hb) * HPB * (C * 2);
-    unsigned char* dst = ring + stage * kUnitBytes;
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      const int ch = c * kScoreThreads + tid;
-      const int t = ui * TPU + ch / (BR / 16);
-      const int byte = (ch % (BR / 16)) * 16;
-      bool ok = t < T;
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer warp
+    int bh = u0 / p.upb;
+    int ui = u0 - bh * p.upb;
+    int s = 0;
+    uint32_t fill = 0;  // how many times stage s has been filled before
+    for (int u = u0; u < u1; ++u) {
+      if (fill > 0 && !mbar_wait(&empty_bar[s], (fill - 1) & 1u, kWaitLimit) && lane == 0)
+        flag_error(p.err, 8u);
+      const int b = (p.nhb == 1) ? bh : bh / p.nhb;
+      const int hb = bh - b * p.nhb;
+      const int T = clamp_len(p, b);
+      const int t0 = ui * TPU;
+      const int t1 = min(T, t0 + TPU);
+      const int* pt = p.page_table + b * p.maxp;
+      unsigned char* dst = ring + s * kUnitBytes;
+      uint32_t nbytes = 0;
       const uint8_t* src = p.label;
-      if (ok) {
-        const int pid = __ldg(pt + (t >> 6));
-        ok = pid >= 0 && pid < p.num_pages;
-        if (ok) {
-          const int slot = pid * kPage + (t & (kPage - 1));
-          src = p.label + static_cast<long long>(slot) * (p.HL * C * 2) + head0 + byte;
+      int dst_off = 0;
+      if (p.nhb == 1) {
+        // Whole token rows: one contiguous span per page of the unit.
+        const int pg = (t0 >> 6) + lane;
+        const int ts = max(t0, pg * kPage);
+        const int te = min(t1, pg * kPage + kPage);
+        if (ts < te) {
+          const int pid = __ldg(pt + pg);
+          if (pid >= 0 && pid < p.num_pages) {
+            nbytes = static_cast<uint32_t>(te - ts) * BR;
+            src = p.label + static_cast<long long>(pid * kPage + (ts & (kPage - 1))) * BR;
+            dst_off = (ts - t0) * BR;
+          } else {
+            flag_error(p.err, 2u);
+          }
+        }
+      } else {
+        // One 512-byte block of heads per token (TPU == 32 tokens, one per lane).
+        const int t = t0 + lane;
+        if (lane < TPU && t < t1) {
+          const int pid = __ldg(pt + (t >> 6));
+          if (pid >= 0 && pid < p.num_pages) {
+            nbytes = BR;
+            src = p.label + (static_cast<long long>(pid * kPage + (t & (kPage - 1))) * p.HL + hb * HPB) * (C * 2);
+            dst_off = lane * BR;
+          } else {
+            flag_error(p.err, 2u);
+          }
         }
       }
-      cp_async16(dst + ch * 16, src, ok);
+      uint32_t total = nbytes;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], total);
+      __syncwarp();
+      if (nbytes) bulk_g2s(dst + dst_off, src, nbytes, &full_bar[s]);
+      if (++s == p.nst) {
+        s = 0;
+        ++fill;
+      }
+      if (++ui == p.upb) {
+        ui = 0;
+        ++bh;
+      }
     }
-  };
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const int chunk = lane % LPR;
+    const int rin = lane / LPR;
+    const int tok_off = rin / HPB;
+    const int hin = rin % HPB;
+    const int G = p.Hq / p.Hkv;
+    int cur = -1;
+    int flushed_at = 0;  // unit of the last histogram flush (16-bit counters must not overflow)
+    int b = 0, hb = 0, T = 0, hl = 0;
+    bool sel = false;
+    float2 q[NGR][4];
 
-  int cur = -1;
-  int flushed_at = 0;  // unit of the last histogram flush (16-bit counters must not overflow)
-  int b = 0, hb = 0, T = 0, hl = 0;
-  bool sel = false;
-  float q[NGR][8];
-
-  // Adds the CTA's shared histogram of (b, hb) into the global one and clears it.
-  auto flush_hist = [&]() {
-      for (int i = tid; i < RB * 1024; i += kScoreThreads) {
+    // Adds the CTA's shared histogram of (b, hb) into the global one and clears it.
+    auto flush_hist = [&]() {
+      for (int i = tid; i < RB * 1024; i += kConsumerThreads) {
         const unsigned v = hist[i];
         if (v) {
           const int r = i >> 10;
@@ -147,138 +200,130 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(const ScoreP
           hist[i] = 0;
         }
       }
-  };
-  // Leaving (b, hb): flush, count this CTA done for (b, hb), and let the
-  // last CTA compute the level-1 thresholds of its rows.
-  auto finish = [&]() {
-    __syncthreads();
-    if (sel) {
-      flush_hist();
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const long long s = static_cast<long long>(cur) * p.upb;
-        const int expected = cta_of(s + p.upb - 1, p.units, gridDim.x) - cta_of(s, p.units, gridDim.x) + 1;
-        const unsigned prev = atomicAdd(p.tw.done1 + cur, 1u);
-        sh_last = (prev + 1 == static_cast<unsigned>(expected));
-      }
-      __syncthreads();
-      if (sh_last) {
+    };
+    // Leaving (b, hb): flush, count this CTA done for (b, hb), and let the
+    // last CTA compute the level-1 thresholds of its rows.
+    auto finish = [&]() {
+      named_barrier(1, kConsumerThreads);
+      if (sel) {
+        flush_hist();
         __threadfence();
-        for (int r = warp; r < RB; r += kWarps) {
-          const int g = (NGR == 1) ? hb * HPB + r : r;
-          level1_threshold_warp(p.tw, b * p.Hkv + g, p.k);
+        named_barrier(1, kConsumerThreads);
+        if (tid == 0) {
+          const long long st = static_cast<long long>(cur) * p.upb;
+          const int expected = cta_of(st + p.upb - 1, p.units, gridDim.x) - cta_of(st, p.units, gridDim.x) + 1;
+          const unsigned prev = atomicAdd(p.tw.done1 + cur, 1u);
+          sh_last = (prev + 1 == static_cast<unsigned>(expected));
         }
-        if (tid == 0) atomicExch(p.tw.done1 + cur, 0u);
-      }
-    }
-  };
-
-  // Compute cursor (bh, ui) and issue cursor, advanced without divisions.
-  int c_bh = u0 / p.upb;
-  int c_ui = u0 - c_bh * p.upb;
-  int i_bh = c_bh, i_ui = c_ui;
-  for (int s = 0; s < p.nst; ++s) {
-    if (u0 + s < u1) {
-      issue(i_bh, i_ui, s);
-      if (++i_ui == p.upb) { i_ui = 0; ++i_bh; }
-    }
-    cp_async_commit();
-  }
-
-  int stage = 0;
-  for (int u = u0; u < u1; ++u) {
-    cp_async_wait_dyn(p.nst - 1);
-    __syncthreads();
-    const int bh = c_bh;
-    if (bh != cur) {
-      if (cur >= 0 && p.hist) finish();
-      cur = bh;
-      flushed_at = u;
-      b = (p.nhb == 1) ? bh : bh / p.nhb;
-      hb = bh - b * p.nhb;
-      hl = hb * HPB + hin;
-      T = clamp_len(p, b);
-      sel = p.hist && needs_selection(p.k, T);
-      if (tid == 0 && hb == 0 && c_ui == 0) {
-        const int raw = __ldg(p.seq_lens + b);
-        if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
-      }
-#pragma unroll
-      for (int n = 0; n < NGR; ++n) {
-        const int g = (NGR == 1) ? hl : n;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[n][i] = 0.f;
-        for (int h = g * G; h < (g + 1) * G; ++h) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.qp + (static_cast<long long>(b) * p.Hq + h) * C + chunk * 8));
-          q[n][0] += bf16_lo(w.x); q[n][1] += bf16_hi(w.x);
-          q[n][2] += bf16_lo(w.y); q[n][3] += bf16_hi(w.y);
-          q[n][4] += bf16_lo(w.z); q[n][5] += bf16_hi(w.z);
-          q[n][6] += bf16_lo(w.w); q[n][7] += bf16_hi(w.w);
+        named_barrier(1, kConsumerThreads);
+        if (sh_last) {
+          __threadfence();
+          for (int r = warp; r < RB; r += kConsumerWarps) {
+            const int g = (NGR == 1) ? hb * HPB + r : r;
+            level1_threshold_warp(p.tw, b * p.Hkv + g, p.k);
+          }
+          if (tid == 0) atomicExch(p.tw.done1 + cur, 0u);
         }
+        named_barrier(1, kConsumerThreads);
       }
-    }
-    if (sel && (u - flushed_at) * TPU > 60000) {
-      flush_hist();
-      __syncthreads();
-      flushed_at = u;
-    }
+    };
 
-    // ---- dot products of this unit
-    const int tbase = c_ui * TPU;
-    if (tbase < T) {
-      const unsigned char* src = ring + stage * kUnitBytes + (warp * U) * 512 + lane * 16;
-      float acc[V];
-#pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
-        const uint4 x = *reinterpret_cast<const uint4*>(src + uu * 512);
-        const float f0 = bf16_lo(x.x), f1 = bf16_hi(x.x), f2 = bf16_lo(x.y), f3 = bf16_hi(x.y);
-        const float f4 = bf16_lo(x.z), f5 = bf16_hi(x.z), f6 = bf16_lo(x.w), f7 = bf16_hi(x.w);
+    int bh = u0 / p.upb;
+    int ui = u0 - bh * p.upb;
+    int s = 0;
+    uint32_t fill = 0;
+    for (int u = u0; u < u1; ++u) {
+      const bool ok = mbar_wait(&full_bar[s], fill & 1u, kWaitLimit);
+      if (!ok && lane == 0) flag_error(p.err, 8u);
+      if (bh != cur) {
+        if (cur >= 0 && p.hist) finish();
+        cur = bh;
+        flushed_at = u;
+        b = (p.nhb == 1) ? bh : bh / p.nhb;
+        hb = bh - b * p.nhb;
+        hl = hb * HPB + hin;
+        T = clamp_len(p, b);
+        sel = p.hist && needs_selection(p.k, T);
+        if (tid == 0 && hb == 0 && ui == 0) {
+          const int raw = __ldg(p.seq_lens + b);
+          if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
+        }
 #pragma unroll
         for (int n = 0; n < NGR; ++n) {
-          float a = q[n][0] * f0;
-          a = fmaf(q[n][1], f1, a); a = fmaf(q[n][2], f2, a); a = fmaf(q[n][3], f3, a);
-          a = fmaf(q[n][4], f4, a); a = fmaf(q[n][5], f5, a); a = fmaf(q[n][6], f6, a);
-          a = fmaf(q[n][7], f7, a);
-          acc[uu * NGR + n] = a;
-        }
-      }
-      transposed_reduce<LPR, V>(acc);
+          const int g = (NGR == 1) ? hl : n;
+          float qs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int h = g * G; h < (g + 1) * G; ++h) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.qp + (static_cast<long long>(b) * p.Hq + h) * C + chunk * 8));
+            qs[0] += bf16_lo(w.x); qs[1] += bf16_hi(w.x);
+            qs[2] += bf16_lo(w.y); qs[3] += bf16_hi(w.y);
+            qs[4] += bf16_lo(w.z); qs[5] += bf16_hi(w.z);
+            qs[6] += bf16_lo(w.w); qs[7] += bf16_hi(w.w);
+          }
 #pragma unroll
-      for (int kk = 0; kk < PER; ++kk) {
-        const int v = (V >= LPR) ? chunk * PER + kk : (chunk * V) / LPR;
-        const bool writer = (V >= LPR) || ((chunk * V) % LPR == 0);
-        const int uu = v / NGR;
-        const int n = v % NGR;
-        const int t = tbase + (warp * U + uu) * TPI + tok_off;
-        const int g = (NGR == 1) ? hl : n;
-        if (writer && t < T) {
-          float sc = acc[kk];
-          const int pid = __ldg(p.page_table + b * p.maxp + (t >> 6));
-          if (pid < 0 || pid >= p.num_pages) {
-            sc = __int_as_float(0x7fc00000);
-            flag_error(p.err, 2u);
+          for (int i = 0; i < 4; ++i) q[n][i] = make_float2(qs[2 * i], qs[2 * i + 1]);
+        }
+      }
+      if (sel && (u - flushed_at) * TPU > 60000) {
+        named_barrier(1, kConsumerThreads);
+        flush_hist();
+        named_barrier(1, kConsumerThreads);
+        flushed_at = u;
+      }
+
+      const int tbase = ui * TPU;
+      if (ok && tbase < T) {
+        const unsigned char* src = ring + s * kUnitBytes + (warp * U) * 512 + lane * 16;
+        float acc[V];
+#pragma unroll
+        for (int uu = 0; uu < U; ++uu) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + uu * 512);
+          const float2 x0 = make_float2(bf16_lo(x.x), bf16_hi(x.x));
+          const float2 x1 = make_float2(bf16_lo(x.y), bf16_hi(x.y));
+          const float2 x2 = make_float2(bf16_lo(x.z), bf16_hi(x.z));
+          const float2 x3 = make_float2(bf16_lo(x.w), bf16_hi(x.w));
+#pragma unroll
+          for (int n = 0; n < NGR; ++n) {
+            float2 a = make_float2(q[n][0].x * x0.x, q[n][0].y * x0.y);
+            a = __ffma2_rn(q[n][1], x1, a);
+            a = __ffma2_rn(q[n][2], x2, a);
+            a = __ffma2_rn(q[n][3], x3, a);
+            acc[uu * NGR + n] = a.x + a.y;
           }
-          p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = sc;
-          if (sel) {
-            const unsigned bin = order_key(sc) >> 21;
-            const int r = (NGR == 1) ? hin : n;
-            atomicAdd(hist + r * 1024 + (bin >> 1), 1u << ((bin & 1u) << 4));
+        }
+        transposed_reduce<LPR, V>(acc);
+#pragma unroll
+        for (int kk = 0; kk < PER; ++kk) {
+          const int v = (V >= LPR) ? chunk * PER + kk : (chunk * V) / LPR;
+          const bool writer = (V >= LPR) || ((chunk * V) % LPR == 0);
+          const int uu = v / NGR;
+          const int n = v % NGR;
+          const int t = tbase + (warp * U + uu) * TPI + tok_off;
+          const int g = (NGR == 1) ? hl : n;
+          if (writer && t < T) {
+            const float sc = acc[kk];
+            p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = sc;
+            if (sel) {
+              const unsigned bin = order_key(sc) >> 21;
+              const int r = (NGR == 1) ? hin : n;
+              atomicAdd(hist + r * 1024 + (bin >> 1), 1u << ((bin & 1u) << 4));
+            }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (++s == p.nst) {
+        s = 0;
+        ++fill;
+      }
+      if (++ui == p.upb) {
+        ui = 0;
+        ++bh;
+      }
     }
-    __syncthreads();
-    if (u + p.nst < u1) {
-      issue(i_bh, i_ui, stage);
-      if (++i_ui == p.upb) { i_ui = 0; ++i_bh; }
-    }
-    cp_async_commit();
-    if (++c_ui == p.upb) { c_ui = 0; ++c_bh; }
-    if (++stage == p.nst) stage = 0;
+    if (cur >= 0 && p.hist) finish();
   }
-  if (cur >= 0 && p.hist) finish();
-  cp_async_wait<0>();
+  __syncthreads();
 }
 
 using KernelFn = void (*)(const ScoreParams);
@@ -387,9 +432,9 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (p.hist) p.tw = topk_ws_view(*a.topk);
   const int hist_bytes = p.hist ? rb * 4096 : 0;
   // Two CTAs per SM when the histogram is small, else one with a deeper ring.
-  int nst = (104 * 1024 - hist_bytes) / kUnitBytes;
-  if (nst < 4) nst = (220 * 1024 - hist_bytes) / kUnitBytes;
-  if (nst > 8) nst = 8;
+  int nst = (112 * 1024 - hist_bytes) / kUnitBytes;
+  if (nst < 3) nst = (220 * 1024 - hist_bytes) / kUnitBytes;
+  if (nst > kMaxStages) nst = kMaxStages;
   if (nst < 2) return cudaErrorNotSupported;
   p.nst = nst;
   const int smem = nst * kUnitBytes + hist_bytes;
