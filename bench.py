@@ -288,7 +288,7 @@ def run_ours(args):
         @staticmethod
         def zero_():
             flush_w.zero_()
-            torch.sum(flush_r, dtype=torch.int64, out=flush_sink)
+            torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
 
     flush = _Flush()
 
