@@ -154,7 +154,7 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-             shape->max_pages_per_req * shape->page_size, k, L, false};
+             shape->max_pages_per_req * shape->page_size, k, L, /*zeroed=*/false};
   return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -261,8 +261,8 @@ int ds_decode_num_splits(const ds_shape* shape, int k) {
 int ds_decode_kernel_launches(const ds_shape* shape, int k) {
   if (check_shape(shape) != DS_OK || k < 0 || shape->batch == 0) return 0;
   int n = 0;
-  if (shape->max_seq_len > 0) n += 1;  // scoring (with the level-1 histograms)
-  if (k > 0) n += 1;                   // filter + select
+  if (shape->max_seq_len > 0) n += 1;       // scoring
+  if (k > 0) n += (shape->max_seq_len > 0 ? 2 : 1);  // histogram, filter + select
   n += 1;                              // attention (with the merge when split)
   return n;
 }
@@ -296,14 +296,14 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (shape->max_seq_len > 0) {
     ScoreArgs sa{args->qp, args->label, args->page_table, args->seq_lens, L.scores, err, shape->batch,
                  shape->num_q_heads, shape->num_kv_heads, args->label_heads, pd, shape->max_pages_per_req,
-                 shape->num_pages, shape->max_seq_len, k > 0 ? &L.topk : nullptr, k};
+                 shape->num_pages, shape->max_seq_len};
     st = from_cuda(launch_index_score(sa, s));
     if (st != DS_OK) return st;
   }
   if (mark(1) != cudaSuccess) return DS_ERR_CUDA;
   if (k > 0) {
     TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-                shape->max_pages_per_req * shape->page_size, k, L.topk, true};
+                shape->max_pages_per_req * shape->page_size, k, L.topk, /*zeroed=*/true};
     st = from_cuda(launch_topk(ta, s));
     if (st != DS_OK) return st;
   }

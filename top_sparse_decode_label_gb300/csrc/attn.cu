@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   const int g = bg % p.Hkv;
   const int b = bg / p.Hkv;
   const int32_t* row = p.idx + static_cast<long long>(bg) * p.k;
+  grid_dependency_wait();
 
   int T = p.seq_lens[b];
   if (T < 0 || T > p.lim) T = T < 0 ? 0 : p.lim;  // flagged by the scoring / top-k stages
@@ -458,7 +459,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int smem = p.nst * stage + kSeg * (a.fp8 ? 4 + 8 : 4);
   cudaError_t e = allow_smem(fn, smem);
   if (e != cudaSuccess) return e;
-  fn<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+  e = launch_pdl(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -113,6 +113,12 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Programmatic dependent launch: blocks until the grids this one depends on
+// have completed and their memory is visible (a no-op without the launch
+// attribute). Every kernel calls it before touching memory an earlier
+// kernel of the stream may write or read.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Order-preserving map float -> uint32: a > b  <=>  key(a) > key(b).
 // -0.0 and +0.0 share one key; every NaN maps to 0, below every number.
 __device__ __forceinline__ uint32_t order_key(float x) {

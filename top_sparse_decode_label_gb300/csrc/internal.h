@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace ds {
 
 constexpr int kHeadDimSupported = 128;
@@ -19,9 +21,7 @@ int sm_count();
 // top-k starts; every completed top-k leaves them zero again.
 struct TopkLayout {
   void* ghist;       // u32 [R, 2048]
-  void* done1;       // u32 [R]
   void* done2;       // u32 [R]
-  void* row_state;   // uint2 [R]
   void* counts;      // u32 [R, nch]
   void* list;        // uint2 [R, Tmax]
   int nch;
@@ -38,8 +38,6 @@ struct ScoreArgs {
   float* scores;           // [B, Hkv, Tmax]
   unsigned* err;
   int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
-  const TopkLayout* topk;  // non-null: also build the level-1 top-k histograms for this k
-  int k;
 };
 // Returns a cudaError_t; cudaErrorNotSupported for shapes without a kernel.
 cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream);
@@ -52,7 +50,7 @@ struct TopkArgs {
   unsigned* err;
   int B, Hkv, Tmax, maxp_tokens, k;
   TopkLayout L;
-  bool histogram_done;     // level-1 thresholds already computed by the scoring kernel
+  bool zeroed;             // the layout's zero region is known to be zero (chained call)
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
@@ -80,5 +78,28 @@ bool sparse_attn_supported(int G);
 
 cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const float* lse_part,
                              void* out, float* lse, cudaStream_t stream);
+
+}  // namespace ds
+
+namespace ds {
+
+// Launches `kernel` on `stream` with programmatic dependent launch enabled, so
+// its CTAs may start while the previous kernel of the stream drains; the
+// kernel must call grid_dependency_wait() before using earlier results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace ds

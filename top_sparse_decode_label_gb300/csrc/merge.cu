@@ -20,6 +20,7 @@ constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(kMergeWarps * 32)
 lse_merge_kernel(int S, int rows, int D, const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -74,8 +75,9 @@ cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const 
                              float* lse, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
-  lse_merge_kernel<<<blocks, kMergeWarps * 32, 0, stream>>>(S, rows, D, o_part, lse_part,
-                                                             static_cast<__nv_bfloat16*>(out), lse);
+  cudaError_t e = launch_pdl(lse_merge_kernel, dim3(blocks), dim3(kMergeWarps * 32), 0, stream, S, rows, D, o_part,
+                             lse_part, static_cast<__nv_bfloat16*>(out), lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -1,5 +1,4 @@
-// Stage 1: proxy scoring of every cached token, optionally fused with the
-// first radix pass of the exact top-k.
+// Stage 1: proxy scoring of every cached token.
 //
 // "Support double sparsity" (sglang PR #1459): the query's heavy channels are
 // dotted with a label cache that holds, per token and KV head, the same heavy
@@ -25,15 +24,9 @@
 // query sits in registers, packed fp32 FMAs form the partial dot products, and
 // a transposed butterfly combines them across the row's lanes. Every mbarrier
 // wait is bounded: on timeout it sets DS_DEVERR_TIMEOUT and carries on.
-//
-// With a top-k to follow, the kernel also builds each row's histogram of the
-// top 11 bits of the order-preserving score key in shared memory (two 16-bit
-// counters per word), adds it into the row's global histogram when the CTA
-// leaves a (request, head block), and the CTA that finishes a (request, head
-// block) last turns the histograms into the level-1 threshold bins.
+
 #include "common.cuh"
 #include "internal.h"
-#include "topk_common.cuh"
 
 namespace ds {
 
@@ -53,23 +46,16 @@ struct ScoreParams {
   const int32_t* seq_lens;
   float* scores;
   unsigned* err;
-  int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb, k;
+  int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb;
   int units;        // B * nhb * upb (< 2^31, checked on the host)
   int upb;          // units per (request, head block)
   int nst;          // ring stages
-  int hist;         // build level-1 top-k histograms
-  TopkWs tw;
 };
 
 __device__ __forceinline__ int clamp_len(const ScoreParams& p, int b) {
   const int lim = min(p.Tmax, p.maxp * kPage);
   const int T = __ldg(p.seq_lens + b);
   return T < 0 ? 0 : (T > lim ? lim : T);
-}
-
-// Index of the CTA whose unit range holds unit i (ranges [c*U/n, (c+1)*U/n)).
-__device__ __forceinline__ int cta_of(long long i, long long units, long long n) {
-  return static_cast<int>(((i + 1) * n + units - 1) / units - 1);
 }
 
 // C: proxy width; NGR: groups fed by one label row (1 for a per-head label,
@@ -84,14 +70,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
   constexpr int U = kUnitBytes / 512 / kConsumerWarps;   // pieces per consumer warp per unit (4)
   constexpr int V = U * NGR;                             // partial sums per lane
   constexpr int PER = V >= LPR ? V / LPR : 1;            // finished sums per lane
-  constexpr int RB = (NGR == 1) ? HPB : NGR;             // histogram rows of a (request, head block)
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  unsigned* hist = reinterpret_cast<unsigned*>(smem + static_cast<size_t>(p.nst) * kUnitBytes);
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ int sh_last;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -106,9 +89,8 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
     }
     mbar_fence_init();
   }
-  if (p.hist && tid < kConsumerThreads)
-    for (int i = tid; i < RB * 1024; i += kConsumerThreads) hist[i] = 0;
   __syncthreads();
+  grid_dependency_wait();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
@@ -181,52 +163,8 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
     const int hin = rin % HPB;
     const int G = p.Hq / p.Hkv;
     int cur = -1;
-    int flushed_at = 0;  // unit of the last histogram flush (16-bit counters must not overflow)
-    int b = 0, hb = 0, T = 0, hl = 0;
-    bool sel = false;
+    int b = 0, T = 0, hl = 0;
     float2 q[NGR][4];
-
-    // Adds the CTA's shared histogram of (b, hb) into the global one and clears it.
-    auto flush_hist = [&]() {
-      for (int i = tid; i < RB * 1024; i += kConsumerThreads) {
-        const unsigned v = hist[i];
-        if (v) {
-          const int r = i >> 10;
-          const int w = i & 1023;
-          const int g = (NGR == 1) ? hb * HPB + r : r;
-          unsigned* gh = p.tw.ghist + (static_cast<size_t>(b) * p.Hkv + g) * kBins1 + 2 * w;
-          if (v & 0xffffu) atomicAdd(gh, v & 0xffffu);
-          if (v >> 16) atomicAdd(gh + 1, v >> 16);
-          hist[i] = 0;
-        }
-      }
-    };
-    // Leaving (b, hb): flush, count this CTA done for (b, hb), and let the
-    // last CTA compute the level-1 thresholds of its rows.
-    auto finish = [&]() {
-      named_barrier(1, kConsumerThreads);
-      if (sel) {
-        flush_hist();
-        __threadfence();
-        named_barrier(1, kConsumerThreads);
-        if (tid == 0) {
-          const long long st = static_cast<long long>(cur) * p.upb;
-          const int expected = cta_of(st + p.upb - 1, p.units, gridDim.x) - cta_of(st, p.units, gridDim.x) + 1;
-          const unsigned prev = atomicAdd(p.tw.done1 + cur, 1u);
-          sh_last = (prev + 1 == static_cast<unsigned>(expected));
-        }
-        named_barrier(1, kConsumerThreads);
-        if (sh_last) {
-          __threadfence();
-          for (int r = warp; r < RB; r += kConsumerWarps) {
-            const int g = (NGR == 1) ? hb * HPB + r : r;
-            level1_threshold_warp(p.tw, b * p.Hkv + g, p.k);
-          }
-          if (tid == 0) atomicExch(p.tw.done1 + cur, 0u);
-        }
-        named_barrier(1, kConsumerThreads);
-      }
-    };
 
     int bh = u0 / p.upb;
     int ui = u0 - bh * p.upb;
@@ -236,14 +174,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
       const bool ok = mbar_wait(&full_bar[s], fill & 1u, kWaitLimit);
       if (!ok && lane == 0) flag_error(p.err, 8u);
       if (bh != cur) {
-        if (cur >= 0 && p.hist) finish();
         cur = bh;
-        flushed_at = u;
         b = (p.nhb == 1) ? bh : bh / p.nhb;
-        hb = bh - b * p.nhb;
+        const int hb = bh - b * p.nhb;
         hl = hb * HPB + hin;
         T = clamp_len(p, b);
-        sel = p.hist && needs_selection(p.k, T);
         if (tid == 0 && hb == 0 && ui == 0) {
           const int raw = __ldg(p.seq_lens + b);
           if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
@@ -262,12 +197,6 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
 #pragma unroll
           for (int i = 0; i < 4; ++i) q[n][i] = make_float2(qs[2 * i], qs[2 * i + 1]);
         }
-      }
-      if (sel && (u - flushed_at) * TPU > 60000) {
-        named_barrier(1, kConsumerThreads);
-        flush_hist();
-        named_barrier(1, kConsumerThreads);
-        flushed_at = u;
       }
 
       const int tbase = ui * TPU;
@@ -299,15 +228,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
           const int n = v % NGR;
           const int t = tbase + (warp * U + uu) * TPI + tok_off;
           const int g = (NGR == 1) ? hl : n;
-          if (writer && t < T) {
-            const float sc = acc[kk];
-            p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = sc;
-            if (sel) {
-              const unsigned bin = order_key(sc) >> 21;
-              const int r = (NGR == 1) ? hin : n;
-              atomicAdd(hist + r * 1024 + (bin >> 1), 1u << ((bin & 1u) << 4));
-            }
-          }
+          if (writer && t < T) p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = acc[kk];
         }
       }
       __syncwarp();
@@ -321,7 +242,6 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
         ++bh;
       }
     }
-    if (cur >= 0 && p.hist) finish();
   }
   __syncthreads();
 }
@@ -404,10 +324,8 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (!fn) return cudaErrorNotSupported;
   if (a.B == 0 || a.Tmax == 0) return cudaSuccess;
   const int rpi = 256 / a.C;
-  const int hpb = rpi / tpi;
   const int nhb = (a.HL > rpi) ? a.HL / rpi : 1;
   const int tpu = kUnitBytes / (512 / tpi);
-  const int rb = (a.HL == 1) ? a.Hkv : hpb;
   ScoreParams p{};
   p.qp = static_cast<const uint16_t*>(a.qp);
   p.label = static_cast<const uint8_t*>(a.label);
@@ -422,22 +340,14 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.num_pages = a.num_pages;
   p.Tmax = a.Tmax;
   p.nhb = nhb;
-  p.k = a.k;
   const long long upb = (static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu;
   const long long units = static_cast<long long>(a.B) * nhb * upb;
   if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;
   p.upb = static_cast<int>(upb);
   p.units = static_cast<int>(units);
-  p.hist = a.topk != nullptr;
-  if (p.hist) p.tw = topk_ws_view(*a.topk);
-  const int hist_bytes = p.hist ? rb * 4096 : 0;
-  // Two CTAs per SM when the histogram is small, else one with a deeper ring.
-  int nst = (112 * 1024 - hist_bytes) / kUnitBytes;
-  if (nst < 3) nst = (220 * 1024 - hist_bytes) / kUnitBytes;
-  if (nst > kMaxStages) nst = kMaxStages;
-  if (nst < 2) return cudaErrorNotSupported;
-  p.nst = nst;
-  const int smem = nst * kUnitBytes + hist_bytes;
+  // Two CTAs per SM, each with a ring of 7 x 16 KB stages.
+  p.nst = 7;
+  const int smem = p.nst * kUnitBytes;
   cudaError_t e = allow_smem(fn, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -446,7 +356,8 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (per_sm < 1) per_sm = 1;
   long long blocks = static_cast<long long>(sm_count()) * per_sm;
   if (p.units < blocks) blocks = p.units;
-  fn<<<static_cast<unsigned>(blocks), kScoreThreads, smem, stream>>>(p);
+  e = launch_pdl(fn, dim3(static_cast<unsigned>(blocks)), dim3(kScoreThreads), smem, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -8,23 +8,24 @@
 //
 // Scores map to order-preserving 32-bit keys (-0.0 == +0.0, NaN lowest).
 // With K_eff = min(k, T), rows with 0 < K_eff < T go through three radix
-// digits (11 + 11 + 10 bits):
-//   level 1 (histogram): a 2048-bin histogram of key >> 21 per row, built by
-//     the scoring kernel in the chained call or by topk_hist_kernel here; the
-//     CTA that completes a row's histogram finds the bin b1 holding the
-//     K_eff-th largest key and the count above it.
-//   filter: one CTA per 4096-score chunk keeps every (key, token) with
-//     key >> 21 >= b1, in token order, in the chunk's slot of the row's list
-//     (one block-wide prefix sum, no atomics per element).
-//   select: the CTA that completes a row's filter refines the threshold key
-//     over the kept entries whose top bits equal b1 (two more digits in shared
-//     memory), giving the exact K_eff-th key `thr` and the number r of tokens
-//     with key == thr to keep. Walking the list in token order with two
-//     block-wide prefix sums (rank among ties, then output position) writes
-//     the kept tokens -- key > thr, or key == thr and tie rank < r --
-//     ascending. The list is typically K_eff plus a few thousand entries.
+// digits (11 + 11 + 10 bits) in two launches:
+//   histogram: one CTA per 4096-score chunk of a row builds a 2048-bin
+//     histogram of key >> 21 in shared memory and adds its nonzero bins into
+//     the row's global histogram (a few dozen atomics per CTA).
+//   filter + select (persistent CTAs over (row, chunk) work items): a CTA
+//     finds, from the row's histogram, the bin b1 holding the K_eff-th largest
+//     key, then keeps every (key, token) of its chunk with key >> 21 >= b1, in
+//     token order, in the chunk's slot of the row's list (one block-wide
+//     prefix sum). The CTA that completes the row's last chunk selects: it
+//     gathers the row's list (typically K_eff plus a few thousand entries)
+//     into shared memory, refines the threshold key over the entries whose
+//     top bits equal b1 (two more digits), giving the exact K_eff-th key `thr`
+//     and the number r of ties to keep, and writes the kept tokens -- key >
+//     thr, or key == thr and tie rank < r -- ascending with two block-wide
+//     prefix sums. It then clears the row's histogram and counter.
 // Completion is detected with per-row counters (the last CTA continues);
-// nothing waits on another CTA.
+// nothing waits on another CTA. Both kernels use programmatic dependent
+// launch and wait for the previous kernel before touching its outputs.
 #include "common.cuh"
 #include "internal.h"
 #include "topk_common.cuh"
@@ -57,36 +58,25 @@ __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
   return T;
 }
 
-// Level 1 on its own (the scores were produced elsewhere).
+// Level-1 histograms of the rows that need a selection.
 __global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const TopkParams p) {
   __shared__ unsigned h[kBins1];
-  __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_res[2];
-  __shared__ int sh_last;
+  grid_dependency_wait();
   const int row = blockIdx.y;
   const int b = row / p.Hkv;
   const int T = row_len(p, b, blockIdx.x == 0 && threadIdx.x == 0 && row % p.Hkv == 0);
   if (!needs_selection(p.k, T)) return;
-  const int nch = (T + kChunk - 1) / kChunk;
-  if (static_cast<int>(blockIdx.x) >= nch) return;
+  const int c0 = blockIdx.x * kChunk;
+  if (c0 >= T) return;
   for (int i = threadIdx.x; i < kBins1; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-  const int c0 = blockIdx.x * kChunk;
   const int c1 = min(T, c0 + kChunk);
   for (int t = c0 + threadIdx.x; t < c1; t += blockDim.x) atomicAdd(&h[order_key(s[t]) >> 21], 1u);
   __syncthreads();
   unsigned* g = p.w.ghist + static_cast<size_t>(row) * kBins1;
   for (int i = threadIdx.x; i < kBins1; i += blockDim.x)
     if (h[i]) atomicAdd(&g[i], h[i]);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) sh_last = (atomicAdd(p.w.done1 + row, 1u) + 1 == static_cast<unsigned>(nch));
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-  level1_threshold(p.w, row, p.k, sh_scan, sh_res);
-  if (threadIdx.x == 0) atomicExch(p.w.done1 + row, 0u);
 }
 
 // Walks entries [e, ...) of a row's list (chunk slots concatenated).
@@ -264,6 +254,9 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
     }
   }
   for (int i = keff + tid; i < p.k; i += blockDim.x) out[i] = -1;
+  // Every chunk of the row has read the histogram: clear it for the next call.
+  unsigned* gh = p.w.ghist + static_cast<size_t>(row) * kBins1;
+  for (int i = tid; i < kBins1; i += blockDim.x) __stcg(gh + i, 0u);
   __syncthreads();
 }
 
@@ -281,6 +274,9 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
   const int nitems = p.R * p.w.nch;
   const int w0 = static_cast<int>(static_cast<long long>(blockIdx.x) * nitems / gridDim.x);
   const int w1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * nitems / gridDim.x);
+  grid_dependency_wait();
+  int cur_row = -1;
+  unsigned b1 = 0, above1 = 0;
   for (int item = w0; item < w1; ++item) {
     const int row = item / p.w.nch;
     const int c = item - row * p.w.nch;
@@ -296,8 +292,14 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
     }
     const int nch = (T + kChunk - 1) / kChunk;
     if (c >= nch) continue;
-    const uint2 st = __ldcg(p.w.row_state + row);
-    const unsigned b1 = st.x;
+    if (row != cur_row) {
+      // Level 1: the bin holding the K_eff-th largest key, from the row's histogram.
+      find_threshold_bin<true>(p.w.ghist + static_cast<size_t>(row) * kBins1, kBins1, static_cast<unsigned>(keff),
+                               sh_scan, sh_res);
+      b1 = sh_res[0];
+      above1 = sh_res[1];
+      cur_row = row;
+    }
 
     // ---- filter: keep key >> 21 >= b1 of this chunk, in token order
     const int c0 = c * kChunk;
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
     __syncthreads();
     if (!sh_last) continue;
     __threadfence();
-    select_row(p, row, T, nch, b1, st.y, sm_list, cap, sh_pref, sh_hist, sh_scan, sh_res);
+    select_row(p, row, T, nch, b1, above1, sm_list, cap, sh_pref, sh_hist, sh_scan, sh_res);
     if (tid == 0) atomicExch(p.w.done2 + row, 0u);
   }
 }
@@ -365,14 +367,10 @@ TopkLayout topk_layout(void* base, int R, int Tmax) {
   size_t off = 0;
   L.ghist = p + off;
   off += static_cast<size_t>(R) * kBins1 * 4;
-  L.done1 = p + off;
-  off += static_cast<size_t>(R) * 4;
   L.done2 = p + off;
   off += static_cast<size_t>(R) * 4;
   L.zero_bytes = off;
   off = align256(off);
-  L.row_state = p + off;
-  off = align256(off + static_cast<size_t>(R) * 8);
   L.counts = p + off;
   off = align256(off + static_cast<size_t>(R) * L.nch * 4);
   L.list = p + off;
@@ -397,14 +395,18 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.k = a.k;
   p.w = topk_ws_view(a.L);
   p.R = R;
-  if (!a.histogram_done) {
-    cudaError_t e = cudaMemsetAsync(a.L.ghist, 0, a.L.zero_bytes, stream);
+  cudaError_t e;
+  if (!a.zeroed) {
+    e = cudaMemsetAsync(a.L.ghist, 0, a.L.zero_bytes, stream);
     if (e != cudaSuccess) return e;
-    if (a.Tmax > 0) topk_hist_kernel<<<dim3(a.L.nch, R), kChunkThreads, 0, stream>>>(p);
+  }
+  if (a.Tmax > 0) {
+    e = launch_pdl(topk_hist_kernel, dim3(a.L.nch, R), dim3(kChunkThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
   }
   // Shared memory: the selected row's kept list (up to kListCap entries) and the chunk prefix.
   const int smem = kListCap * 8 + (a.L.nch + 1) * 4;
-  cudaError_t e = allow_select_smem(smem);
+  e = allow_select_smem(smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_filter_select_kernel, kChunkThreads, smem);
@@ -413,7 +415,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   long long blocks = static_cast<long long>(sm_count()) * per_sm;
   const long long items = static_cast<long long>(R) * a.L.nch;
   if (items < blocks) blocks = items;
-  topk_filter_select_kernel<<<static_cast<unsigned>(blocks), kChunkThreads, smem, stream>>>(p, kListCap);
+  e = launch_pdl(topk_filter_select_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kChunkThreads), smem, stream,
+                 p, static_cast<int>(kListCap));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -1,12 +1,10 @@
-// Exact top-k machinery shared by the fused scoring kernel and the top-k
-// kernels: the scratch layout, the radix threshold search and the level-1
-// epilogue that turns a row's 2048-bin histogram of the top 11 key bits into
-// (threshold bin b1, number of keys above it).
+// Exact top-k machinery shared by the top-k kernels: the scratch layout and
+// the radix threshold search.
 //
-// Completion counters: a multi-CTA phase counts finished CTAs per row (or per
-// request and head block) with one atomicAdd each; the CTA that sees the last
-// count does the per-row follow-up and resets the counter to zero. Nothing
-// waits on another CTA, so no launch order or co-residency is assumed.
+// Completion counters: the filter phase counts finished chunks per row with
+// one atomicAdd each; the CTA that sees the last count selects the row and
+// resets the counter and the row's histogram to zero. Nothing waits on
+// another CTA, so no launch order or co-residency is assumed.
 #pragma once
 
 #include "common.cuh"
@@ -15,15 +13,13 @@
 namespace ds {
 
 constexpr int kBins1 = 2048;   // level-1 digit: key bits 21..31
-constexpr int kChunk = 4096;   // scores per filter CTA
+constexpr int kChunk = 4096;   // scores per histogram / filter work item
 constexpr int kChunkThreads = 256;
 
 // Device view of the top-k scratch (see TopkLayout in internal.h).
 struct TopkWs {
   unsigned* ghist;     // [R, 2048] level-1 histograms (zero between calls)
-  unsigned* done1;     // [R] completion counters of the histogram phase (zero between calls)
   unsigned* done2;     // [R] completion counters of the filter phase (zero between calls)
-  uint2* row_state;    // [R] (b1, count above b1)
   unsigned* counts;    // [R, nch] kept-list length of each chunk
   uint2* list;         // [R, Tmax] (key, token) with key >> 21 >= b1, per chunk in token order
   int nch;             // chunks per row = ceil(Tmax / kChunk)
@@ -32,9 +28,7 @@ struct TopkWs {
 inline TopkWs topk_ws_view(const TopkLayout& L) {
   TopkWs w;
   w.ghist = static_cast<unsigned*>(L.ghist);
-  w.done1 = static_cast<unsigned*>(L.done1);
   w.done2 = static_cast<unsigned*>(L.done2);
-  w.row_state = static_cast<uint2*>(L.row_state);
   w.counts = static_cast<unsigned*>(L.counts);
   w.list = static_cast<uint2*>(L.list);
   w.nch = L.nch;
@@ -72,56 +66,6 @@ __device__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned nee
     }
   }
   __syncthreads();
-}
-
-// Level-1 epilogue of one row, run by every thread of the CTA that finished
-// the row's histogram last: records (b1, above) and clears the histogram.
-__device__ __forceinline__ void level1_threshold(const TopkWs& w, int row, int keff, unsigned* sh_scan,
-                                                 unsigned* sh_res) {
-  unsigned* h = w.ghist + static_cast<size_t>(row) * kBins1;
-  find_threshold_bin<true>(h, kBins1, static_cast<unsigned>(keff), sh_scan, sh_res);
-  if (threadIdx.x == 0) w.row_state[row] = make_uint2(sh_res[0], sh_res[1]);
-  for (int i = threadIdx.x; i < kBins1; i += blockDim.x) __stcg(h + i, 0u);
-  __syncthreads();
-}
-
-// Level-1 epilogue of one row run by a single warp: lane l holds bins
-// [2048 - 64(l+1), 2048 - 64 l) in registers (one round of loads), a warp
-// prefix over lanes from the top finds the lane holding the K_eff-th key,
-// which scans its bins. Records (b1, above) and clears the histogram.
-__device__ __forceinline__ void level1_threshold_warp(const TopkWs& w, int row, int keff) {
-  const int lane = threadIdx.x & 31;
-  unsigned* h = w.ghist + static_cast<size_t>(row) * kBins1 + (kBins1 - 64 * (lane + 1));
-  uint4 v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __ldcg(reinterpret_cast<const uint4*>(h) + i);
-  unsigned c = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) c += v[i].x + v[i].y + v[i].z + v[i].w;
-  const unsigned inc = warp_incl_scan(c);
-  const unsigned before = inc - c;
-  const unsigned need = static_cast<unsigned>(keff);
-  if (before < need && inc >= need) {
-    unsigned run = before;
-    unsigned bin = 0, above = 0;
-    bool found = false;
-#pragma unroll
-    for (int i = 15; i >= 0; --i) {
-      const unsigned e[4] = {v[i].w, v[i].z, v[i].y, v[i].x};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (!found && run + e[q] >= need) {
-          found = true;
-          bin = kBins1 - 64 * (lane + 1) + 4 * i + (3 - q);
-          above = run;
-        }
-        run += e[q];
-      }
-    }
-    w.row_state[row] = make_uint2(bin, above);
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) __stcg(reinterpret_cast<uint4*>(h) + i, make_uint4(0u, 0u, 0u, 0u));
 }
 
 // Rows that need a selection at all: 0 < K_eff < T.
