@@ -72,11 +72,17 @@ __global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const TopkPara
   __syncthreads();
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
   const int c1 = min(T, c0 + kChunk);
-  for (int t = c0 + threadIdx.x; t < c1; t += blockDim.x) atomicAdd(&h[order_key(s[t]) >> 21], 1u);
+  for (int base = c0; base < c1; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    const bool in = t < c1;
+    warp_hist_add(h, in ? order_key(s[t]) >> 21 : 0u, in);
+  }
   __syncthreads();
   unsigned* g = p.w.ghist + static_cast<size_t>(row) * kBins1;
-  for (int i = threadIdx.x; i < kBins1; i += blockDim.x)
-    if (h[i]) atomicAdd(&g[i], h[i]);
+  for (int i = threadIdx.x; i < kBins1; i += blockDim.x) {
+    const unsigned v = h[hslot(i)];
+    if (v) atomicAdd(&g[i], v);
+  }
 }
 
 // Walks entries [e, ...) of a row's list (chunk slots concatenated).
@@ -133,25 +139,21 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   const int M = static_cast<int>(sh_pref[nch]);
   const bool in_smem = M <= cap;
   if (in_smem) {
-    // Gather the list into shared memory, 8 independent loads in flight per thread.
-    for (int e0 = tid; e0 < M; e0 += 8 * kChunkThreads) {
-      uint2 v[8];
+    // Gather the list into shared memory: warp w copies chunks w, w+8, ...,
+    // eight independent loads in flight per lane.
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
+      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
+      const uint2* src = base + static_cast<size_t>(ci) * kChunk;
+      uint2* dst = sm_list + sh_pref[ci];
+      for (int j0 = lane; j0 < n; j0 += 8 * 32) {
+        uint2 v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = e0 + i * kChunkThreads;
-        if (e < M) {
-          int lo = 0, hi = nch - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (sh_pref[mid] <= static_cast<unsigned>(e)) lo = mid; else hi = mid - 1;
-          }
-          v[i] = __ldcg(base + static_cast<size_t>(lo) * kChunk + (e - static_cast<int>(sh_pref[lo])));
-        }
-      }
+        for (int i = 0; i < 8; ++i)
+          if (j0 + i * 32 < n) v[i] = __ldcg(src + j0 + i * 32);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = e0 + i * kChunkThreads;
-        if (e < M) sm_list[e] = v[i];
+        for (int i = 0; i < 8; ++i)
+          if (j0 + i * 32 < n) dst[j0 + i * 32] = v[i];
       }
     }
     __syncthreads();
@@ -163,17 +165,19 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
   if (in_smem) {
-    for (int e = tid; e < M; e += kChunkThreads) {
-      const uint32_t key = sm_list[e].x;
-      if ((key >> 21) == b1) atomicAdd(&sh_hist[(key >> 10) & 2047u], 1u);
+    for (int e0 = 0; e0 < M; e0 += kChunkThreads) {
+      const int e = e0 + tid;
+      const uint32_t key = e < M ? sm_list[e].x : 0u;
+      warp_hist_add(sh_hist, (key >> 10) & 2047u, e < M && (key >> 21) == b1);
     }
   } else {
     const int lane = tid & 31, warp = tid >> 5;
     for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
       const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-      for (int j = lane; j < n; j += 32) {
-        const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
-        if ((key >> 21) == b1) atomicAdd(&sh_hist[(key >> 10) & 2047u], 1u);
+      for (int j0 = 0; j0 < n; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < n ? __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x : 0u;
+        warp_hist_add(sh_hist, (key >> 10) & 2047u, j < n && (key >> 21) == b1);
       }
     }
   }
@@ -186,17 +190,19 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   for (int i = tid; i < 1024; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
   if (in_smem) {
-    for (int e = tid; e < M; e += kChunkThreads) {
-      const uint32_t key = sm_list[e].x;
-      if ((key >> 10) == hi22) atomicAdd(&sh_hist[key & 1023u], 1u);
+    for (int e0 = 0; e0 < M; e0 += kChunkThreads) {
+      const int e = e0 + tid;
+      const uint32_t key = e < M ? sm_list[e].x : 0u;
+      warp_hist_add(sh_hist, key & 1023u, e < M && (key >> 10) == hi22);
     }
   } else {
     const int lane = tid & 31, warp = tid >> 5;
     for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
       const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-      for (int j = lane; j < n; j += 32) {
-        const uint32_t key = __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x;
-        if ((key >> 10) == hi22) atomicAdd(&sh_hist[key & 1023u], 1u);
+      for (int j0 = 0; j0 < n; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < n ? __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x : 0u;
+        warp_hist_add(sh_hist, key & 1023u, j < n && (key >> 10) == hi22);
       }
     }
   }
@@ -204,7 +210,7 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   find_threshold_bin<false>(sh_hist, 1024, need2, sh_scan, sh_res);
   const unsigned d3 = sh_res[0];
   const unsigned r_eq = need2 - sh_res[1];
-  const unsigned eq_total = sh_hist[d3];
+  const unsigned eq_total = sh_hist[hslot(static_cast<int>(d3))];
   const uint32_t thr = (hi22 << 10) | d3;
   __syncthreads();
 

@@ -35,11 +35,28 @@ inline TopkWs topk_ws_view(const TopkLayout& L) {
   return w;
 }
 
+// Shared-memory slot of histogram bin b: the low 5 bits (the bank) are XOR-
+// folded with the higher bits, a bijection per 32-bin block, so digit
+// patterns that vary only in high bits (e.g. integer-valued scores, whose low
+// mantissa bits are all zero) still spread over all banks.
+__device__ __forceinline__ int hslot(int b) { return (b & ~31) | ((b ^ (b >> 5) ^ (b >> 10)) & 31); }
+
+// Adds 1 to bin `bin` of a shared histogram for every lane with `pred`; all
+// 32 lanes must call it. Lanes with equal bins are combined first, so a warp
+// issues one atomic per distinct bin.
+__device__ __forceinline__ void warp_hist_add(unsigned* h, unsigned bin, bool pred) {
+  const unsigned active = __ballot_sync(kFull, pred);
+  if (!pred) return;
+  const unsigned same = __match_any_sync(active, bin);
+  if ((threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(h + hslot(static_cast<int>(bin)), __popc(same));
+}
+
 // Scanning a histogram from its highest bin down, finds the bin where the
 // running count first reaches `need` (1 <= need <= total). Writes out[0] =
 // bin, out[1] = count in the bins above it (0, 0 if no bin qualifies).
 // nbins must be a multiple of blockDim.x. GLOBAL: the histogram is in global
-// memory written by other CTAs' atomics, read through L2.
+// memory written by other CTAs' atomics, read through L2 (bin b at index b);
+// otherwise it is a shared histogram filled by warp_hist_add (bin b at hslot(b)).
 template <bool GLOBAL>
 __device__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned need, unsigned* sh_scan,
                                    unsigned* out) {
@@ -50,13 +67,13 @@ __device__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned nee
     out[1] = 0;
   }
   unsigned c = 0;
-  for (int i = 1; i <= per; ++i) c += GLOBAL ? __ldcg(hist + hi - i) : hist[hi - i];
+  for (int i = 1; i <= per; ++i) c += GLOBAL ? __ldcg(hist + hi - i) : hist[hslot(hi - i)];
   unsigned total;
   const unsigned before = block_excl_scan(c, sh_scan, &total);
   if (before < need && before + c >= need) {
     unsigned run = before;
     for (int i = 1; i <= per; ++i) {
-      const unsigned h = GLOBAL ? __ldcg(hist + hi - i) : hist[hi - i];
+      const unsigned h = GLOBAL ? __ldcg(hist + hi - i) : hist[hslot(hi - i)];
       if (run + h >= need) {
         out[0] = hi - i;
         out[1] = run;
