@@ -41,14 +41,12 @@ inline TopkWs topk_ws_view(const TopkLayout& L) {
 // mantissa bits are all zero) still spread over all banks.
 __device__ __forceinline__ int hslot(int b) { return (b & ~31) | ((b ^ (b >> 5) ^ (b >> 10)) & 31); }
 
-// Adds 1 to bin `bin` of a shared histogram for every lane with `pred`; all
-// 32 lanes must call it. Lanes with equal bins are combined first, so a warp
-// issues one atomic per distinct bin.
+// Adds 1 to bin `bin` of a shared histogram (slot hslot(bin)) when `pred`.
+// Shared atomics to one address are combined by the hardware; bank conflicts
+// between different addresses are what serialises them, and hslot spreads
+// those.
 __device__ __forceinline__ void warp_hist_add(unsigned* h, unsigned bin, bool pred) {
-  const unsigned active = __ballot_sync(kFull, pred);
-  if (!pred) return;
-  const unsigned same = __match_any_sync(active, bin);
-  if ((threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(h + hslot(static_cast<int>(bin)), __popc(same));
+  if (pred) atomicAdd(h + hslot(static_cast<int>(bin)), 1u);
 }
 
 // Scanning a histogram from its highest bin down, finds the bin where the
