@@ -21,6 +21,7 @@ int sm_count();
 // top-k starts; every completed top-k leaves them zero again.
 struct TopkLayout {
   void* ghist;       // u32 [R, 2048]
+  void* ghist2;      // u32 [R, 2048]
   void* done2;       // u32 [R]
   void* counts;      // u32 [R, nch]
   void* list;        // uint2 [R, Tmax]

@@ -49,6 +49,26 @@ struct TopkParams {
   TopkWs w;
 };
 
+// Keys of scores [t0, t0 + kElems) of a row (only t < c1 is meaningful); four
+// 16-byte loads in flight when aligned, else scalar loads.
+__device__ __forceinline__ void load_keys(const float* s, int t0, int c1, uint32_t (&keys)[kElems]) {
+  if (((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1)) {
+    float4 v[kElems / 4];
+#pragma unroll
+    for (int i = 0; i < kElems / 4; ++i) v[i] = *reinterpret_cast<const float4*>(s + t0 + 4 * i);
+#pragma unroll
+    for (int i = 0; i < kElems / 4; ++i) {
+      keys[4 * i] = order_key(v[i].x);
+      keys[4 * i + 1] = order_key(v[i].y);
+      keys[4 * i + 2] = order_key(v[i].z);
+      keys[4 * i + 3] = order_key(v[i].w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
+  }
+}
+
 __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
   int T = p.seq_lens[b];
   if (T < 0 || T > p.lim) {
@@ -72,11 +92,11 @@ __global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const TopkPara
   __syncthreads();
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
   const int c1 = min(T, c0 + kChunk);
-  for (int base = c0; base < c1; base += blockDim.x) {
-    const int t = base + threadIdx.x;
-    const bool in = t < c1;
-    warp_hist_add(h, in ? order_key(s[t]) >> 21 : 0u, in);
-  }
+  const int t0 = c0 + threadIdx.x * kElems;
+  uint32_t keys[kElems];
+  load_keys(s, t0, c1, keys);
+#pragma unroll
+  for (int i = 0; i < kElems; ++i) warp_hist_add(h, keys[i] >> 21, t0 + i < c1);
   __syncthreads();
   unsigned* g = p.w.ghist + static_cast<size_t>(row) * kBins1;
   for (int i = threadIdx.x; i < kBins1; i += blockDim.x) {
@@ -113,7 +133,7 @@ struct ListWalker {
 // Select phase of one row, run by the CTA that completed the row's filter.
 // `lst` holds the kept entries of the row in token order when M <= cap
 // (copied to shared memory); otherwise they are walked in global memory.
-__device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigned b1, unsigned above1,
+__device__ __forceinline__ void select_row(const TopkParams& p, int row, int T, int nch, unsigned b1, unsigned above1,
                            uint2* sm_list, int cap, unsigned* sh_pref, unsigned* sh_hist, unsigned* sh_scan,
                            unsigned* sh_res) {
   const int tid = threadIdx.x;
@@ -161,28 +181,10 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   auto key_at = [&](int e, ListWalker& wk) -> uint2 { return in_smem ? sm_list[e] : wk.next(); };
   const unsigned need = static_cast<unsigned>(keff) - above1;
 
-  // Level 2: bits 10..20 of the entries in bin b1.
-  for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
-  __syncthreads();
-  if (in_smem) {
-    for (int e0 = 0; e0 < M; e0 += kChunkThreads) {
-      const int e = e0 + tid;
-      const uint32_t key = e < M ? sm_list[e].x : 0u;
-      warp_hist_add(sh_hist, (key >> 10) & 2047u, e < M && (key >> 21) == b1);
-    }
-  } else {
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
-      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-      for (int j0 = 0; j0 < n; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t key = j < n ? __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x : 0u;
-        warp_hist_add(sh_hist, (key >> 10) & 2047u, j < n && (key >> 21) == b1);
-      }
-    }
-  }
-  __syncthreads();
-  find_threshold_bin<false>(sh_hist, kBins1, need, sh_scan, sh_res);
+  // Level 2: bits 10..20 of the bin-b1 keys, histogram built by the filter CTAs.
+  unsigned* gh2 = p.w.ghist2 + static_cast<size_t>(row) * kBins1;
+  find_threshold_bin<true>(gh2, kBins1, need, sh_scan, sh_res);
+  for (int i = tid; i < kBins1; i += blockDim.x) __stcg(gh2 + i, 0u);
   const unsigned d2 = sh_res[0];
   const unsigned need2 = need - sh_res[1];
   // Level 3: bits 0..9 of the entries that match so far.
@@ -190,10 +192,16 @@ __device__ void select_row(const TopkParams& p, int row, int T, int nch, unsigne
   for (int i = tid; i < 1024; i += blockDim.x) sh_hist[i] = 0;
   __syncthreads();
   if (in_smem) {
-    for (int e0 = 0; e0 < M; e0 += kChunkThreads) {
-      const int e = e0 + tid;
-      const uint32_t key = e < M ? sm_list[e].x : 0u;
-      warp_hist_add(sh_hist, key & 1023u, e < M && (key >> 10) == hi22);
+    for (int e0 = 0; e0 < M; e0 += 4 * kChunkThreads) {
+      uint32_t key[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = e0 + i * kChunkThreads + tid;
+        key[i] = e < M ? sm_list[e].x : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        warp_hist_add(sh_hist, key[i] & 1023u, e0 + i * kChunkThreads + tid < M && (key[i] >> 10) == hi22);
     }
   } else {
     const int lane = tid & 31, warp = tid >> 5;
@@ -314,26 +322,16 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
     const int t0 = c0 + tid * kElems;
     uint32_t keys[kElems];
     unsigned flags = 0, cnt = 0;
-    const bool vec = ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1);
-    if (vec) {
-#pragma unroll
-      for (int i = 0; i < kElems; i += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(s + t0 + i);
-        keys[i] = order_key(v.x);
-        keys[i + 1] = order_key(v.y);
-        keys[i + 2] = order_key(v.z);
-        keys[i + 3] = order_key(v.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
-    }
+    load_keys(s, t0, c1, keys);
+    for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < kElems; ++i) {
       if (t0 + i < c1 && (keys[i] >> 21) >= b1) {
         flags |= 1u << i;
         ++cnt;
       }
+      warp_hist_add(sh_hist, (keys[i] >> 10) & 2047u, t0 + i < c1 && (keys[i] >> 21) == b1);
     }
     unsigned total;
     unsigned pos = block_excl_scan(cnt, sh_scan, &total);
@@ -342,6 +340,13 @@ __global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const
     for (int i = 0; i < kElems; ++i)
       if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
     if (tid == 0) p.w.counts[static_cast<size_t>(row) * p.w.nch + c] = total;
+    {
+      unsigned* gh2 = p.w.ghist2 + static_cast<size_t>(row) * kBins1;
+      for (int i = tid; i < kBins1; i += blockDim.x) {
+        const unsigned v = sh_hist[hslot(i)];
+        if (v) atomicAdd(gh2 + i, v);
+      }
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) sh_last = (atomicAdd(p.w.done2 + row, 1u) + 1 == static_cast<unsigned>(nch));
@@ -372,6 +377,8 @@ TopkLayout topk_layout(void* base, int R, int Tmax) {
   L.nch = (T1 + kChunk - 1) / kChunk;
   size_t off = 0;
   L.ghist = p + off;
+  off += static_cast<size_t>(R) * kBins1 * 4;
+  L.ghist2 = p + off;
   off += static_cast<size_t>(R) * kBins1 * 4;
   L.done2 = p + off;
   off += static_cast<size_t>(R) * 4;

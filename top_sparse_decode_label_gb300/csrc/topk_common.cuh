@@ -19,6 +19,7 @@ constexpr int kChunkThreads = 256;
 // Device view of the top-k scratch (see TopkLayout in internal.h).
 struct TopkWs {
   unsigned* ghist;     // [R, 2048] level-1 histograms (zero between calls)
+  unsigned* ghist2;    // [R, 2048] level-2 histograms of the bin-b1 keys (zero between calls)
   unsigned* done2;     // [R] completion counters of the filter phase (zero between calls)
   unsigned* counts;    // [R, nch] kept-list length of each chunk
   uint2* list;         // [R, Tmax] (key, token) with key >> 21 >= b1, per chunk in token order
@@ -28,6 +29,7 @@ struct TopkWs {
 inline TopkWs topk_ws_view(const TopkLayout& L) {
   TopkWs w;
   w.ghist = static_cast<unsigned*>(L.ghist);
+  w.ghist2 = static_cast<unsigned*>(L.ghist2);
   w.done2 = static_cast<unsigned*>(L.done2);
   w.counts = static_cast<unsigned*>(L.counts);
   w.list = static_cast<uint2*>(L.list);
@@ -56,7 +58,7 @@ __device__ __forceinline__ void warp_hist_add(unsigned* h, unsigned bin, bool pr
 // memory written by other CTAs' atomics, read through L2 (bin b at index b);
 // otherwise it is a shared histogram filled by warp_hist_add (bin b at hslot(b)).
 template <bool GLOBAL>
-__device__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned need, unsigned* sh_scan,
+__device__ __forceinline__ void find_threshold_bin(const unsigned* hist, int nbins, unsigned need, unsigned* sh_scan,
                                    unsigned* out) {
   const int per = nbins / blockDim.x;
   const int hi = nbins - per * threadIdx.x;
