@@ -221,8 +221,8 @@ typedef struct {
  * ds_sparse_decode_attn (internal split-KV chosen for occupancy) ->
  * ds_lse_merge, on one stream, with scores and partials in `workspace`
  * (at least ds_decode_workspace_bytes bytes, 256-byte aligned). The
- * workspace holds completion counters and histograms that must be zero
- * before its first use (e.g. cudaMemsetAsync(workspace, 0, bytes) once);
+ * workspace holds completion counters of the split-KV merge that must be
+ * zero before its first use (e.g. cudaMemsetAsync(workspace, 0, bytes) once);
  * every call leaves them zero again, so it is reused without clearing. Calls
  * sharing one workspace must not overlap on the GPU. No host synchronisation
  * and no allocation, so the call can be captured in a CUDA graph and replayed

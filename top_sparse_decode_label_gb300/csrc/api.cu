@@ -154,7 +154,7 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-             shape->max_pages_per_req * shape->page_size, k, L, /*zeroed=*/false};
+             shape->max_pages_per_req * shape->page_size, k, L};
   return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -213,9 +213,8 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
 
 namespace {
 
-// Workspace of the chained call. The top-k counters and histograms and the
-// merge counters must be zero before the first call; every call leaves them
-// zero again.
+// Workspace of the chained call. The merge counters must be zero before the
+// first call; every call leaves them zero again.
 struct DecodeLayout {
   float* scores;
   TopkLayout topk;
@@ -262,7 +261,7 @@ int ds_decode_kernel_launches(const ds_shape* shape, int k) {
   if (check_shape(shape) != DS_OK || k < 0 || shape->batch == 0) return 0;
   int n = 0;
   if (shape->max_seq_len > 0) n += 1;       // scoring
-  if (k > 0) n += (shape->max_seq_len > 0 ? 2 : 1);  // histogram, filter + select
+  if (k > 0) n += 1;                   // top-k (one cluster per row)
   n += 1;                              // attention (with the merge when split)
   return n;
 }
@@ -303,7 +302,7 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (mark(1) != cudaSuccess) return DS_ERR_CUDA;
   if (k > 0) {
     TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-                shape->max_pages_per_req * shape->page_size, k, L.topk, /*zeroed=*/true};
+                shape->max_pages_per_req * shape->page_size, k, L.topk};
     st = from_cuda(launch_topk(ta, s));
     if (st != DS_OK) return st;
   }

@@ -163,6 +163,94 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* sh, un
   return r;
 }
 
+// Exclusive block prefix sum of 64-bit values (two 32-bit counters packed
+// as lo | hi << 32 scan together as long as each column's total fits in 32
+// bits). `sh` needs 33 entries.
+__device__ __forceinline__ unsigned long long block_excl_scan64(unsigned long long v, unsigned long long* sh,
+                                                                unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long s = (lane < nw) ? sh[lane] : 0ull;
+    unsigned long long si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long n = __shfl_up_sync(kFull, si, o);
+      if (lane >= o) si += n;
+    }
+    if (lane < nw) sh[lane] = si - s;
+    if (lane == 31) sh[32] = si;
+  }
+  __syncthreads();
+  const unsigned long long r = sh[warp] + inc - v;
+  if (total) *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+// ---- thread-block clusters: rank, barriers and distributed shared memory
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_nctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Split cluster barrier: every thread of every CTA of the cluster arrives
+// once, then waits. Shared-memory writes (local or remote) made before the
+// arrive are visible to every thread of the cluster after its wait. Both are
+// also a barrier of the CTA's own threads. All threads must execute them
+// convergently.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+// Address, in the cluster's shared window, of the variable at local shared
+// address `addr` in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, unsigned rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_red_add(uint32_t addr, unsigned v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned cluster_ld(uint32_t addr) {
+  unsigned v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 cluster_ld2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 cluster_ld4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Transposed butterfly reduction over groups of L consecutive lanes (L a power
 // of two <= 32). Each lane holds N partial sums v[0..N) of the same N
 // quantities; afterwards lane j (= lane % L) holds the full sums of

@@ -16,17 +16,11 @@ constexpr long long kDecodeTargetCtas = 456;  // attention CTAs the chained call
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
-// Scratch of the exact top-k for R rows of up to Tmax scores. The first
-// `zero_bytes` bytes (histograms and completion counters) must be zero when a
-// top-k starts; every completed top-k leaves them zero again.
+// Scratch of the exact top-k for R rows of up to Tmax scores: a (key, token)
+// list per row, used only by rows whose candidates overflow shared memory.
+// Needs no initialisation.
 struct TopkLayout {
-  void* ghist;       // u32 [R, 2048]
-  void* ghist2;      // u32 [R, 2048]
-  void* done2;       // u32 [R]
-  void* counts;      // u32 [R, nch]
   void* list;        // uint2 [R, Tmax]
-  int nch;
-  size_t zero_bytes;
   size_t bytes;
 };
 TopkLayout topk_layout(void* base, int R, int Tmax);
@@ -51,7 +45,6 @@ struct TopkArgs {
   unsigned* err;
   int B, Hkv, Tmax, maxp_tokens, k;
   TopkLayout L;
-  bool zeroed;             // the layout's zero region is known to be zero (chained call)
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 

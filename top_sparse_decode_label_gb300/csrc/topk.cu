@@ -7,25 +7,22 @@
 // heavy-token count of tokens per head.
 //
 // Scores map to order-preserving 32-bit keys (-0.0 == +0.0, NaN lowest).
-// With K_eff = min(k, T), rows with 0 < K_eff < T go through three radix
-// digits (11 + 11 + 10 bits) in two launches:
-//   histogram: one CTA per 4096-score chunk of a row builds a 2048-bin
-//     histogram of key >> 21 in shared memory and adds its nonzero bins into
-//     the row's global histogram (a few dozen atomics per CTA).
-//   filter + select (persistent CTAs over (row, chunk) work items): a CTA
-//     finds, from the row's histogram, the bin b1 holding the K_eff-th largest
-//     key, then keeps every (key, token) of its chunk with key >> 21 >= b1, in
-//     token order, in the chunk's slot of the row's list (one block-wide
-//     prefix sum). The CTA that completes the row's last chunk selects: it
-//     gathers the row's list (typically K_eff plus a few thousand entries)
-//     into shared memory, refines the threshold key over the entries whose
-//     top bits equal b1 (two more digits), giving the exact K_eff-th key `thr`
-//     and the number r of ties to keep, and writes the kept tokens -- key >
-//     thr, or key == thr and tie rank < r -- ascending with two block-wide
-//     prefix sums. It then clears the row's histogram and counter.
-// Completion is detected with per-row counters (the last CTA continues);
-// nothing waits on another CTA. Both kernels use programmatic dependent
-// launch and wait for the previous kernel before touching its outputs.
+// With K_eff = min(k, T), a row with 0 < K_eff < T is selected by one
+// thread-block cluster of CS CTAs (CS a power of two, up to 16), CTA q owning
+// the contiguous token slice q of the row. The threshold key -- the K_eff-th
+// largest -- is found digit by digit (11 + 11 + 10 bits): each CTA builds the
+// histogram of its slice's digits in shared memory and adds its nonzero bins
+// into the bins' owner CTA (bins are split evenly over the cluster) with
+// distributed-shared-memory atomics; after a cluster barrier every CTA reads
+// the row's totals from the owners and finds the digit where the running
+// count from the top reaches the remaining need. After digit 1 each CTA
+// compacts the (key, token) pairs of its slice whose first digit is at least
+// the threshold's into a token-ordered list (shared memory, or the workspace
+// when it overflows); digits 2 and 3 and the output work on that list. With
+// `thr` the threshold key and r the number of keys equal to it that must be
+// kept, a CTA keeps its keys > thr and its equal keys whose rank in the row's
+// token order is below r; the counts of the CTAs before it give its output
+// offset. No global atomics, no completion counters, nothing to clear.
 #include "common.cuh"
 #include "internal.h"
 #include "topk_common.cuh"
@@ -34,9 +31,11 @@ namespace ds {
 
 namespace {
 
-constexpr int kElems = kChunk / kChunkThreads;   // 16 scores per thread
-constexpr int kMaxChunks = 4096;                 // rows of up to 16M tokens
-constexpr int kListCap = 8192;                   // kept entries selected from shared memory (64 KB)
+constexpr int kThreads = 512;
+constexpr int kPer = 16;                      // scores per thread per pass
+constexpr int kBatch = kThreads * kPer;       // scores per CTA pass
+constexpr int kListCap = 4096;                // kept (key, token) pairs in shared memory
+constexpr int kMaxCluster = 16;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -45,19 +44,33 @@ struct TopkParams {
   const int32_t* seq_lens;
   int32_t* idx;
   unsigned* err;
-  int Hkv, Tmax, lim, k, R;
-  TopkWs w;
+  uint2* list;     // [R, Tmax] overflow lists
+  int Hkv, Tmax, lim, k;
 };
 
-// Keys of scores [t0, t0 + kElems) of a row (only t < c1 is meaningful); four
+struct __align__(16) Smem {
+  unsigned h1[kBins1];   // this CTA's digit histograms, bin b at hslot(b)
+  unsigned h2[kBins1];
+  unsigned h3[kBins3];
+  unsigned t1[kBins1];   // row totals of the bins this CTA owns, bin b at b
+  unsigned t2[kBins1];
+  unsigned t3[kBins3];
+  unsigned long long scan[33];
+  unsigned cnt[2];       // this CTA's keys above the threshold, equal to it
+  unsigned res[4];
+  uint2 list[kListCap];
+};
+constexpr int kZeroWords = 4 * kBins1 + 2 * kBins3;   // h1 .. t3
+
+// Keys of scores [t0, t0 + kPer) of a row (only t < c1 is meaningful); four
 // 16-byte loads in flight when aligned, else scalar loads.
-__device__ __forceinline__ void load_keys(const float* s, int t0, int c1, uint32_t (&keys)[kElems]) {
-  if (((reinterpret_cast<uintptr_t>(s) & 15u) == 0) && (t0 + kElems <= c1)) {
-    float4 v[kElems / 4];
+__device__ __forceinline__ void load_keys(const float* s, int t0, int c1, uint32_t (&keys)[kPer]) {
+  if (((reinterpret_cast<uintptr_t>(s + t0) & 15u) == 0) && (t0 + kPer <= c1)) {
+    float4 v[kPer / 4];
 #pragma unroll
-    for (int i = 0; i < kElems / 4; ++i) v[i] = *reinterpret_cast<const float4*>(s + t0 + 4 * i);
+    for (int i = 0; i < kPer / 4; ++i) v[i] = __ldcg(reinterpret_cast<const float4*>(s + t0 + 4 * i));
 #pragma unroll
-    for (int i = 0; i < kElems / 4; ++i) {
+    for (int i = 0; i < kPer / 4; ++i) {
       keys[4 * i] = order_key(v[i].x);
       keys[4 * i + 1] = order_key(v[i].y);
       keys[4 * i + 2] = order_key(v[i].z);
@@ -65,8 +78,68 @@ __device__ __forceinline__ void load_keys(const float* s, int t0, int c1, uint32
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < kElems; ++i) keys[i] = (t0 + i < c1) ? order_key(s[t0 + i]) : 0u;
+    for (int i = 0; i < kPer; ++i) keys[i] = (t0 + i < c1) ? order_key(__ldcg(s + t0 + i)) : 0u;
   }
+}
+
+// Adds this CTA's histogram h (nbins bins, slots hslot) into the owners'
+// totals t: bin b belongs to cluster rank b / (nbins / cs).
+template <int NB>
+__device__ __forceinline__ void push_bins(const unsigned* h, unsigned* t, unsigned cs) {
+  constexpr int per = NB / kThreads;
+  const int own_shift = __ffs(NB / static_cast<int>(cs)) - 1;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    const int b = threadIdx.x * per + j;
+    const unsigned v = h[hslot(b)];
+    if (v) cluster_red_add(cluster_map(smem_u32(t + b), static_cast<unsigned>(b >> own_shift)), v);
+  }
+}
+
+// Reads the row totals of bins hi-1 .. hi-PER (hi = NB - PER * tid) from
+// their owner: c[j] = total of bin hi-1-j.
+template <int NB, int PER>
+__device__ __forceinline__ void read_totals(const unsigned* t, unsigned cs, unsigned (&c)[PER]) {
+  const int hi = NB - PER * static_cast<int>(threadIdx.x);
+  const int own_shift = __ffs(NB / static_cast<int>(cs)) - 1;
+  const uint32_t a = cluster_map(smem_u32(t + hi - PER), static_cast<unsigned>((hi - PER) >> own_shift));
+  if constexpr (PER == 4) {
+    const uint4 v = cluster_ld4(a);
+    c[0] = v.w;
+    c[1] = v.z;
+    c[2] = v.y;
+    c[3] = v.x;
+  } else {
+    static_assert(PER == 2, "two or four bins per thread");
+    const uint2 v = cluster_ld2(a);
+    c[0] = v.y;
+    c[1] = v.x;
+  }
+}
+
+// Bins hi-1 .. hi-PER per thread (thread 0 the highest): finds the bin where
+// the count from the top first reaches `need` (1 <= need <= total) and writes
+// res[0] = bin, res[1] = count in the bins above it.
+template <int NB, int PER>
+__device__ __forceinline__ void find_crossing(const unsigned (&c)[PER], unsigned need, Smem& S) {
+  const int hi = NB - PER * static_cast<int>(threadIdx.x);
+  unsigned sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) sum += c[j];
+  unsigned tot;
+  unsigned run = block_excl_scan(sum, reinterpret_cast<unsigned*>(S.scan), &tot);
+  if (run < need && run + sum >= need) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      if (run + c[j] >= need) {
+        S.res[0] = static_cast<unsigned>(hi - 1 - j);
+        S.res[1] = run;
+        break;
+      }
+      run += c[j];
+    }
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
@@ -78,358 +151,290 @@ __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
   return T;
 }
 
-// Level-1 histograms of the rows that need a selection.
-__global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const TopkParams p) {
-  __shared__ unsigned h[kBins1];
-  grid_dependency_wait();
-  const int row = blockIdx.y;
-  const int b = row / p.Hkv;
-  const int T = row_len(p, b, blockIdx.x == 0 && threadIdx.x == 0 && row % p.Hkv == 0);
-  if (!needs_selection(p.k, T)) return;
-  const int c0 = blockIdx.x * kChunk;
-  if (c0 >= T) return;
-  for (int i = threadIdx.x; i < kBins1; i += blockDim.x) h[i] = 0;
-  __syncthreads();
-  const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-  const int c1 = min(T, c0 + kChunk);
-  const int t0 = c0 + threadIdx.x * kElems;
-  uint32_t keys[kElems];
-  load_keys(s, t0, c1, keys);
-#pragma unroll
-  for (int i = 0; i < kElems; ++i) warp_hist_add(h, keys[i] >> 21, t0 + i < c1);
-  __syncthreads();
-  unsigned* g = p.w.ghist + static_cast<size_t>(row) * kBins1;
-  for (int i = threadIdx.x; i < kBins1; i += blockDim.x) {
-    const unsigned v = h[hslot(i)];
-    if (v) atomicAdd(&g[i], v);
+__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  Smem& S = *reinterpret_cast<Smem*>(dsm);
+  const int tid = threadIdx.x;
+  const unsigned cs = cluster_nctarank();
+  const unsigned q = cluster_ctarank();
+  const int row = static_cast<int>(blockIdx.x / cs);
+  {
+    uint4* z = reinterpret_cast<uint4*>(S.h1);
+    for (int i = tid; i < kZeroWords / 4; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
+  __syncthreads();
+  grid_dependency_wait();
+  const int b = row / p.Hkv;
+  const int T = row_len(p, b, q == 0 && tid == 0 && row % p.Hkv == 0);
+  int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
+  const int keff = min(p.k, T);
+  if (!needs_selection(p.k, T)) {
+    // The whole cluster takes this branch (same row): no shared memory is
+    // exchanged, so CTAs leave independently.
+    for (int i = static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads)
+      out[i] = (i < keff) ? i : -1;
+    return;
+  }
+  cluster_arrive();   // this CTA's totals are zero: owners may receive adds
+
+  // ---- digit 1 (key bits 21..31) over the slice
+  const int SL = ((T + static_cast<int>(cs) - 1) / static_cast<int>(cs) + 15) & ~15;
+  const int s0 = min(T, static_cast<int>(q) * SL);
+  const int s1 = min(T, s0 + SL);
+  const int nb = (s1 - s0 + kBatch - 1) / kBatch;
+  const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
+  uint32_t keys[kPer];
+  for (int bt = 0; bt < nb; ++bt) {
+    const int t0 = s0 + bt * kBatch + tid * kPer;
+    load_keys(s, t0, s1, keys);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, keys[i] >> 21, t0 + i < s1);
+  }
+  __syncthreads();
+  cluster_wait();
+  push_bins<kBins1>(S.h1, S.t1, cs);
+  cluster_sync();
+  unsigned b1, above1, M;
+  {
+    // Row totals and this CTA's own counts scanned together (lo | own << 32).
+    unsigned c[4], l[4];
+    read_totals<kBins1, 4>(S.t1, cs, c);
+    const int hi = kBins1 - 4 * tid;
+    unsigned sc = 0, sl = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      l[j] = S.h1[hslot(hi - 1 - j)];
+      sc += c[j];
+      sl += l[j];
+    }
+    const unsigned long long v = static_cast<unsigned long long>(sc) | (static_cast<unsigned long long>(sl) << 32);
+    const unsigned long long before = block_excl_scan64(v, S.scan, nullptr);
+    unsigned run = static_cast<unsigned>(before), lrun = static_cast<unsigned>(before >> 32);
+    const unsigned need = static_cast<unsigned>(keff);
+    if (run < need && run + sc >= need) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (run + c[j] >= need) {
+          S.res[0] = static_cast<unsigned>(hi - 1 - j);
+          S.res[1] = run;
+          S.res[2] = lrun + l[j];   // this CTA's keys with digit 1 >= the threshold's
+          break;
+        }
+        run += c[j];
+        lrun += l[j];
+      }
+    }
+    __syncthreads();
+    b1 = S.res[0];
+    above1 = S.res[1];
+    M = S.res[2];
+  }
+  const unsigned need1 = static_cast<unsigned>(keff) - above1;
+
+  // ---- compaction of the candidates (digit 1 >= b1), token order; digit 2
+  // (bits 10..20) histogram of the keys whose digit 1 equals b1
+  uint2* lst = (M <= static_cast<unsigned>(kListCap)) ? S.list : p.list + static_cast<size_t>(row) * p.Tmax + s0;
+  {
+    unsigned base = 0;
+    for (int bt = 0; bt < nb; ++bt) {
+      const int t0 = s0 + bt * kBatch + tid * kPer;
+      if (nb > 1) load_keys(s, t0, s1, keys);
+      unsigned flags = 0, cnt = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const bool valid = t0 + i < s1;
+        const unsigned d1 = keys[i] >> 21;
+        if (valid && d1 >= b1) {
+          flags |= 1u << i;
+          ++cnt;
+        }
+        warp_hist_add(S.h2, (keys[i] >> 10) & 2047u, valid && d1 == b1);
+      }
+      unsigned tot;
+      unsigned pos = base + block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &tot);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
+      base += tot;
+    }
+  }
+  __syncthreads();
+  push_bins<kBins1>(S.h2, S.t2, cs);
+  cluster_sync();
+  unsigned d2, need2;
+  {
+    unsigned c[4];
+    read_totals<kBins1, 4>(S.t2, cs, c);
+    find_crossing<kBins1, 4>(c, need1, S);
+    d2 = S.res[0];
+    need2 = need1 - S.res[1];
+  }
+
+  // ---- digit 3 (bits 0..9) of the candidates whose top 22 bits match
+  const uint32_t hi22 = (b1 << 11) | d2;
+  for (int e = tid; e < static_cast<int>(M); e += kThreads) {
+    const uint32_t key = lst[e].x;
+    warp_hist_add(S.h3, key & 1023u, (key >> 10) == hi22);
+  }
+  __syncthreads();
+  push_bins<kBins3>(S.h3, S.t3, cs);
+  cluster_sync();
+  uint32_t thr;
+  unsigned r_eq;
+  {
+    unsigned c[2];
+    read_totals<kBins3, 2>(S.t3, cs, c);
+    find_crossing<kBins3, 2>(c, need2, S);
+    thr = (hi22 << 10) | S.res[0];
+    r_eq = need2 - S.res[1];   // keys equal to thr that are kept, lowest tokens first
+  }
+
+  // ---- output: per-thread contiguous list segments in token order
+  const int seg = (static_cast<int>(M) + kThreads - 1) / kThreads;
+  const int e0 = min(static_cast<int>(M), tid * seg);
+  const int e1 = min(static_cast<int>(M), e0 + seg);
+  unsigned gt = 0, eq = 0;
+  for (int e = e0; e < e1; ++e) {
+    const uint32_t key = lst[e].x;
+    gt += key > thr;
+    eq += key == thr;
+  }
+  unsigned long long tot;
+  const unsigned long long ex =
+      block_excl_scan64(static_cast<unsigned long long>(gt) | (static_cast<unsigned long long>(eq) << 32), S.scan,
+                        &tot);
+  if (tid == 0) {
+    S.cnt[0] = static_cast<unsigned>(tot);
+    S.cnt[1] = static_cast<unsigned>(tot >> 32);
+  }
+  cluster_sync();
+  if (tid < 32) {
+    unsigned g = 0, e = 0;
+    if (static_cast<unsigned>(tid) < q) {
+      const uint2 v = cluster_ld2(cluster_map(smem_u32(S.cnt), static_cast<unsigned>(tid)));
+      g = v.x;
+      e = v.y;
+    }
+    g = __reduce_add_sync(kFull, g);
+    e = __reduce_add_sync(kFull, e);
+    if (tid == 0) {
+      S.res[2] = g;
+      S.res[3] = e;
+    }
+  }
+  __syncthreads();
+  cluster_arrive();   // no more reads of other CTAs' shared memory
+  const unsigned gt_before = S.res[2], eq_before = S.res[3];
+  const unsigned admit = r_eq > eq_before ? r_eq - eq_before : 0u;   // ties this CTA may keep
+  unsigned eqr = static_cast<unsigned>(ex >> 32);
+  unsigned pos = gt_before + min(r_eq, eq_before) + static_cast<unsigned>(ex) + min(admit, eqr);
+  for (int e = e0; e < e1; ++e) {
+    const uint2 v = lst[e];
+    bool keep = v.x > thr;
+    if (v.x == thr) {
+      keep = eqr < admit;
+      ++eqr;
+    }
+    if (keep) {
+      if (pos < static_cast<unsigned>(p.k)) out[pos] = static_cast<int32_t>(v.y);
+      ++pos;
+    }
+  }
+  for (int i = keff + static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads) out[i] = -1;
+  cluster_wait();   // keep this CTA's shared memory until every CTA is done with it
 }
 
-// Walks entries [e, ...) of a row's list (chunk slots concatenated).
-struct ListWalker {
-  const uint2* base;   // row's list
-  const unsigned* pref;  // shared: chunk prefix, nch + 1 entries
-  int ci, off;
-  __device__ void seek(int e, int nch) {
-    int lo = 0, hi = nch - 1;  // largest ci with pref[ci] <= e
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pref[mid] <= static_cast<unsigned>(e)) lo = mid; else hi = mid - 1;
-    }
-    ci = lo;
-    off = e - static_cast<int>(pref[ci]);
-  }
-  __device__ uint2 next() {
-    while (static_cast<unsigned>(off) >= pref[ci + 1] - pref[ci]) {
-      ++ci;
-      off = 0;
-    }
-    const uint2 v = __ldcg(base + static_cast<size_t>(ci) * kChunk + off);
-    ++off;
-    return v;
-  }
+struct LaunchCache {
+  bool init = false;
+  int max_cs = 8;
 };
 
-// Select phase of one row, run by the CTA that completed the row's filter.
-// `lst` holds the kept entries of the row in token order when M <= cap
-// (copied to shared memory); otherwise they are walked in global memory.
-__device__ __forceinline__ void select_row(const TopkParams& p, int row, int T, int nch, unsigned b1, unsigned above1,
-                           uint2* sm_list, int cap, unsigned* sh_pref, unsigned* sh_hist, unsigned* sh_scan,
-                           unsigned* sh_res) {
-  const int tid = threadIdx.x;
-  const int keff = min(p.k, T);
-  int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
-  const unsigned* counts = p.w.counts + static_cast<size_t>(row) * p.w.nch;
-  const uint2* base = p.w.list + static_cast<size_t>(row) * p.Tmax;
-
-  // Chunk prefix of the list lengths.
-  const int cpt = (nch + kChunkThreads - 1) / kChunkThreads;
-  {
-    unsigned mine = 0;
-    for (int i = tid * cpt; i < min(nch, (tid + 1) * cpt); ++i) mine += __ldcg(counts + i);
-    unsigned tot;
-    unsigned run = block_excl_scan(mine, sh_scan, &tot);
-    for (int i = tid * cpt; i < min(nch, (tid + 1) * cpt); ++i) {
-      sh_pref[i] = run;
-      run += __ldcg(counts + i);
-    }
-    if (tid == 0) sh_pref[nch] = tot;
-  }
-  __syncthreads();
-  const int M = static_cast<int>(sh_pref[nch]);
-  const bool in_smem = M <= cap;
-  if (in_smem) {
-    // Gather the list into shared memory: warp w copies chunks w, w+8, ...,
-    // eight independent loads in flight per lane.
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
-      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-      const uint2* src = base + static_cast<size_t>(ci) * kChunk;
-      uint2* dst = sm_list + sh_pref[ci];
-      for (int j0 = lane; j0 < n; j0 += 8 * 32) {
-        uint2 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (j0 + i * 32 < n) v[i] = __ldcg(src + j0 + i * 32);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (j0 + i * 32 < n) dst[j0 + i * 32] = v[i];
-      }
-    }
-    __syncthreads();
-  }
-  auto key_at = [&](int e, ListWalker& wk) -> uint2 { return in_smem ? sm_list[e] : wk.next(); };
-  const unsigned need = static_cast<unsigned>(keff) - above1;
-
-  // Level 2: bits 10..20 of the bin-b1 keys, histogram built by the filter CTAs.
-  unsigned* gh2 = p.w.ghist2 + static_cast<size_t>(row) * kBins1;
-  find_threshold_bin<true>(gh2, kBins1, need, sh_scan, sh_res);
-  for (int i = tid; i < kBins1; i += blockDim.x) __stcg(gh2 + i, 0u);
-  const unsigned d2 = sh_res[0];
-  const unsigned need2 = need - sh_res[1];
-  // Level 3: bits 0..9 of the entries that match so far.
-  const uint32_t hi22 = (b1 << 11) | d2;
-  for (int i = tid; i < 1024; i += blockDim.x) sh_hist[i] = 0;
-  __syncthreads();
-  if (in_smem) {
-    for (int e0 = 0; e0 < M; e0 += 4 * kChunkThreads) {
-      uint32_t key[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = e0 + i * kChunkThreads + tid;
-        key[i] = e < M ? sm_list[e].x : 0u;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        warp_hist_add(sh_hist, key[i] & 1023u, e0 + i * kChunkThreads + tid < M && (key[i] >> 10) == hi22);
-    }
-  } else {
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int ci = warp; ci < nch; ci += kChunkThreads / 32) {
-      const int n = static_cast<int>(sh_pref[ci + 1] - sh_pref[ci]);
-      for (int j0 = 0; j0 < n; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t key = j < n ? __ldcg(base + static_cast<size_t>(ci) * kChunk + j).x : 0u;
-        warp_hist_add(sh_hist, key & 1023u, j < n && (key >> 10) == hi22);
-      }
-    }
-  }
-  __syncthreads();
-  find_threshold_bin<false>(sh_hist, 1024, need2, sh_scan, sh_res);
-  const unsigned d3 = sh_res[0];
-  const unsigned r_eq = need2 - sh_res[1];
-  const unsigned eq_total = sh_hist[hslot(static_cast<int>(d3))];
-  const uint32_t thr = (hi22 << 10) | d3;
-  __syncthreads();
-
-  // Ordered output: thread segments in token order, prefix sums across threads.
-  const int seg = (M + kChunkThreads - 1) / kChunkThreads;
-  const int e0 = min(M, tid * seg);
-  const int e1 = min(M, e0 + seg);
-  ListWalker wk{base, sh_pref, 0, 0};
-  unsigned eq_base = 0;
-  if (eq_total > r_eq) {
-    unsigned eqc = 0;
-    if (!in_smem && e0 < e1) wk.seek(e0, nch);
-    for (int e = e0; e < e1; ++e) eqc += (key_at(e, wk).x == thr);
-    unsigned tot;
-    eq_base = block_excl_scan(eqc, sh_scan, &tot);
-  }
-  unsigned selc = 0;
-  {
-    if (!in_smem && e0 < e1) wk.seek(e0, nch);
-    unsigned eq = eq_base;
-    for (int e = e0; e < e1; ++e) {
-      const uint32_t key = key_at(e, wk).x;
-      if (key > thr) {
-        ++selc;
-      } else if (key == thr) {
-        selc += (eq < r_eq);
-        ++eq;
-      }
-    }
-  }
-  unsigned tot_sel;
-  unsigned opos = block_excl_scan(selc, sh_scan, &tot_sel);
-  {
-    if (!in_smem && e0 < e1) wk.seek(e0, nch);
-    unsigned eq = eq_base;
-    for (int e = e0; e < e1; ++e) {
-      const uint2 v = key_at(e, wk);
-      bool keep = v.x > thr;
-      if (v.x == thr) {
-        keep = eq < r_eq;
-        ++eq;
-      }
-      if (keep) {
-        if (opos < static_cast<unsigned>(p.k)) out[opos] = static_cast<int32_t>(v.y);
-        ++opos;
-      }
-    }
-  }
-  for (int i = keff + tid; i < p.k; i += blockDim.x) out[i] = -1;
-  // Every chunk of the row has read the histogram: clear it for the next call.
-  unsigned* gh = p.w.ghist + static_cast<size_t>(row) * kBins1;
-  for (int i = tid; i < kBins1; i += blockDim.x) __stcg(gh + i, 0u);
-  __syncthreads();
-}
-
-// Persistent filter: CTAs walk (row, chunk) work items; the CTA that completes
-// a row's last chunk selects the row.
-__global__ void __launch_bounds__(kChunkThreads) topk_filter_select_kernel(const TopkParams p, int cap) {
-  extern __shared__ __align__(16) unsigned char dsmem[];
-  uint2* sm_list = reinterpret_cast<uint2*>(dsmem);                         // [cap]
-  unsigned* sh_pref = reinterpret_cast<unsigned*>(dsmem + static_cast<size_t>(cap) * 8);  // [nch + 1]
-  __shared__ unsigned sh_scan[33];
-  __shared__ unsigned sh_res[2];
-  __shared__ int sh_last;
-  __shared__ unsigned sh_hist[kBins1];
-  const int tid = threadIdx.x;
-  const int nitems = p.R * p.w.nch;
-  const int w0 = static_cast<int>(static_cast<long long>(blockIdx.x) * nitems / gridDim.x);
-  const int w1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * nitems / gridDim.x);
-  grid_dependency_wait();
-  int cur_row = -1;
-  unsigned b1 = 0, above1 = 0;
-  for (int item = w0; item < w1; ++item) {
-    const int row = item / p.w.nch;
-    const int c = item - row * p.w.nch;
-    const int b = row / p.Hkv;
-    const int T = row_len(p, b, false);
-    const int keff = min(p.k, T);
-    if (!needs_selection(p.k, T)) {
-      if (c == 0) {
-        int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
-        for (int i = tid; i < p.k; i += blockDim.x) out[i] = (i < keff) ? i : -1;
-      }
-      continue;
-    }
-    const int nch = (T + kChunk - 1) / kChunk;
-    if (c >= nch) continue;
-    if (row != cur_row) {
-      // Level 1: the bin holding the K_eff-th largest key, from the row's histogram.
-      find_threshold_bin<true>(p.w.ghist + static_cast<size_t>(row) * kBins1, kBins1, static_cast<unsigned>(keff),
-                               sh_scan, sh_res);
-      b1 = sh_res[0];
-      above1 = sh_res[1];
-      cur_row = row;
-    }
-
-    // ---- filter: keep key >> 21 >= b1 of this chunk, in token order
-    const int c0 = c * kChunk;
-    const int c1 = min(T, c0 + kChunk);
-    const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-    const int t0 = c0 + tid * kElems;
-    uint32_t keys[kElems];
-    unsigned flags = 0, cnt = 0;
-    load_keys(s, t0, c1, keys);
-    for (int i = tid; i < kBins1; i += blockDim.x) sh_hist[i] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kElems; ++i) {
-      if (t0 + i < c1 && (keys[i] >> 21) >= b1) {
-        flags |= 1u << i;
-        ++cnt;
-      }
-      warp_hist_add(sh_hist, (keys[i] >> 10) & 2047u, t0 + i < c1 && (keys[i] >> 21) == b1);
-    }
-    unsigned total;
-    unsigned pos = block_excl_scan(cnt, sh_scan, &total);
-    uint2* lst = p.w.list + static_cast<size_t>(row) * p.Tmax + c0;
-#pragma unroll
-    for (int i = 0; i < kElems; ++i)
-      if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
-    if (tid == 0) p.w.counts[static_cast<size_t>(row) * p.w.nch + c] = total;
-    {
-      unsigned* gh2 = p.w.ghist2 + static_cast<size_t>(row) * kBins1;
-      for (int i = tid; i < kBins1; i += blockDim.x) {
-        const unsigned v = sh_hist[hslot(i)];
-        if (v) atomicAdd(gh2 + i, v);
-      }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) sh_last = (atomicAdd(p.w.done2 + row, 1u) + 1 == static_cast<unsigned>(nch));
-    __syncthreads();
-    if (!sh_last) continue;
-    __threadfence();
-    select_row(p, row, T, nch, b1, above1, sm_list, cap, sh_pref, sh_hist, sh_scan, sh_res);
-    if (tid == 0) atomicExch(p.w.done2 + row, 0u);
-  }
-}
-
-cudaError_t allow_select_smem(int bytes) {
-  static int done[64] = {};
+// Largest cluster the device can schedule with this kernel's footprint.
+cudaError_t prepare(int smem, int* max_cs) {
+  static LaunchCache cache[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(topk_filter_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
-  return e;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  LaunchCache* c = (dev >= 0 && dev < 64) ? &cache[dev] : nullptr;
+  if (c && c->init) {
+    *max_cs = c->max_cs;
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int best = 8;
+  if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxCluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMaxCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel, &cfg) == cudaSuccess && n > 0) best = kMaxCluster;
+    cudaGetLastError();
+  } else {
+    cudaGetLastError();
+  }
+  if (c) {
+    c->max_cs = best;
+    c->init = true;
+  }
+  *max_cs = best;
+  return cudaSuccess;
 }
 
 }  // namespace
 
 TopkLayout topk_layout(void* base, int R, int Tmax) {
   TopkLayout L;
-  char* p = static_cast<char*>(base);
   const int T1 = Tmax > 0 ? Tmax : 1;
-  L.nch = (T1 + kChunk - 1) / kChunk;
-  size_t off = 0;
-  L.ghist = p + off;
-  off += static_cast<size_t>(R) * kBins1 * 4;
-  L.ghist2 = p + off;
-  off += static_cast<size_t>(R) * kBins1 * 4;
-  L.done2 = p + off;
-  off += static_cast<size_t>(R) * 4;
-  L.zero_bytes = off;
-  off = align256(off);
-  L.counts = p + off;
-  off = align256(off + static_cast<size_t>(R) * L.nch * 4);
-  L.list = p + off;
-  off = align256(off + static_cast<size_t>(R) * T1 * 8);
-  L.bytes = off;
+  L.list = base;
+  L.bytes = align256(static_cast<size_t>(R) * T1 * 8);
   return L;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   const int R = a.B * a.Hkv;
   if (R == 0 || a.k == 0) return cudaSuccess;
-  const int T1 = a.Tmax > 0 ? a.Tmax : 1;
-  if ((T1 + kChunk - 1) / kChunk > kMaxChunks) return cudaErrorNotSupported;
   TopkParams p{};
   p.scores = a.scores;
   p.seq_lens = a.seq_lens;
   p.idx = a.idx;
   p.err = a.err;
+  p.list = static_cast<uint2*>(a.L.list);
   p.Hkv = a.Hkv;
   p.Tmax = a.Tmax;
   p.lim = a.maxp_tokens < a.Tmax ? a.maxp_tokens : a.Tmax;
   p.k = a.k;
-  p.w = topk_ws_view(a.L);
-  p.R = R;
-  cudaError_t e;
-  if (!a.zeroed) {
-    e = cudaMemsetAsync(a.L.ghist, 0, a.L.zero_bytes, stream);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.Tmax > 0) {
-    e = launch_pdl(topk_hist_kernel, dim3(a.L.nch, R), dim3(kChunkThreads), 0, stream, p);
-    if (e != cudaSuccess) return e;
-  }
-  // Shared memory: the selected row's kept list (up to kListCap entries) and the chunk prefix.
-  const int smem = kListCap * 8 + (a.L.nch + 1) * 4;
-  e = allow_select_smem(smem);
+  const int smem = static_cast<int>(sizeof(Smem));
+  int max_cs = 8;
+  cudaError_t e = prepare(smem, &max_cs);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_filter_select_kernel, kChunkThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  long long blocks = static_cast<long long>(sm_count()) * per_sm;
-  const long long items = static_cast<long long>(R) * a.L.nch;
-  if (items < blocks) blocks = items;
-  e = launch_pdl(topk_filter_select_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kChunkThreads), smem, stream,
-                 p, static_cast<int>(kListCap));
+  // One pass of kBatch scores per CTA where the cluster allows it.
+  int cs = 1;
+  while (cs < max_cs && static_cast<long long>(cs) * kBatch < a.Tmax) cs *= 2;
+  if (static_cast<long long>(R) * cs > 0x7fffffffLL) return cudaErrorNotSupported;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(R * cs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -49,7 +49,7 @@ extern "C" ds_status ds_topk_select_static(const ds_shape* shape, const float* s
   if (need > static_cast<size_t>(DS_TOPK_STATIC_SCRATCH_BYTES)) return DS_ERR_WORKSPACE;
   void* scratch = static_scratch();
   if (!scratch) return DS_ERR_CUDA;
-  // ds_topk_select clears the counters it needs zeroed at the start of every
-  // call, so leftovers of the previous call in the shared array do no harm.
+  // ds_topk_select needs no initialised scratch (it only spills candidate
+  // lists there), so leftovers of the previous call do no harm.
   return ds_topk_select(shape, scores, seq_lens, k, idx, scratch, DS_TOPK_STATIC_SCRATCH_BYTES, stream);
 }
