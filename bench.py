@@ -162,13 +162,16 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- distributed plumbing
 
 def dist_setup(n_gpus: int):
+    """Joins the torchrun job (one rank per GPU, NCCL; gloo on a host without CUDA)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
 
@@ -179,12 +182,24 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the slowest rank's time decides the job's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def workload_config(w: dsgen.Workload, world: int, flush_mib: int) -> dict:
+    """The `config` object of the JSON line; the same for both arms."""
+    return {"workload": w.name, "batch": w.batch, "seq_len": w.max_seq_len, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "proxy_dim": w.proxy_dim,
+            "label_heads": w.label_heads, "top_k": w.top_k, "kv_dtype": w.kv_dtype, "page_size": w.page_size,
+            "l2": f"flushed before every timed step: {flush_mib} MiB device write, then a "
+                  f"{flush_mib} MiB read so the write-back happens outside the timed region",
+            "parallelism": f"replicas x{world}"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -253,7 +268,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.max_seq_len, "top_k": w.top_k},
+        "config": workload_config(w, world, args.flush_mib),
         "cpu_baseline": {"value": calls_per_s, "unit": "calls/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": calls_per_s, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -408,12 +423,7 @@ def run_ours(args):
         "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "seq_len": w.max_seq_len, "num_q_heads": Hq,
-                   "num_kv_heads": Hkv, "head_dim": D, "proxy_dim": w.proxy_dim, "label_heads": w.label_heads,
-                   "top_k": k, "kv_dtype": w.kv_dtype, "page_size": w.page_size,
-                   "l2": f"flushed before every timed step: {args.flush_mib} MiB device write, then a "
-                         f"{args.flush_mib} MiB read so the write-back happens outside the timed region",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world, args.flush_mib),
         "tokens_per_s": calls_per_s * B, "scanned_tokens_per_s": calls_per_s * sum(w.seq_lens),
         "step_hbm": {"alg_bytes_per_call": ab["total"], "bytes_breakdown": ab, "achieved_gbs": step_gbs,
                      "frac_of_peak": step_gbs / peak},

@@ -1,0 +1,65 @@
+"""Host logic of the benchmark's multi-process path, on CPU: two gloo ranks join
+the job, meet at the barrier, agree on the slowest rank's time, and only rank 0
+prints the reference arm's line."""
+import contextlib
+import io
+import json
+import os
+import socket
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    w, r, _ = bench.dist_setup(world)
+    assert (w, r) == (world, rank)
+    assert dist.get_backend() == "gloo"
+    bench.barrier(w)
+    slowest = bench.max_over_ranks(1.5 + rank, w)
+    # The reference arm under torchrun: rank 0 alone runs the oracle and prints.
+    sys.argv = ["bench.py", "--impl", "reference", "--config", "0", "--steps", "1", "--warmup", "0"]
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        rc = bench.main()
+    bench.barrier(w)
+    dist.destroy_process_group()
+    results.put((rank, slowest, rc, out.getvalue()))
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time_and_only_rank0_prints():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(world):
+        rank, slowest, rc, text = q.get(timeout=300)
+        got[rank] = (slowest, rc, text)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0][0] == got[1][0] == 2.5
+    assert got[0][1] == 0 and got[1][1] == 0
+    assert got[1][2] == ""
+    line = json.loads(got[0][2].strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["unit"] == "calls/s"
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"]["workload"] == "tiny_ds_b1_h4_t4096_c16_k256"

@@ -184,9 +184,9 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
     """The chained decode step (ds_sparse_decode): idx, out and lse from the caches and queries.
 
     ``workspace`` must be zero-filled before its first use (torch.zeros); the
-    call leaves it zero-filled again. With ``events`` (four recorded
-    torch.cuda.Event objects) the instrumented entry point records them before
-    scoring and after scoring, top-k and attention.
+    call leaves it zero-filled again. With ``events`` (four torch.cuda.Event
+    objects with timing enabled) the instrumented entry point records them
+    before scoring and after scoring, top-k and attention.
     """
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(shape.head_dim)
@@ -198,6 +198,11 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
     if events is None:
         st = lib().ds_sparse_decode(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes, _stream(stream))
     else:
+        if len(events) != 4:
+            raise ValueError("events: four torch.cuda.Event objects")
+        for e in events:
+            if not e.cuda_event:   # torch creates the handle on the first record
+                e.record(stream if stream is not None else torch.cuda.current_stream())
         handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         st = lib().ds_sparse_decode_profiled(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes,
                                              _stream(stream), handles)
