@@ -183,8 +183,9 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
                      stream=None, events=None) -> None:
     """The chained decode step (ds_sparse_decode): idx, out and lse from the caches and queries.
 
-    ``workspace`` must be zero-filled before its first use (torch.zeros); the
-    call leaves it zero-filled again. With ``events`` (four torch.cuda.Event
+    ``workspace`` (ds_decode_workspace_bytes bytes) must be zero-filled before
+    its first use (torch.zeros); every call leaves it reusable without
+    clearing. With ``events`` (four torch.cuda.Event
     objects with timing enabled) the instrumented entry point records them
     before scoring and after scoring, top-k and attention.
     """

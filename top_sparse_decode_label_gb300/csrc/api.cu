@@ -75,16 +75,24 @@ int sm_count() {
   return counts[dev];
 }
 
-// Internal split count of the chained call: enough (request, KV head, split)
-// CTAs to cover the GPU about twice, at least 64 selected tokens per split.
+// Internal split count of the chained call: the largest power of two up to
+// 16 (the splits of a (request, KV head) form one thread-block cluster) that
+// keeps the (request, KV head, split) CTAs within about three per SM, with at
+// least 64 selected tokens per split -- and, when the device can be queried,
+// with every cluster resident at once (no second wave).
 int decode_splits(const ds_shape* s, int k) {
   const long long rows = static_cast<long long>(s->batch) * s->num_kv_heads;
   if (rows <= 0 || k <= 64) return 1;
-  long long want = (kDecodeTargetCtas + rows - 1) / rows;
-  long long cap = (k + 63) / 64;
-  if (want > cap) want = cap;
-  if (want > 64) want = 64;
-  return want < 1 ? 1 : static_cast<int>(want);
+  const long long cap = (k + 63) / 64;
+  int S = 1;
+  while (S < 16 && 2 * S <= cap && rows * 2 * S <= kDecodeTargetCtas) S *= 2;
+  const int G = s->num_q_heads / s->num_kv_heads;
+  while (S > 1) {
+    const int resident = sparse_attn_resident_clusters(G, 1, S);
+    if (resident == 0 || 4LL * rows <= 3LL * resident) break;   // unknown device, or one wave with headroom
+    S /= 2;
+  }
+  return S;
 }
 
 }  // namespace ds
@@ -154,7 +162,7 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-             shape->max_pages_per_req * shape->page_size, k, L};
+             shape->max_pages_per_req * shape->page_size, k, L, nullptr, nullptr, nullptr, nullptr, 0, 0, 0, 0};
   return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -162,8 +170,8 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
                              ds_kv_dtype kv_dtype, const float* k_scale, const float* v_scale,
                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* idx, int k,
                              float sm_scale, int num_splits, int split_mode, float* o_part, float* lse_part,
-                             void* out, float* lse, int n_from_seq_len, unsigned* merge_done,
-                             cudaStream_t stream) {
+                             void* out, float* lse, const int32_t* slots, int n_from_seq_len,
+                             int cluster_merge, int pre_wait, cudaStream_t stream) {
   ds_status st = check_shape(shape);
   if (st != DS_OK) return st;
   if (kv_dtype != DS_KV_BF16 && kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
@@ -175,10 +183,10 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || (k > 0 && !idx)) return DS_ERR_INVALID_ARG;
   if (kv_dtype == DS_KV_FP8_E4M3 && (!k_scale || !v_scale)) return DS_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return DS_ERR_INVALID_ARG;
-  if (num_splits == 1 || merge_done) {
+  if (num_splits == 1 || cluster_merge) {
     if (!out || !aligned(out, 4)) return DS_ERR_INVALID_ARG;
   }
-  if (num_splits > 1) {
+  if (num_splits > 1 && !cluster_merge) {
     if (!o_part || !lse_part || !aligned(o_part, 4)) return DS_ERR_INVALID_ARG;
   }
   unsigned* err = error_word();
@@ -186,7 +194,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   AttnArgs a{q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx, o_part, lse_part, out, lse, err,
              shape->batch, shape->num_q_heads, shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
              shape->max_seq_len, k, num_splits, split_mode, kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, sm_scale,
-             n_from_seq_len, merge_done};
+             slots, n_from_seq_len, cluster_merge, pre_wait};
   return from_cuda(launch_sparse_attn(a, stream));
 }
 
@@ -197,7 +205,7 @@ ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void
                                 int num_splits, ds_split_mode split_mode, float* o_part,
                                 float* lse_part, void* out, float* lse, ds_stream_t stream) {
   return attn_common(shape, q, k_cache, v_cache, kv_dtype, k_scale, v_scale, page_table, seq_lens, idx, k,
-                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, 0, nullptr,
+                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, nullptr, 0, 0, 0,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -213,14 +221,14 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
 
 namespace {
 
-// Workspace of the chained call. The merge counters must be zero before the
-// first call; every call leaves them zero again.
+// Workspace of the chained call: the scan's unit counters (zero before the
+// first call, left zero by every call), the scores, the top-k overflow lists
+// and the physical slots of the selection.
 struct DecodeLayout {
+  unsigned* work;   // [2]
   float* scores;
   TopkLayout topk;
-  float* o_part;
-  float* lse_part;
-  unsigned* merge_done;
+  int32_t* slots;   // [B, Hkv, k]
   size_t bytes;
 };
 
@@ -229,17 +237,14 @@ DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
   char* p = static_cast<char*>(base);
   const int R = s->batch * s->num_kv_heads;
   size_t off = 0;
+  L.work = reinterpret_cast<unsigned*>(p + off);
+  off = align256(off + 2 * sizeof(unsigned));
   L.scores = reinterpret_cast<float*>(p + off);
   off = align256(off + static_cast<size_t>(R) * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
   L.topk = topk_layout(p + off, R, s->max_seq_len);
   off = align256(off + L.topk.bytes);
-  const int S = decode_splits(s, k);
-  L.o_part = reinterpret_cast<float*>(p + off);
-  if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * s->head_dim * 4);
-  L.lse_part = reinterpret_cast<float*>(p + off);
-  if (S > 1) off = align256(off + static_cast<size_t>(S) * s->batch * s->num_q_heads * 4);
-  L.merge_done = reinterpret_cast<unsigned*>(p + off);
-  off = align256(off + static_cast<size_t>(R) * 4);
+  L.slots = reinterpret_cast<int32_t*>(p + off);
+  off = align256(off + static_cast<size_t>(R) * (k > 0 ? k : 1) * 4);
   L.bytes = off;
   return L;
 }
@@ -262,7 +267,7 @@ int ds_decode_kernel_launches(const ds_shape* shape, int k) {
   int n = 0;
   if (shape->max_seq_len > 0) n += 1;       // scoring
   if (k > 0) n += 1;                   // top-k (one cluster per row)
-  n += 1;                              // attention (with the merge when split)
+  n += 1;                              // attention (splits merged inside their cluster)
   return n;
 }
 
@@ -283,6 +288,13 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
     return DS_ERR_UNSUPPORTED;
   if (!args->qp || !args->label || !args->page_table || !args->seq_lens) return DS_ERR_INVALID_ARG;
   if (!aligned(args->qp, 16) || !aligned(args->label, 16)) return DS_ERR_INVALID_ARG;
+  // The caches are also touched by the top-k stage (L2 prefetch of the kept
+  // rows): check them before anything is launched.
+  if (args->kv_dtype != DS_KV_BF16 && args->kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
+  if (!args->q || !args->k_cache || !args->v_cache) return DS_ERR_INVALID_ARG;
+  if (!aligned(args->q, 16) || !aligned(args->k_cache, 16) || !aligned(args->v_cache, 16)) return DS_ERR_INVALID_ARG;
+  if (args->kv_dtype == DS_KV_FP8_E4M3 && (!args->k_scale || !args->v_scale)) return DS_ERR_INVALID_ARG;
+  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads)) return DS_ERR_UNSUPPORTED;
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -295,21 +307,25 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (shape->max_seq_len > 0) {
     ScoreArgs sa{args->qp, args->label, args->page_table, args->seq_lens, L.scores, err, shape->batch,
                  shape->num_q_heads, shape->num_kv_heads, args->label_heads, pd, shape->max_pages_per_req,
-                 shape->num_pages, shape->max_seq_len};
+                 shape->num_pages, shape->max_seq_len, L.work};
     st = from_cuda(launch_index_score(sa, s));
     if (st != DS_OK) return st;
   }
   if (mark(1) != cudaSuccess) return DS_ERR_CUDA;
   if (k > 0) {
+    const int row_bytes = shape->head_dim * (args->kv_dtype == DS_KV_FP8_E4M3 ? 1 : 2);
     TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-                shape->max_pages_per_req * shape->page_size, k, L.topk};
+                shape->max_pages_per_req * shape->page_size, k, L.topk, L.slots, args->page_table,
+                args->k_cache, args->v_cache, row_bytes, shape->max_pages_per_req, shape->num_pages,
+                shape->max_seq_len > 0 ? 1 : 0};
     st = from_cuda(launch_topk(ta, s));
     if (st != DS_OK) return st;
   }
   if (mark(2) != cudaSuccess) return DS_ERR_CUDA;
   st = attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
                    args->page_table, args->seq_lens, args->idx, k, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
-                   L.o_part, L.lse_part, args->out, args->lse, 1, S > 1 ? L.merge_done : nullptr, s);
+                   nullptr, nullptr, args->out, args->lse, k > 0 ? L.slots : nullptr, 1, S > 1 ? 1 : 0,
+                   (shape->max_seq_len > 0 || k > 0) ? 1 : 0, s);
   if (st != DS_OK) return st;
   return mark(3) == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }

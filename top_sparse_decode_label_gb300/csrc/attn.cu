@@ -1,6 +1,6 @@
 // Stage 3: sparse GQA decode attention over the selected tokens, gathered
 // from a paged bf16 or FP8-E4M3 KV cache, with the log-sum-exp merge of the
-// split partials optionally fused into the last CTA of each (request, KV head).
+// split partials.
 //
 // "Support double sparsity" (sglang PR #1459): attention over the heavy
 // tokens only. sglang PR #39721: sparse_gqa over the indexer's selection.
@@ -9,20 +9,27 @@
 // sglang PR #43527, "Distributed QSA execution": owner-side partial outputs
 // merged with FP32 log-sum-exp normalisation.
 //
-// One CTA per (request b, KV head g, split j), 4 warps. The CTA first
-// resolves the physical slot (index -> page table -> slot) of every selected
-// token of its chunk into shared memory, in order, with one prefix sum. The
-// K and V rows of those slots are then gathered in tiles of 32 tokens
-// through a ring of cp.async stages (16-byte copies; a bf16 row is 256 B,
-// an e4m3 row 128 B), so the gather keeps many rows in flight per SM. Each
-// warp takes 8 tokens of a tile: one K or V row is read by the whole warp in
-// one conflict-free shared-memory instruction (dims 4l..4l+3 in lane l); the
-// G query heads of the group are in registers (pre-scaled by sm_scale*log2 e),
-// a transposed butterfly turns the J x G partial dot products into one logit
-// per lane, and online softmax accumulates P.V into 4 dims x G heads per lane.
-// The warps' states are combined in shared memory; the CTA writes the final
-// bf16 output (one split) or fp32 partials, and with a fused merge the CTA
-// that finishes a (b, g) last merges all splits.
+// One CTA per (request b, KV head g, split j), 4 warps. The CTA resolves the
+// physical slot (index -> page table -> slot) of every selected token of its
+// chunk into shared memory, in order, with one prefix sum. Each warp then
+// takes every fourth 16-token tile and gathers its K and V rows into its own
+// ring of shared-memory stages with 16-byte cp.async copies (rows XOR-swizzled
+// by 16-byte chunk so that ldmatrix reads are conflict-free), waiting only on
+// its own copies. Per tile the warp computes, on the tensor cores
+// (mma.sync m16n8k16, fp32 accumulators):
+//   S^T[16 tokens x 8 heads] = K_tile[16 x 128] . Q^T[128 x 8]
+//   O^T[128 dims x 8 heads] += V_tile^T[128 x 16] . P^T[16 x 8]
+// with the group's G <= 8 query heads as the N = 8 columns, an online softmax
+// on the S^T fragments (exp2 domain), and P^T moved into the B-operand layout
+// with movmatrix. bf16 caches feed bf16 MMAs directly; e4m3 rows are loaded
+// as byte pairs and converted to f16 in registers (the dimension order inside
+// each 16-wide step is permuted identically in K and in Q, and the V rows'
+// dimension order is undone when writing the output), the query is scaled by
+// a power of two into f16 range, and the per-page K scale multiplies the
+// logits and the V scale the probabilities. The warps' states are combined in
+// shared memory. One split writes bf16 out; several write fp32 partials, or,
+// when the splits of a (b, g) run as one thread-block cluster, merge through
+// distributed shared memory with no global round trip.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -34,7 +41,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 32;     // tokens per gather stage
+constexpr int kTok = 16;      // tokens per warp tile
 constexpr int kSeg = 512;     // selected positions resolved at a time
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -48,50 +55,109 @@ struct AttnParams {
   const int32_t* page_table;
   const int32_t* seq_lens;
   const int32_t* idx;
+  const int32_t* slots;   // non-null: physical slot per selected position (-1 = skip); idx unused
   float* o_part;
   float* lse_part;
   __nv_bfloat16* out;
   float* lse;
   unsigned* err;
-  unsigned* merge_done;
-  int B, Hq, Hkv, maxp, num_pages, lim, k, S, split_mode, n_known, nst;
-  float qscale;  // sm_scale * log2(e)
+  int B, Hq, Hkv, maxp, num_pages, lim, k, S, split_mode, n_known;
+  int cluster_merge;   // the S splits of a (b, g) are one cluster: merge in shared memory
+  int pre_wait;        // q may be read before waiting on the previous kernel
+  float qscale;        // sm_scale * log2(e)
+};
+
+template <bool FP8>
+struct Cfg {
+  static constexpr int ROWB = FP8 ? kHeadDim : kHeadDim * 2;   // bytes per K or V row
+  static constexpr int NST = FP8 ? 4 : 2;                       // ring stages per warp
+  static constexpr int STAGE = 2 * kTok * ROWB;                 // K tile then V tile
+  static constexpr int RING = kWarps * NST * STAGE;
+  static constexpr int SMEM = RING + kSeg * 4 + (FP8 ? kSeg * 8 : 0);
 };
 
 template <int G, bool FP8>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams p) {
-  constexpr int J = (G >= 4) ? 32 / G : 8;   // tokens per sub-tile
-  constexpr int V = J * G;                   // logits per sub-tile (<= 32)
-  constexpr int SH = (V >= 32) ? 0 : (V == 16 ? 1 : (V == 8 ? 2 : 3));  // lane -> value shift
-  constexpr int ROWB = FP8 ? kHeadDim : kHeadDim * 2;  // bytes per K/V row
-  constexpr int CPR = ROWB / 16;                        // 16-byte copies per row
-  constexpr int STAGE = 2 * kTile * ROWB;               // K tile then V tile
-  constexpr int CPT = 2 * kTile * CPR / kThreads;       // copies per thread per stage
-  constexpr int WTOK = kTile / kWarps;                  // tokens per warp per tile (8)
+  using C = Cfg<FP8>;
+  constexpr int ROWB = C::ROWB;
+  constexpr int NST = C::NST;
+  constexpr int CPR = ROWB / 16;          // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR;           // rows a warp copies per instruction
+  constexpr int NI = kTok / RPI;          // copy instructions per lane per K (or V) tile
 
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  int* sl = reinterpret_cast<int*>(smem + static_cast<size_t>(p.nst) * STAGE);   // [kSeg] slots
-  float2* sc = reinterpret_cast<float2*>(sl + kSeg);                             // [kSeg] (kscale, vscale)
-  __shared__ float sm_m[kWarps][G];
-  __shared__ float sm_l[kWarps][G];
-  __shared__ float sm_o[kWarps][G][kHeadDim];
+  int* sl = reinterpret_cast<int*>(smem + C::RING);                 // [kSeg] slots
+  float2* sc = reinterpret_cast<float2*>(sl + kSeg);                // [kSeg] (k scale, v scale)
+  __shared__ float wm[kWarps][8], wl[kWarps][8];
+  __shared__ float cm[8], cl[8];
   __shared__ unsigned sh_scan[33];
   __shared__ unsigned sh_cnt[kWarps];
-  __shared__ int sh_last;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  const int pr = lane >> 2;   // fragment row group
+  const int qc = lane & 3;    // fragment column pair
   const int j = blockIdx.x % p.S;
   const int bg = blockIdx.x / p.S;
   const int g = bg % p.Hkv;
   const int b = bg / p.Hkv;
-  const int32_t* row = p.idx + static_cast<long long>(bg) * p.k;
+
+  // ---- query B fragments: head pr of the group (0 past G), 8 k-steps.
+  uint32_t qb[8][2];
+  float qs = p.qscale;
+  auto load_q = [&]() {
+    float qv[8][4];
+    const bool hv = pr < G;
+    const uint16_t* qrow = p.q + (static_cast<long long>(b) * p.Hq + g * G + (hv ? pr : 0)) * kHeadDim;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      // bf16: dims 16kk + 2qc (+1) and +8; e4m3 order: dims 16kk + 4qc .. 4qc + 3
+      const int d0 = FP8 ? 16 * kk + 4 * qc : 16 * kk + 2 * qc;
+      const int d1 = FP8 ? d0 + 2 : d0 + 8;
+      const uint32_t w0 = hv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
+      const uint32_t w1 = hv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
+      if (!FP8) {
+        qb[kk][0] = w0;
+        qb[kk][1] = w1;
+      } else {
+        qv[kk][0] = bf16_lo(w0);
+        qv[kk][1] = bf16_hi(w0);
+        qv[kk][2] = bf16_lo(w1);
+        qv[kk][3] = bf16_hi(w1);
+      }
+    }
+    if (FP8) {
+      // Scale the query by 2^sh so that its largest magnitude lies in
+      // [2^13, 2^14): f16 keeps every bf16 mantissa there without overflow.
+      float mx = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[kk][i]));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      int sh = 0;
+      if (mx > 0.f && mx < INFINITY) sh = 13 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xff) - 127);
+      sh = max(-100, min(100, sh));
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);   // 2^sh, exact
+      qs = p.qscale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][0] = pack_f16(qv[kk][0] * up, qv[kk][1] * up);
+        qb[kk][1] = pack_f16(qv[kk][2] * up, qv[kk][3] * up);
+      }
+    }
+  };
+  if (p.pre_wait) load_q();
   grid_dependency_wait();
+  grid_launch_dependents();
+  if (!p.pre_wait) load_q();
 
   int T = p.seq_lens[b];
   if (T < 0 || T > p.lim) T = T < 0 ? 0 : p.lim;  // flagged by the scoring / top-k stages
+  const int32_t* row = p.idx + static_cast<long long>(bg) * p.k;
 
   int n;
   if (p.n_known) {
@@ -113,30 +179,18 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
     p1 = static_cast<int>(static_cast<long long>(j + 1) * n / p.S);
   }
 
-  // Query heads g*G .. g*G+G-1, dims 4*lane .. 4*lane+3, scaled to log2 units.
-  float qf[G][4];
+  float m0 = -INFINITY, m1 = -INFINITY;   // running max of heads 2qc, 2qc+1 (log2 units)
+  float l0 = 0.f, l1 = 0.f;                // this lane's share of the running sums
+  float acc[8][4];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.q + (static_cast<long long>(b) * p.Hq + g * G + h) * kHeadDim + lane * 4));
-    qf[h][0] = bf16_lo(w.x) * p.qscale;
-    qf[h][1] = bf16_hi(w.x) * p.qscale;
-    qf[h][2] = bf16_lo(w.y) * p.qscale;
-    qf[h][3] = bf16_hi(w.y) * p.qscale;
-  }
-  float m[G], o[G][4];
+  for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[h][i] = 0.f;
-  }
-  float lsum = 0.f;  // running sum of the (token, head) value this lane holds
-  const int my_v = lane >> SH;
-  const int my_h = my_v % G;
-  const int my_j = my_v / G;
+    for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
 
   const long long head_off = static_cast<long long>(g) * ROWB;
   const long long slot_stride = static_cast<long long>(p.Hkv) * ROWB;
+  unsigned char* wring = ring + warp * NST * C::STAGE;
+  const uint32_t wring_s = smem_u32(wring);
 
   for (int sb = p0; sb < p1; sb += kSeg) {
     const int se = min(p1, sb + kSeg);
@@ -150,7 +204,14 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       const int pos = sb + tid * PPT + i;
       slot_v[i] = -1;
       sc_v[i] = make_float2(1.f, 1.f);
-      if (pos < se) {
+      if (pos < se && p.slots) {
+        const int sv = __ldcg(p.slots + static_cast<long long>(bg) * p.k + pos);
+        if (sv >= 0) {
+          slot_v[i] = sv;
+          if (FP8) sc_v[i] = make_float2(__ldg(p.ks + sv / kPage), __ldg(p.vs + sv / kPage));
+          ++cnt;
+        }
+      } else if (pos < se) {
         const int t = row[pos];
         bool ok = t >= 0;
         if (ok && t >= T) {
@@ -170,8 +231,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
         }
       }
     }
-    unsigned nseg;
-    unsigned wpos = block_excl_scan(cnt, sh_scan, &nseg);
+    unsigned nseg_u;
+    unsigned wpos = block_excl_scan(cnt, sh_scan, &nseg_u);
 #pragma unroll
     for (int i = 0; i < PPT; ++i) {
       if (slot_v[i] >= 0) {
@@ -181,214 +242,267 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       }
     }
     __syncthreads();
-    const int ntile = (static_cast<int>(nseg) + kTile - 1) / kTile;
+    const int nseg = static_cast<int>(nseg_u);
+    const int ntile = (nseg + kTok - 1) / kTok;
+    const int nt_w = ntile > warp ? (ntile - warp + kWarps - 1) / kWarps : 0;   // this warp's tiles
 
-    auto issue = [&](int tile, int stage) {
-      unsigned char* dst = ring + stage * STAGE;
+    // Copies of tile `tile` into stage `st` of this warp's ring: chunk c of
+    // row r lands at chunk position c ^ (r & 7).
+    auto issue = [&](int tile, int st) {
+      unsigned char* dst = wring + st * C::STAGE;
+      const int c = lane % CPR;
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        const int id = c * kThreads + tid;          // 0 .. 2*kTile*CPR-1
-        const int kv = id / (kTile * CPR);          // 0: K, 1: V
-        const int r = (id / CPR) % kTile;
-        const int part = id % CPR;
-        const int e = tile * kTile + r;
-        const bool ok = e < static_cast<int>(nseg);
-        const uint8_t* base = kv ? p.vc : p.kc;
-        const uint8_t* src = ok ? base + sl[e] * slot_stride + head_off + part * 16 : base;
-        cp_async16(dst + id * 16, src, ok);
+      for (int i = 0; i < NI; ++i) {
+        const int r = lane / CPR + RPI * i;
+        const int e = tile * kTok + r;
+        const bool ok = e < nseg;
+        const long long off = ok ? static_cast<long long>(sl[e]) * slot_stride + head_off + c * 16 : 0;
+        const int so = r * ROWB + ((c ^ (r & 7)) << 4);
+        cp_async16(dst + so, p.kc + off, ok);
+        cp_async16(dst + kTok * ROWB + so, p.vc + off, ok);
       }
     };
 
-    for (int s = 0; s < p.nst; ++s) {
-      if (s < ntile) issue(s, s);
+#pragma unroll
+    for (int s = 0; s < NST; ++s) {
+      if (s < nt_w) issue(warp + kWarps * s, s);
       cp_async_commit();
     }
-    for (int tile = 0; tile < ntile; ++tile) {
-      const int stage = tile % p.nst;
-      cp_async_wait_dyn(p.nst - 1);
-      __syncthreads();
-      const unsigned char* kt = ring + stage * STAGE;
-      const unsigned char* vt = kt + kTile * ROWB;
-      const int tok_base = tile * kTile + warp * WTOK;   // entry index of this warp's first token
+    for (int it = 0; it < nt_w; ++it) {
+      const int st = it % NST;
+      const int tile = warp + kWarps * it;
+      cp_async_wait<NST - 1>();
+      __syncwarp();
+      const uint32_t kb = wring_s + st * C::STAGE;
+      const uint32_t vb = kb + kTok * ROWB;
+
+      // ---- S^T = K . Q^T
+      float sa[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!FP8) {
+        const int r = lane & 15;
+        const uint32_t rb = kb + r * ROWB;
+        const int x = (lane >> 4) ^ (r & 7);
 #pragma unroll
-      for (int sub = 0; sub < WTOK / J; ++sub) {
-        const int r0 = warp * WTOK + sub * J;           // row within the tile
-        const int e0 = tok_base + sub * J;              // entry index
-        const int nvalid = min(J, static_cast<int>(nseg) - e0);
-        if (nvalid <= 0) break;
-        float part[V];
-#pragma unroll
-        for (int jj = 0; jj < J; ++jj) {
-          float k0, k1, k2, k3;
-          if (FP8) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + (r0 + jj) * ROWB + lane * 4);
-            const float2 a = e4m3x2_to_float2(w);
-            const float2 c = e4m3x2_to_float2(w >> 16);
-            k0 = a.x; k1 = a.y; k2 = c.x; k3 = c.y;
-          } else {
-            const uint2 w = *reinterpret_cast<const uint2*>(kt + (r0 + jj) * ROWB + lane * 8);
-            k0 = bf16_lo(w.x); k1 = bf16_hi(w.x); k2 = bf16_lo(w.y); k3 = bf16_hi(w.y);
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float a = qf[h][0] * k0;
-            a = fmaf(qf[h][1], k1, a);
-            a = fmaf(qf[h][2], k2, a);
-            a = fmaf(qf[h][3], k3, a);
-            part[jj * G + h] = a;
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(rb + (((2 * kk) ^ x) << 4), a0, a1, a2, a3);
+          mma_bf16(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         }
-        transposed_reduce<32, V>(part);
-        // This lane now holds the logit of (token my_j, head my_h) of the sub-tile.
-        const bool tv = my_j < nvalid;
-        float2 scl = make_float2(1.f, 1.f);
-        if (FP8 && tv) scl = sc[e0 + my_j];
-        const float z = tv ? part[0] * scl.x : -INFINITY;
-        float zm = z;
+      } else {
+        const int mi = lane >> 3;
+        const int r = (lane & 7) + 8 * (mi & 1);
+        const uint32_t rb = kb + r * ROWB;
+        const int x = (mi >> 1) ^ (lane & 7);
 #pragma unroll
-        for (int off = (1 << SH) * G; off < 32; off <<= 1) zm = fmaxf(zm, __shfl_xor_sync(kFull, zm, off));
-        float mnew[G], corr[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float tm = __shfl_sync(kFull, zm, h << SH);
-          mnew[h] = fmaxf(m[h], tm);
-          corr[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
-          m[h] = mnew[h];
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(rb + (((2 * cc) ^ x) << 4), r0, r1, r2, r3);
+          mma_f16(sa, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                  e4m3x2_to_f16x2(r1 >> 16), qb[2 * cc][0], qb[2 * cc][1]);
+          mma_f16(sa, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                  e4m3x2_to_f16x2(r3 >> 16), qb[2 * cc + 1][0], qb[2 * cc + 1][1]);
         }
-        float my_m = mnew[0], my_corr = corr[0];
-#pragma unroll
-        for (int h = 1; h < G; ++h) {
-          my_m = (my_h == h) ? mnew[h] : my_m;
-          my_corr = (my_h == h) ? corr[h] : my_corr;
+      }
+
+      // ---- online softmax on tokens pr (lo) and pr + 8 (hi), heads 2qc, 2qc + 1
+      const int e_lo = tile * kTok + pr;
+      const int e_hi = e_lo + 8;
+      float kl = qs, kh = qs, vl = 1.f, vh = 1.f;
+      if (FP8) {
+        if (e_lo < nseg) {
+          const float2 t = sc[e_lo];
+          kl *= t.x;
+          vl = t.y;
         }
-        const float pw = (z == -INFINITY) ? 0.f : exp2f(z - my_m);
-        lsum = lsum * my_corr + pw;
-        const float pv = FP8 ? pw * scl.y : pw;
+        if (e_hi < nseg) {
+          const float2 t = sc[e_hi];
+          kh *= t.x;
+          vh = t.y;
+        }
+      }
+      const float s0 = e_lo < nseg ? sa[0] * kl : -INFINITY;
+      const float s1 = e_lo < nseg ? sa[1] * kl : -INFINITY;
+      const float s2 = e_hi < nseg ? sa[2] * kh : -INFINITY;
+      const float s3 = e_hi < nseg ? sa[3] * kh : -INFINITY;
+      float t0 = fmaxf(s0, s2), t1 = fmaxf(s1, s3);
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+      for (int o = 4; o < 32; o <<= 1) {
+        t0 = fmaxf(t0, __shfl_xor_sync(kFull, t0, o));
+        t1 = fmaxf(t1, __shfl_xor_sync(kFull, t1, o));
+      }
+      const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);   // finite: the tile has a valid token
+      const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      const float e0 = exp2f(s0 - n0), e1 = exp2f(s1 - n1), e2 = exp2f(s2 - n0), e3 = exp2f(s3 - n1);
+      l0 = l0 * c0 + e0 + e2;
+      l1 = l1 * c1 + e1 + e3;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[h][i] *= corr[h];
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[mt][0] *= c0;
+        acc[mt][1] *= c1;
+        acc[mt][2] *= c0;
+        acc[mt][3] *= c1;
+      }
+      uint32_t pb0, pb1;
+      if (!FP8) {
+        pb0 = movm_t(pack_bf16(e0, e1));
+        pb1 = movm_t(pack_bf16(e2, e3));
+      } else {
+        pb0 = movm_t(pack_f16(e0 * vl, e1 * vl));
+        pb1 = movm_t(pack_f16(e2 * vh, e3 * vh));
+      }
+
+      // ---- O^T += V^T . P^T
+      {
+        const int mi = lane >> 3;
+        if (!FP8) {
+          // matrices: (tokens 0-7, chunk 2mt), (tokens 0-7, chunk 2mt+1),
+          //           (tokens 8-15, chunk 2mt), (tokens 8-15, chunk 2mt+1)
+          const uint32_t rb = vb + ((lane & 7) + 8 * (mi >> 1)) * ROWB;
+          const int x = (mi & 1) ^ (lane & 7);
 #pragma unroll
-        for (int jj = 0; jj < J; ++jj) {
-          float v0, v1, v2, v3;
-          if (FP8) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + (r0 + jj) * ROWB + lane * 4);
-            const float2 a = e4m3x2_to_float2(w);
-            const float2 c = e4m3x2_to_float2(w >> 16);
-            v0 = a.x; v1 = a.y; v2 = c.x; v3 = c.y;
-          } else {
-            const uint2 w = *reinterpret_cast<const uint2*>(vt + (r0 + jj) * ROWB + lane * 8);
-            v0 = bf16_lo(w.x); v1 = bf16_hi(w.x); v2 = bf16_lo(w.y); v3 = bf16_hi(w.y);
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(rb + (((2 * mt) ^ x) << 4), a0, a1, a2, a3);
+            mma_bf16(acc[mt], a0, a1, a2, a3, pb0, pb1);
           }
+        } else {
+          // matrices: (tokens 0-7, chunk 2cc), (tokens 8-15, chunk 2cc),
+          //           (tokens 0-7, chunk 2cc+1), (tokens 8-15, chunk 2cc+1)
+          const int r8 = (lane & 7) + 8 * (mi & 1);
+          const uint32_t rb8 = vb + r8 * ROWB;
+          const int x = (mi >> 1) ^ (lane & 7);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float pj = __shfl_sync(kFull, pv, (jj * G + h) << SH);
-            o[h][0] = fmaf(pj, v0, o[h][0]);
-            o[h][1] = fmaf(pj, v1, o[h][1]);
-            o[h][2] = fmaf(pj, v2, o[h][2]);
-            o[h][3] = fmaf(pj, v3, o[h][3]);
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(rb8 + (((2 * cc) ^ x) << 4), r0, r1, r2, r3);
+            // (token 2qc, dims 2pr, 2pr+1), (token 2qc+1, ...) -> per-dim token pairs
+            const uint32_t u0 = __byte_perm(r0, 0, 0x3120), u1 = __byte_perm(r1, 0, 0x3120);
+            const uint32_t u2 = __byte_perm(r2, 0, 0x3120), u3 = __byte_perm(r3, 0, 0x3120);
+            mma_f16(acc[2 * cc], e4m3x2_to_f16x2(u0), e4m3x2_to_f16x2(u0 >> 16), e4m3x2_to_f16x2(u1),
+                    e4m3x2_to_f16x2(u1 >> 16), pb0, pb1);
+            mma_f16(acc[2 * cc + 1], e4m3x2_to_f16x2(u2), e4m3x2_to_f16x2(u2 >> 16), e4m3x2_to_f16x2(u3),
+                    e4m3x2_to_f16x2(u3 >> 16), pb0, pb1);
           }
         }
       }
-      __syncthreads();
-      if (tile + p.nst < ntile) issue(tile + p.nst, stage);
+      __syncwarp();
+      if (it + NST < nt_w) issue(warp + kWarps * (it + NST), st);
       cp_async_commit();
     }
     cp_async_wait<0>();
     __syncthreads();
   }
 
-  // Per-head sums of this warp: add the lanes of the other tokens.
+  // ---- this warp's state -> shared memory (the ring is free now)
 #pragma unroll
-  for (int off = (1 << SH) * G; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, o);
+    l1 += __shfl_xor_sync(kFull, l1, o);
+  }
+  float* wo = reinterpret_cast<float*>(ring);   // [kWarps][G][kHeadDim]
+  const int h0 = 2 * qc, h1 = 2 * qc + 1;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float lh = __shfl_sync(kFull, lsum, h << SH);
-    if (lane == 0) {
-      sm_m[warp][h] = m[h];
-      sm_l[warp][h] = lh;
+  for (int mt = 0; mt < 8; ++mt) {
+    // bf16: rows pr / pr + 8 are dims 16mt + pr / + 8; e4m3: dims 16mt + 2pr / + 1
+    const int da = FP8 ? 16 * mt + 2 * pr : 16 * mt + pr;
+    const int db = FP8 ? da + 1 : da + 8;
+    if (h0 < G) {
+      wo[(warp * G + h0) * kHeadDim + da] = acc[mt][0];
+      wo[(warp * G + h0) * kHeadDim + db] = acc[mt][2];
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sm_o[warp][h][lane * 4 + i] = o[h][i];
+    if (h1 < G) {
+      wo[(warp * G + h1) * kHeadDim + da] = acc[mt][1];
+      wo[(warp * G + h1) * kHeadDim + db] = acc[mt][3];
+    }
+  }
+  if (pr == 0) {
+    if (h0 < G) {
+      wm[warp][h0] = m0;
+      wl[warp][h0] = l0;
+    }
+    if (h1 < G) {
+      wm[warp][h1] = m1;
+      wl[warp][h1] = l1;
+    }
   }
   __syncthreads();
 
-  // Combine the warps: the log-sum-exp merge of kWarps partial states.
-  for (int e = tid; e < G * kHeadDim; e += kThreads) {
-    const int h = e / kHeadDim;
-    const int d = e % kHeadDim;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
-    float L = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float c = (sm_m[w][h] == -INFINITY) ? 0.f : exp2f(sm_m[w][h] - M);
-        L += c * sm_l[w][h];
-        acc += c * sm_o[w][h][d];
-      }
-    }
-    const float val = (L > 0.f) ? acc / L : 0.f;
-    const float lse = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
-    const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
-    if (p.S == 1) {
-      p.out[qrow * kHeadDim + d] = __float2bfloat16_rn(val);
-      if (d == 0 && p.lse) p.lse[qrow] = lse;
-    } else {
-      const long long prow = static_cast<long long>(j) * p.B * p.Hq + qrow;
-      p.o_part[prow * kHeadDim + d] = val;
-      if (d == 0) p.lse_part[prow] = lse;
-    }
-  }
-  if (p.S == 1 || !p.merge_done) return;
-
-  // ---- fused merge: the CTA that finishes (b, g) last merges its S splits.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh_last = (atomicAdd(p.merge_done + bg, 1u) + 1 == static_cast<unsigned>(p.S));
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-  const long long rows = static_cast<long long>(p.B) * p.Hq;
-  const long long qrow0 = static_cast<long long>(b) * p.Hq + g * G;
-  // All split lse values of the group's heads in one round of loads, then the
-  // merge weights exp(lse_s - lse) in shared memory (reusing the ring).
-  float* sw = reinterpret_cast<float*>(ring);          // [S][G] weights
-  float* slse = sw + p.S * G;                          // [G] merged lse
-  for (int i = tid; i < p.S * G; i += kThreads) sw[i] = __ldcg(p.lse_part + (i / G) * rows + qrow0 + (i % G));
-  __syncthreads();
+  // ---- combine the warps: state (M, L, O unnormalised) per (head, dim)
+  float* co = wo + kWarps * G * kHeadDim;   // [G][kHeadDim]
   if (tid < G) {
     float M = -INFINITY;
-    for (int s = 0; s < p.S; ++s) M = fmaxf(M, sw[s * G + tid]);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][tid]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int s = 0; s < p.S; ++s) L += expf(sw[s * G + tid] - M);
-    const float lse = (M == -INFINITY) ? -INFINITY : M + logf(L);
-    slse[tid] = lse;
-    for (int s = 0; s < p.S; ++s) {
-      const float ls = sw[s * G + tid];
-      sw[s * G + tid] = (ls == -INFINITY) ? 0.f : expf(ls - lse);
-    }
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) L += (wm[w][tid] == -INFINITY) ? 0.f : exp2f(wm[w][tid] - M) * wl[w][tid];
+    cm[tid] = M;
+    cl[tid] = L;
   }
   __syncthreads();
   for (int e = tid; e < G * kHeadDim; e += kThreads) {
     const int h = e / kHeadDim;
     const int d = e % kHeadDim;
-    float acc = 0.f;
-    for (int s0 = 0; s0 < p.S; s0 += 8) {
-      float v[8];
+    const float M = cm[h];
+    float acc_o = 0.f;
+    if (M != -INFINITY)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[i] = (s0 + i < p.S) ? __ldcg(p.o_part + ((s0 + i) * rows + qrow0 + h) * kHeadDim + d) : 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (s0 + i < p.S) acc = fmaf(sw[(s0 + i) * G + h], v[i], acc);
+      for (int w = 0; w < kWarps; ++w)
+        acc_o += (wm[w][h] == -INFINITY) ? 0.f : exp2f(wm[w][h] - M) * wo[(w * G + h) * kHeadDim + d];
+    const float L = cl[h];
+    const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
+    if (p.cluster_merge) {
+      co[e] = acc_o;
+    } else if (p.S == 1) {
+      p.out[qrow * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? acc_o / L : 0.f);
+      if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    } else {
+      const long long prow = static_cast<long long>(j) * p.B * p.Hq + qrow;
+      p.o_part[prow * kHeadDim + d] = L > 0.f ? acc_o / L : 0.f;
+      if (d == 0) p.lse_part[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
-    p.out[(qrow0 + h) * kHeadDim + d] = __float2bfloat16_rn(acc);
-    if (d == 0 && p.lse) p.lse[qrow0 + h] = slse[h];
   }
-  if (tid == 0) atomicExch(p.merge_done + bg, 0u);
+  if (!p.cluster_merge) return;
+
+  // ---- merge the cluster's S splits: CTA j finishes elements [e0, e1)
+  cluster_sync();
+  const int E = G * kHeadDim;
+  const int e0 = j * E / p.S, e1 = (j + 1) * E / p.S;
+  for (int e = e0 + tid; e < e1; e += kThreads) {
+    const int h = e / kHeadDim;
+    const int d = e % kHeadDim;
+    float Ms[16], Ls[16], Os[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s < p.S) {
+        Ms[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cm + h), s)));
+        Ls[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cl + h), s)));
+        Os[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(co + e), s)));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < p.S) M = fmaxf(M, Ms[s]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        if (s < p.S && Ms[s] != -INFINITY) {
+          const float w = exp2f(Ms[s] - M);
+          L += w * Ls[s];
+          O += w * Os[s];
+        }
+      }
+    }
+    const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
+    p.out[qrow * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+  cluster_sync();   // keep this CTA's shared memory until every CTA has read it
 }
 
 using KernelFn = void (*)(const AttnParams);
@@ -404,22 +518,29 @@ KernelFn pick(int G) {
   return nullptr;
 }
 
-cudaError_t allow_smem(KernelFn fn, int bytes) {
-  struct Entry { KernelFn fn; int dev; int bytes; };
+cudaError_t prepare(KernelFn fn, int bytes) {
+  struct Entry { KernelFn fn; int dev; };
   static Entry done[64];
   static int n = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   for (int i = 0; i < n; ++i)
-    if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+    if (done[i].fn == fn && done[i].dev == dev) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && n < 64) done[n++] = Entry{fn, dev, bytes};
-  return e;
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // clusters stay at the portable size
+  }
+  if (n < 64) done[n++] = Entry{fn, dev};
+  return cudaSuccess;
 }
 
 }  // namespace
 
 bool sparse_attn_supported(int G) { return pick<false>(G) != nullptr; }
+
+int sparse_attn_smem_bytes(int fp8) { return fp8 ? Cfg<true>::SMEM : Cfg<false>::SMEM; }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
@@ -427,6 +548,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (!fn) return cudaErrorNotSupported;
   const long long blocks = static_cast<long long>(a.B) * a.Hkv * a.S;
   if (blocks == 0) return cudaSuccess;
+  if (a.cluster_merge && (a.S > 16 || a.split_mode != 0)) return cudaErrorInvalidValue;
   AttnParams p{};
   p.q = static_cast<const uint16_t*>(a.q);
   p.kc = static_cast<const uint8_t*>(a.k_cache);
@@ -436,12 +558,12 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.page_table = a.page_table;
   p.seq_lens = a.seq_lens;
   p.idx = a.idx;
+  p.slots = a.slots;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.err = a.err;
-  p.merge_done = a.merge_done;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -453,15 +575,61 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.split_mode = a.split_mode;
   p.qscale = a.sm_scale * kLog2e;
   p.n_known = a.n_from_seq_len;
-  const int rowb = a.fp8 ? kHeadDim : kHeadDim * 2;
-  const int stage = 2 * kTile * rowb;
-  p.nst = a.fp8 ? 6 : 4;
-  const int smem = p.nst * stage + kSeg * (a.fp8 ? 4 + 8 : 4);
-  cudaError_t e = allow_smem(fn, smem);
+  p.cluster_merge = a.cluster_merge;
+  p.pre_wait = a.pre_wait;
+  const int smem = sparse_attn_smem_bytes(a.fp8);
+  cudaError_t e = prepare(fn, smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.cluster_merge ? a.S : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, fn, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+int sparse_attn_resident_clusters(int G, int fp8, int S) {
+  static int cache[2][9][5][64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int si = S == 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : S == 16 ? 4 : -1;
+  if (si < 0) return 0;
+  int& c = cache[fp8 ? 1 : 0][G][si][dev];
+  if (c) return c > 0 ? c : 0;
+  KernelFn fn = fp8 ? pick<true>(G) : pick<false>(G);
+  if (!fn) return 0;
+  const int smem = sparse_attn_smem_bytes(fp8);
+  if (prepare(fn, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 0) n = 0;
+  cudaGetLastError();
+  c = n > 0 ? n : -1;
+  return n;
 }
 
 }  // namespace ds

@@ -22,6 +22,65 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t w) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// Two e4m3 bytes (low 16 bits of w) -> an f16 pair (exact: every e4m3 value
+// is an f16 value), low byte in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// ---- warp-level tensor-core fragments (m16n8k16, fp32 accumulate)
+
+// Four 8x8 16-bit matrices from shared memory; lane l gives the row address of
+// matrix l / 8, row l % 8. Without .trans lane l receives (row l/4, columns
+// 2(l%4), 2(l%4)+1) of each matrix; with .trans (rows 2(l%4), 2(l%4)+1,
+// column l/4).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// Transpose of an 8x8 16-bit matrix held one row pair per lane (lane l: row
+// l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+// d += A (16x16, row) * B (16x8, col); bf16 or f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Two fp32 -> packed bf16 / f16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 16-byte read-only load that does not allocate in L1 (streamed data).
 __device__ __forceinline__ uint4 ld_nc_na_16(const void* p) {
   uint4 r;
@@ -118,6 +177,13 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // attribute). Every kernel calls it before touching memory an earlier
 // kernel of the stream may write or read.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream (launched with programmatic dependent
+// launch) be scheduled once every CTA of this grid has executed it or exited;
+// the next kernel still waits in grid_dependency_wait() for this grid to
+// complete before it reads any result.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Brings the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // Order-preserving map float -> uint32: a > b  <=>  key(a) > key(b).
 // -0.0 and +0.0 share one key; every NaN maps to 0, below every number.

@@ -33,6 +33,7 @@ struct ScoreArgs {
   float* scores;           // [B, Hkv, Tmax]
   unsigned* err;
   int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
+  unsigned* work;          // [2] zeroed unit counters (left zero): dynamic unit scheduling; null: static
 };
 // Returns a cudaError_t; cudaErrorNotSupported for shapes without a kernel.
 cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream);
@@ -45,6 +46,14 @@ struct TopkArgs {
   unsigned* err;
   int B, Hkv, Tmax, maxp_tokens, k;
   TopkLayout L;
+  // Chained call only (slots == nullptr otherwise): physical slots of the kept
+  // tokens ([B, Hkv, k], -1 past K_eff) and L2 prefetch of their K/V rows.
+  int32_t* slots;
+  const int32_t* page_table;
+  const void* k_cache;
+  const void* v_cache;
+  int row_bytes, maxp, num_pages;
+  int pre_wait;            // inputs may be read before the previous kernel completes
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
@@ -64,11 +73,16 @@ struct AttnArgs {
   unsigned* err;
   int B, Hq, Hkv, maxp, num_pages, Tmax, k, S, split_mode, fp8;
   float sm_scale;
+  const int32_t* slots;    // non-null: physical slots per selected position ([B, Hkv, k], -1 = skip), idx unused
   int n_from_seq_len;      // 1: each idx row holds exactly min(k, seq_len) valid entries (top-k output)
-  unsigned* merge_done;    // non-null (S > 1): [B, Hkv] zeroed counters; the last split CTA merges into out
+  int cluster_merge;       // 1: the S (<= 16) splits of a (b, g) run as one cluster and merge into out
+  int pre_wait;            // 1: q may be read before the previous kernel of the stream completes
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 bool sparse_attn_supported(int G);
+// Clusters of S attention CTAs the current device keeps resident at once (0
+// when it cannot be determined).
+int sparse_attn_resident_clusters(int G, int fp8, int S);
 
 cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const float* lse_part,
                              void* out, float* lse, cudaStream_t stream);

@@ -13,12 +13,17 @@
 // HBM-bound scan. The label cache is cut into 16 KB units: consecutive tokens
 // of one request, either whole token rows (HL*C*2 bytes <= 512) or one
 // 512-byte block of heads of each token (per-head label with many heads). A
-// persistent grid gives each CTA a contiguous range of units. In each CTA a
-// producer warp streams the units into a ring of shared-memory stages with
+// persistent grid takes the units in request order: with a work counter
+// (chained call) each CTA's producer claims 4 units at a time with one
+// atomicAdd, so faster CTAs take more work and all CTAs finish together (the
+// last CTA to finish rearms the counter); without one each CTA takes a
+// contiguous range. In each CTA a producer warp streams its units into a ring
+// of shared-memory stages with
 // bulk (TMA) copies -- one per page span or head block -- that complete on the
 // stage's mbarrier; eight consumer warps wait on it, compute, and release the
 // stage through a second mbarrier, so copies run ahead by the ring depth with
-// no CTA-wide barrier per unit. Each consumer warp reads 4 consecutive
+// no CTA-wide barrier per unit; each stage carries its unit number, and a
+// stage marked -1 ends the consumers. Each consumer warp reads 4 consecutive
 // 512-byte pieces of a unit: C/8 lanes hold one C-wide row, every lane keeps
 // the same (head, channel chunk) for the whole unit, its slice of the summed
 // query sits in registers, packed fp32 FMAs form the partial dot products, and
@@ -38,6 +43,7 @@ constexpr int kScoreThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kUnitBytes = 16384;                     // 32 pieces of 512 B
 constexpr int kMaxStages = 12;
 constexpr uint32_t kWaitLimit = 1u << 22;             // bounded mbarrier polls
+constexpr int kChunkUnits = 4;                        // units a CTA takes per dynamic fetch
 
 struct ScoreParams {
   const uint16_t* qp;
@@ -47,6 +53,7 @@ struct ScoreParams {
   float* scores;
   unsigned* err;
   int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb;
+  unsigned* work;   // [2]: next unit, finished CTAs (zero between calls); null: static unit ranges
   int units;        // B * nhb * upb (< 2^31, checked on the host)
   int upb;          // units per (request, head block)
   int nst;          // ring stages
@@ -75,6 +82,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
   unsigned char* ring = smem;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ int stage_unit[kMaxStages];   // unit held by each ring stage, -1: no more units
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -91,16 +99,40 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
   }
   __syncthreads();
   grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
-    int bh = u0 / p.upb;
-    int ui = u0 - bh * p.upb;
     int s = 0;
     uint32_t fill = 0;  // how many times stage s has been filled before
-    for (int u = u0; u < u1; ++u) {
+    int su = u0;        // static cursor
+    int cu = 0, ce = 0; // dynamic chunk [cu, ce)
+    for (;;) {
+      int unit = -1;
+      if (p.work) {
+        if (cu >= ce) {
+          int base = 0;
+          if (lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(kChunkUnits)));
+          base = __shfl_sync(kFull, base, 0);
+          cu = base;
+          ce = base < p.units ? min(p.units, base + kChunkUnits) : base;
+        }
+        if (cu < ce) unit = cu++;
+      } else if (su < u1) {
+        unit = su++;
+      }
       if (fill > 0 && !mbar_wait(&empty_bar[s], (fill - 1) & 1u, kWaitLimit) && lane == 0)
         flag_error(p.err, 8u);
+      if (unit < 0) {
+        // No more units: a stage marked -1 (plain arrive, no bytes) stops the consumers.
+        if (lane == 0) {
+          stage_unit[s] = -1;
+          mbar_arrive(&full_bar[s]);
+        }
+        break;
+      }
+      const int bh = unit / p.upb;
+      const int ui = unit - bh * p.upb;
       const int b = (p.nhb == 1) ? bh : bh / p.nhb;
       const int hb = bh - b * p.nhb;
       const int T = clamp_len(p, b);
@@ -143,16 +175,15 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
       uint32_t total = nbytes;
 #pragma unroll
       for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], total);
+      if (lane == 0) {
+        stage_unit[s] = unit;
+        mbar_arrive_expect_tx(&full_bar[s], total);
+      }
       __syncwarp();
       if (nbytes) bulk_g2s(dst + dst_off, src, nbytes, &full_bar[s]);
       if (++s == p.nst) {
         s = 0;
         ++fill;
-      }
-      if (++ui == p.upb) {
-        ui = 0;
-        ++bh;
       }
     }
   } else {
@@ -166,13 +197,15 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
     int b = 0, T = 0, hl = 0;
     float2 q[NGR][4];
 
-    int bh = u0 / p.upb;
-    int ui = u0 - bh * p.upb;
     int s = 0;
     uint32_t fill = 0;
-    for (int u = u0; u < u1; ++u) {
+    for (;;) {
       const bool ok = mbar_wait(&full_bar[s], fill & 1u, kWaitLimit);
       if (!ok && lane == 0) flag_error(p.err, 8u);
+      const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
+      if (unit < 0) break;
+      const int bh = unit / p.upb;
+      const int ui = unit - bh * p.upb;
       if (bh != cur) {
         cur = bh;
         b = (p.nhb == 1) ? bh : bh / p.nhb;
@@ -237,13 +270,18 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
         s = 0;
         ++fill;
       }
-      if (++ui == p.upb) {
-        ui = 0;
-        ++bh;
-      }
     }
   }
   __syncthreads();
+  if (p.work && tid == 0) {
+    // Every unit has been handed out; the last CTA to finish rearms the
+    // counters for the next call.
+    __threadfence();
+    if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.work, 0u);
+      atomicExch(p.work + 1, 0u);
+    }
+  }
 }
 
 using KernelFn = void (*)(const ScoreParams);
@@ -340,6 +378,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.num_pages = a.num_pages;
   p.Tmax = a.Tmax;
   p.nhb = nhb;
+  p.work = a.work;
   const long long upb = (static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu;
   const long long units = static_cast<long long>(a.B) * nhb * upb;
   if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;

@@ -36,6 +36,7 @@ constexpr int kPer = 16;                      // scores per thread per pass
 constexpr int kBatch = kThreads * kPer;       // scores per CTA pass
 constexpr int kListCap = 4096;                // kept (key, token) pairs in shared memory
 constexpr int kMaxCluster = 16;
+constexpr int kPtCap = 1040;                  // page-table entries of a slice kept in shared memory
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -46,6 +47,15 @@ struct TopkParams {
   unsigned* err;
   uint2* list;     // [R, Tmax] overflow lists
   int Hkv, Tmax, lim, k;
+  // Chained call only (slots == nullptr otherwise): the physical slot of each
+  // kept token, and an L2 prefetch of its K and V rows for the attention.
+  const int32_t* page_table;
+  int32_t* slots;  // [R, k]
+  const uint8_t* kc;
+  const uint8_t* vc;
+  long long slot_stride;   // bytes per slot (Hkv rows)
+  int rowb, maxp, num_pages;
+  int pre_wait;    // inputs may be read before the previous kernel completes
 };
 
 struct __align__(16) Smem {
@@ -58,6 +68,7 @@ struct __align__(16) Smem {
   unsigned long long scan[33];
   unsigned cnt[2];       // this CTA's keys above the threshold, equal to it
   unsigned res[4];
+  int pt[kPtCap];        // page-table entries of this CTA's slice (chained call)
   uint2 list[kListCap];
 };
 constexpr int kZeroWords = 4 * kBins1 + 2 * kBins3;   // h1 .. t3
@@ -151,6 +162,30 @@ __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
   return T;
 }
 
+// Writes kept token t at output position pos; in the chained call also its
+// physical slot, and prefetches its K and V rows into L2.
+__device__ __forceinline__ void emit(const TopkParams& p, const Smem& S, int row, int b, int g, int pg0, int npg,
+                                     int pos, int t) {
+  p.idx[static_cast<size_t>(row) * p.k + pos] = t;
+  if (!p.slots) return;
+  const int pg = t >> 6;
+  const int pid = (npg <= kPtCap && pg - pg0 < npg) ? S.pt[pg - pg0]
+                                                     : __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg);
+  int slot = -1;
+  if (pid < 0 || pid >= p.num_pages) {
+    flag_error(p.err, 2u);
+  } else {
+    slot = pid * kPage + (t & (kPage - 1));
+    const long long off = static_cast<long long>(slot) * p.slot_stride + static_cast<long long>(g) * p.rowb;
+    const uintptr_t k0 = reinterpret_cast<uintptr_t>(p.kc + off), v0 = reinterpret_cast<uintptr_t>(p.vc + off);
+    for (uintptr_t a = k0 & ~static_cast<uintptr_t>(127); a < k0 + p.rowb; a += 128)
+      prefetch_l2(reinterpret_cast<const void*>(a));
+    for (uintptr_t a = v0 & ~static_cast<uintptr_t>(127); a < v0 + p.rowb; a += 128)
+      prefetch_l2(reinterpret_cast<const void*>(a));
+  }
+  p.slots[static_cast<size_t>(row) * p.k + pos] = slot;
+}
+
 __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkParams p) {
   extern __shared__ __align__(16) unsigned char dsm[];
   Smem& S = *reinterpret_cast<Smem*>(dsm);
@@ -162,25 +197,42 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
     uint4* z = reinterpret_cast<uint4*>(S.h1);
     for (int i = tid; i < kZeroWords / 4; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-  grid_dependency_wait();
   const int b = row / p.Hkv;
-  const int T = row_len(p, b, q == 0 && tid == 0 && row % p.Hkv == 0);
+  const int g = row - b * p.Hkv;
+  int T = 0, s0 = 0, s1 = 0, pg0 = 0, npg = 0;
+  // This CTA's token slice and, in the chained call, its page-table entries.
+  auto setup = [&]() {
+    T = row_len(p, b, q == 0 && tid == 0 && g == 0);
+    const int SL = ((T + static_cast<int>(cs) - 1) / static_cast<int>(cs) + 15) & ~15;
+    s0 = min(T, static_cast<int>(q) * SL);
+    s1 = min(T, s0 + SL);
+    if (p.slots && s1 > s0) {
+      pg0 = s0 >> 6;
+      npg = ((s1 - 1) >> 6) - pg0 + 1;
+      if (npg <= kPtCap)
+        for (int i = tid; i < npg; i += kThreads) S.pt[i] = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg0 + i);
+    }
+  };
+  if (p.pre_wait) setup();
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (!p.pre_wait) setup();
+  __syncthreads();
   int32_t* out = p.idx + static_cast<size_t>(row) * p.k;
   const int keff = min(p.k, T);
   if (!needs_selection(p.k, T)) {
     // The whole cluster takes this branch (same row): no shared memory is
-    // exchanged, so CTAs leave independently.
-    for (int i = static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads)
-      out[i] = (i < keff) ? i : -1;
+    // exchanged, so CTAs leave independently. Every token is kept.
+    for (int t = s0 + tid; t < min(s1, p.k); t += kThreads) emit(p, S, row, b, g, pg0, npg, t, t);
+    for (int i = keff + static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads) {
+      out[i] = -1;
+      if (p.slots) p.slots[static_cast<size_t>(row) * p.k + i] = -1;
+    }
     return;
   }
   cluster_arrive();   // this CTA's totals are zero: owners may receive adds
 
   // ---- digit 1 (key bits 21..31) over the slice
-  const int SL = ((T + static_cast<int>(cs) - 1) / static_cast<int>(cs) + 15) & ~15;
-  const int s0 = min(T, static_cast<int>(q) * SL);
-  const int s1 = min(T, s0 + SL);
   const int nb = (s1 - s0 + kBatch - 1) / kBatch;
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
   uint32_t keys[kPer];
@@ -336,57 +388,50 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
       ++eqr;
     }
     if (keep) {
-      if (pos < static_cast<unsigned>(p.k)) out[pos] = static_cast<int32_t>(v.y);
+      if (pos < static_cast<unsigned>(p.k)) emit(p, S, row, b, g, pg0, npg, static_cast<int>(pos), static_cast<int>(v.y));
       ++pos;
     }
   }
-  for (int i = keff + static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads) out[i] = -1;
+  for (int i = keff + static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads) {
+    out[i] = -1;
+    if (p.slots) p.slots[static_cast<size_t>(row) * p.k + i] = -1;
+  }
   cluster_wait();   // keep this CTA's shared memory until every CTA is done with it
 }
 
-struct LaunchCache {
-  bool init = false;
-  int max_cs = 8;
-};
-
-// Largest cluster the device can schedule with this kernel's footprint.
-cudaError_t prepare(int smem, int* max_cs) {
-  static LaunchCache cache[64];
+// Clusters of `cs` top-k CTAs the current device keeps resident at once
+// (cached per device; 0 if unknown). Also sets the kernel's attributes.
+int resident_clusters(int cs, int smem) {
+  static int cache[64][5] = {};
+  static bool attr_done[64] = {};
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  LaunchCache* c = (dev >= 0 && dev < 64) ? &cache[dev] : nullptr;
-  if (c && c->init) {
-    *max_cs = c->max_cs;
-    return cudaSuccess;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return 0;
+    if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      cudaGetLastError();
+    attr_done[dev] = true;
   }
-  e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int best = 8;
-  if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMaxCluster);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kMaxCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel, &cfg) == cudaSuccess && n > 0) best = kMaxCluster;
-    cudaGetLastError();
-  } else {
-    cudaGetLastError();
-  }
-  if (c) {
-    c->max_cs = best;
-    c->init = true;
-  }
-  *max_cs = best;
-  return cudaSuccess;
+  const int ci = cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : cs == 8 ? 3 : 4;
+  int& c = cache[dev][ci];
+  if (c) return c > 0 ? c : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel, &cfg) != cudaSuccess || n < 0) n = 0;
+  cudaGetLastError();
+  c = n > 0 ? n : -1;
+  return n;
 }
 
 }  // namespace
@@ -412,13 +457,28 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.Tmax = a.Tmax;
   p.lim = a.maxp_tokens < a.Tmax ? a.maxp_tokens : a.Tmax;
   p.k = a.k;
+  p.page_table = a.page_table;
+  p.slots = a.slots;
+  p.kc = static_cast<const uint8_t*>(a.k_cache);
+  p.vc = static_cast<const uint8_t*>(a.v_cache);
+  p.rowb = a.row_bytes;
+  p.slot_stride = static_cast<long long>(a.Hkv) * a.row_bytes;
+  p.maxp = a.maxp;
+  p.num_pages = a.num_pages;
+  p.pre_wait = a.pre_wait;
   const int smem = static_cast<int>(sizeof(Smem));
-  int max_cs = 8;
-  cudaError_t e = prepare(smem, &max_cs);
-  if (e != cudaSuccess) return e;
-  // One pass of kBatch scores per CTA where the cluster allows it.
+  // Cluster size: one pass of kBatch scores per CTA where possible, but no
+  // more CTAs than the device keeps resident at once (a second wave would
+  // double the latency-bound selection). The occupancy query assumes an empty
+  // GPU and ideal cluster placement; a quarter of headroom keeps the launch in
+  // one wave when clusters land on partly busy GPCs.
+  if (resident_clusters(1, smem) <= 0) return cudaErrorNotSupported;
   int cs = 1;
-  while (cs < max_cs && static_cast<long long>(cs) * kBatch < a.Tmax) cs *= 2;
+  while (cs < kMaxCluster && static_cast<long long>(cs) * kBatch < a.Tmax) {
+    const int n = resident_clusters(cs * 2, smem);
+    if (n <= 0 || 4LL * R > 3LL * n) break;
+    cs *= 2;
+  }
   if (static_cast<long long>(R) * cs > 0x7fffffffLL) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(R * cs));
@@ -434,7 +494,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
