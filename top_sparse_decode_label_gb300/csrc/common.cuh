@@ -168,6 +168,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 // Barrier over a subset of the CTA's warps (ids 1..15; `threads` a multiple of 32).
+// Tiled tensor copy (TMA) of the box at coordinates (x, y) of a 2-D tensor
+// map into shared memory, completing on `bar` with its byte count. x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tensor_g2s_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

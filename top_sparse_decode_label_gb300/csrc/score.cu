@@ -30,6 +30,9 @@
 // a transposed butterfly combines them across the row's lanes. Every mbarrier
 // wait is bounded: on timeout it sets DS_DEVERR_TIMEOUT and carries on.
 
+#include <cuda.h>
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,13 +49,14 @@ constexpr uint32_t kWaitLimit = 1u << 22;             // bounded mbarrier polls
 constexpr int kChunkUnits = 4;                        // units a CTA takes per dynamic fetch
 
 struct ScoreParams {
+  CUtensorMap tmap;   // tensor-core path: the key cache as [slots, 64] bf16 rows, 64 x 64 boxes, 128-byte swizzle
   const uint16_t* qp;
   const uint8_t* label;
   const int32_t* page_table;
   const int32_t* seq_lens;
   float* scores;
   unsigned* err;
-  int Hq, Hkv, HL, maxp, num_pages, Tmax, nhb;
+  int B, Hq, Hkv, HL, maxp, num_pages, Tmax, nhb;
   unsigned* work;   // [2]: next unit, finished CTAs (zero between calls); null: static unit ranges
   int units;        // B * nhb * upb (< 2^31, checked on the host)
   int upb;          // units per (request, head block)
@@ -67,8 +71,10 @@ __device__ __forceinline__ int clamp_len(const ScoreParams& p, int b) {
 
 // C: proxy width; NGR: groups fed by one label row (1 for a per-head label,
 // Hkv for a shared index key); TPI: tokens covered by one 512-byte piece.
-template <int C, int NGR, int TPI>
-__global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score_kernel(const ScoreParams p) {
+template <int C, int NGR, int TPI, bool MMA>
+__global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
+    index_score_kernel(const __grid_constant__ ScoreParams p) {
+  static_assert(!MMA || (C == 64 && TPI == 4), "tensor-core path: shared 64-wide keys");
   constexpr int LPR = C / 8;                             // lanes per C-wide row
   constexpr int RPI = 32 / LPR;                          // rows per 512-byte piece
   constexpr int HPB = RPI / TPI;                         // label heads per piece
@@ -79,7 +85,9 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
   constexpr int PER = V >= LPR ? V / LPR : 1;            // finished sums per lane
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;
+  // Ring of stages. The tensor-core path aligns it to 1024 bytes for the
+  // 128-byte swizzle of its tensor copies (its launch adds 1 KB for that).
+  unsigned char* ring = MMA ? smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u) : smem;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ int stage_unit[kMaxStages];   // unit held by each ring stage, -1: no more units
@@ -103,24 +111,84 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
+    // Units come in chunks of kChunkUnits consecutive units. The page ids of
+    // a chunk's pages are loaded together, one lane per page, one chunk
+    // before the chunk is copied, and dynamic chunk claims are also issued a
+    // chunk ahead, so no global round trip sits on the per-unit path; the
+    // ring of stages covers the one round trip per chunk that remains.
+    constexpr int PPU = TPU >= kPage ? TPU / kPage : 1;   // pages per unit
+    static_assert(PPU * kChunkUnits <= 32, "one lane per page of a chunk");
+    // Sequence lengths of up to 32 requests, one per lane (clamped).
+    const int Tl = lane < p.B ? clamp_len(p, lane) : 0;
+    auto seq_len = [&](int b) { return p.B <= 32 ? __shfl_sync(kFull, Tl, b & 31) : clamp_len(p, b); };
+    // Chunk ranges: static -- the CTA's own range [u0, u1) cut in chunks;
+    // dynamic -- each CTA's first chunk is fixed, later ones come from the
+    // counter (offset past the fixed ones).
+    int su = u0;
+    auto first_chunk = [&](int& a, int& e) {
+      if (p.work) {
+        a = blockIdx.x * kChunkUnits;
+        e = min(p.units, a + kChunkUnits);
+        if (a > e) a = e;
+      } else {
+        a = su;
+        e = min(u1, su + kChunkUnits);
+        su = e;
+      }
+    };
+    auto claim = [&]() -> int {   // dynamic: counter value (lane 0), resolved later
+      int base = 0;
+      if (p.work && lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(kChunkUnits)));
+      return base;
+    };
+    auto resolve = [&](int claimed, int& a, int& e) {
+      if (p.work) {
+        const long long base = static_cast<long long>(__shfl_sync(kFull, claimed, 0)) +
+                               static_cast<long long>(gridDim.x) * kChunkUnits;
+        a = static_cast<int>(base < p.units ? base : p.units);
+        e = min(p.units, a + kChunkUnits);
+      } else {
+        a = su;
+        e = min(u1, su + kChunkUnits);
+        su = e;
+      }
+    };
+    // Page id for lane l: page l % PPU of unit a + l / PPU (-1 past the sequence).
+    auto load_pids = [&](int a, int e) -> int {
+      const int u = a + lane / PPU;
+      const int bh = u / p.upb;
+      const int b = (p.nhb == 1) ? bh : bh / p.nhb;
+      const int T = seq_len(u < e ? b : 0);
+      int pid = -1;
+      if (u < e) {
+        const int pg = (((u - bh * p.upb) * TPU) >> 6) + lane % PPU;
+        if (pg * kPage < T) pid = __ldg(p.page_table + b * p.maxp + pg);
+      }
+      return pid;
+    };
+    int cu = 0, ce = 0, na = 0, ne = 0;
+    first_chunk(cu, ce);
+    int claimed = claim();
+    int cpid = load_pids(cu, ce);
+    resolve(claimed, na, ne);
+    int npid = load_pids(na, ne);
+    int ca = cu;          // first unit of the current chunk
+    claimed = claim();    // the chunk after next
     int s = 0;
     uint32_t fill = 0;  // how many times stage s has been filled before
-    int su = u0;        // static cursor
-    int cu = 0, ce = 0; // dynamic chunk [cu, ce)
     for (;;) {
-      int unit = -1;
-      if (p.work) {
-        if (cu >= ce) {
-          int base = 0;
-          if (lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(kChunkUnits)));
-          base = __shfl_sync(kFull, base, 0);
-          cu = base;
-          ce = base < p.units ? min(p.units, base + kChunkUnits) : base;
-        }
-        if (cu < ce) unit = cu++;
-      } else if (su < u1) {
-        unit = su++;
+      if (cu >= ce && na < ne) {
+        // Next chunk: its page ids were loaded a chunk ago; start loading the
+        // one after it, and claim another.
+        cu = na;
+        ce = ne;
+        ca = cu;
+        cpid = npid;
+        resolve(claimed, na, ne);
+        npid = load_pids(na, ne);
+        claimed = claim();
       }
+      const int unit = cu < ce ? cu++ : -1;
       if (fill > 0 && !mbar_wait(&empty_bar[s], (fill - 1) & 1u, kWaitLimit) && lane == 0)
         flag_error(p.err, 8u);
       if (unit < 0) {
@@ -135,21 +203,48 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
       const int ui = unit - bh * p.upb;
       const int b = (p.nhb == 1) ? bh : bh / p.nhb;
       const int hb = bh - b * p.nhb;
-      const int T = clamp_len(p, b);
+      const int T = seq_len(b);
       const int t0 = ui * TPU;
       const int t1 = min(T, t0 + TPU);
-      const int* pt = p.page_table + b * p.maxp;
+      const int pbase = (unit - ca) * PPU;   // lane of this unit's first page id
       unsigned char* dst = ring + s * kUnitBytes;
       uint32_t nbytes = 0;
       const uint8_t* src = p.label;
       int dst_off = 0;
-      if (p.nhb == 1) {
+      if constexpr (MMA) {
+        // Tensor copies: one 64-token page (64 x 64 bf16, 8 KB) per lane,
+        // swizzled into the stage for conflict-free ldmatrix reads.
+        const int pid = __shfl_sync(kFull, cpid, (pbase + lane) & 31);
+        const int pg = (t0 >> 6) + lane;
+        if (lane < PPU && pg * kPage < t1) {
+          if (pid >= 0 && pid < p.num_pages) {
+            nbytes = 8192u;
+            dst_off = lane * 8192;
+          } else {
+            flag_error(p.err, 2u);
+          }
+        }
+        uint32_t total = nbytes;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+        if (lane == 0) {
+          stage_unit[s] = unit;
+          mbar_arrive_expect_tx(&full_bar[s], total);
+        }
+        __syncwarp();
+        if (nbytes) tensor_g2s_2d(dst + dst_off, &p.tmap, 0, pid * kPage, &full_bar[s]);
+        if (++s == p.nst) {
+          s = 0;
+          ++fill;
+        }
+        continue;
+      } else if (p.nhb == 1) {
         // Whole token rows: one contiguous span per page of the unit.
+        const int pid = __shfl_sync(kFull, cpid, (pbase + lane) & 31);
         const int pg = (t0 >> 6) + lane;
         const int ts = max(t0, pg * kPage);
         const int te = min(t1, pg * kPage + kPage);
-        if (ts < te) {
-          const int pid = __ldg(pt + pg);
+        if (lane < PPU && ts < te) {
           if (pid >= 0 && pid < p.num_pages) {
             nbytes = static_cast<uint32_t>(te - ts) * BR;
             src = p.label + static_cast<long long>(pid * kPage + (ts & (kPage - 1))) * BR;
@@ -159,10 +254,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
           }
         }
       } else {
-        // One 512-byte block of heads per token (TPU == 32 tokens, one per lane).
+        // One 512-byte block of heads per token (TPU == 32 tokens, one per
+        // lane, all in one page).
+        const int pid = __shfl_sync(kFull, cpid, pbase & 31);
         const int t = t0 + lane;
         if (lane < TPU && t < t1) {
-          const int pid = __ldg(pt + (t >> 6));
           if (pid >= 0 && pid < p.num_pages) {
             nbytes = BR;
             src = p.label + (static_cast<long long>(pid * kPage + (t & (kPage - 1))) * p.HL + hb * HPB) * (C * 2);
@@ -188,6 +284,103 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
     }
   } else {
     // ------------------------------------------------------------ consumer warps
+    if constexpr (MMA) {
+      // Tensor cores: warp w takes tokens [16w, 16w + 16) of each 128-token
+      // unit and forms D[16 tokens x 8] = K_tile[16 x 64] . B[64 x 8] with
+      // mma.sync m16n8k16 (bf16 in, fp32 accumulate). Column 2g of B holds
+      // the group-g query summed over its heads, rounded to bf16 (hi);
+      // column 2g + 1 the bf16 rounding of the remainder (lo), so hi + lo
+      // carries the fp32 sum to about 2^-16 relative and integer-valued sums
+      // exactly; the score of group g is D[., 2g] + D[., 2g + 1].
+      constexpr int NT = (2 * NGR + 7) / 8;   // n8 tiles
+      const int gr = lane >> 2, qc = lane & 3;
+      const int G = p.Hq / p.Hkv;
+      uint32_t qb[NT][4][2];
+      int cur = -1, b = 0, T = 0;
+      int s = 0;
+      uint32_t fill = 0;
+      for (;;) {
+        const bool ok = mbar_wait(&full_bar[s], fill & 1u, kWaitLimit);
+        if (!ok && lane == 0) flag_error(p.err, 8u);
+        const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
+        if (unit < 0) break;
+        const int bh = unit / p.upb;
+        const int ui = unit - bh * p.upb;
+        if (bh != cur) {
+          cur = bh;
+          b = bh;
+          T = clamp_len(p, b);
+          if (tid == 0 && ui == 0) {
+            const int raw = __ldg(p.seq_lens + b);
+            if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + gr;   // this lane's B column
+            const int g = n >> 1;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              float qs[4] = {0.f, 0.f, 0.f, 0.f};   // channels 16ks + 2qc, +1, +8, +9
+              if (g < NGR) {
+                for (int h = g * G; h < (g + 1) * G; ++h) {
+                  const uint16_t* qrow = p.qp + (static_cast<long long>(b) * p.Hq + h) * C + 16 * ks + 2 * qc;
+                  const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t*>(qrow));
+                  const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t*>(qrow + 8));
+                  qs[0] += bf16_lo(w0);
+                  qs[1] += bf16_hi(w0);
+                  qs[2] += bf16_lo(w1);
+                  qs[3] += bf16_hi(w1);
+                }
+              }
+              uint16_t part[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(qs[i]);
+                const __nv_bfloat16 v = (n & 1) ? __float2bfloat16_rn(qs[i] - __bfloat162float(hi)) : hi;
+                part[i] = __bfloat16_as_ushort(v);
+              }
+              qb[nt][ks][0] = static_cast<uint32_t>(part[0]) | (static_cast<uint32_t>(part[1]) << 16);
+              qb[nt][ks][1] = static_cast<uint32_t>(part[2]) | (static_cast<uint32_t>(part[3]) << 16);
+            }
+          }
+        }
+        const int tw = ui * TPU + 16 * warp;   // this warp's first token
+        if (ok && tw < T) {
+          const int row0 = (16 * warp) & (kPage - 1);
+          const uint32_t tile = smem_u32(ring + s * kUnitBytes + ((16 * warp) >> 6) * 8192);
+          const int r = row0 + (lane & 15);
+          float acc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const int chunk = 2 * ks + (lane >> 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(tile + r * 128 + ((chunk ^ (r & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+          }
+          const int t_lo = tw + gr, t_hi = tw + gr + 8;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 4 + qc;
+            if (g < NGR) {
+              float* srow = p.scores + (static_cast<long long>(b) * p.Hkv + g) * p.Tmax;
+              if (t_lo < T) srow[t_lo] = acc[nt][0] + acc[nt][1];
+              if (t_hi < T) srow[t_hi] = acc[nt][2] + acc[nt][3];
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (++s == p.nst) {
+          s = 0;
+          ++fill;
+        }
+      }
+    } else {
     const int chunk = lane % LPR;
     const int rin = lane / LPR;
     const int tok_off = rin / HPB;
@@ -271,6 +464,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8) ? 1 : 2) index_score
         ++fill;
       }
     }
+    }
   }
   __syncthreads();
   if (p.work && tid == 0) {
@@ -290,26 +484,38 @@ template <int C, int NGR>
 KernelFn pick_tpi(int tpi) {
   constexpr int RPI = 256 / C;
   switch (tpi) {
-    case 1: return index_score_kernel<C, NGR, 1>;
-    case 2: if constexpr (RPI >= 2) return index_score_kernel<C, NGR, 2>; break;
-    case 4: if constexpr (RPI >= 4) return index_score_kernel<C, NGR, 4>; break;
-    case 8: if constexpr (RPI >= 8) return index_score_kernel<C, NGR, 8>; break;
-    case 16: if constexpr (RPI >= 16) return index_score_kernel<C, NGR, 16>; break;
+    case 1: return index_score_kernel<C, NGR, 1, false>;
+    case 2: if constexpr (RPI >= 2) return index_score_kernel<C, NGR, 2, false>; break;
+    case 4: if constexpr (RPI >= 4) return index_score_kernel<C, NGR, 4, false>; break;
+    case 8: if constexpr (RPI >= 8) return index_score_kernel<C, NGR, 8, false>; break;
+    case 16: if constexpr (RPI >= 16) return index_score_kernel<C, NGR, 16, false>; break;
   }
   return nullptr;
 }
 
 template <int C>
-KernelFn pick(int HL, int Hkv, int* tpi_out) {
+KernelFn pick(int HL, int Hkv, int* tpi_out, bool* mma) {
   constexpr int RPI = 256 / C;
+  *mma = false;
   if (HL == 1) {
     // Shared key (or a single KV head): one row per token, feeds every group.
+    // 64-wide keys: the tensor-core path.
     *tpi_out = RPI;
+    if constexpr (C == 64) {
+      *mma = true;
+      switch (Hkv) {
+        case 1: return index_score_kernel<C, 1, RPI, true>;
+        case 2: return index_score_kernel<C, 2, RPI, true>;
+        case 4: return index_score_kernel<C, 4, RPI, true>;
+        case 8: return index_score_kernel<C, 8, RPI, true>;
+      }
+      return nullptr;
+    }
     switch (Hkv) {
-      case 1: return index_score_kernel<C, 1, RPI>;
-      case 2: return index_score_kernel<C, 2, RPI>;
-      case 4: return index_score_kernel<C, 4, RPI>;
-      case 8: return index_score_kernel<C, 8, RPI>;
+      case 1: return index_score_kernel<C, 1, RPI, false>;
+      case 2: return index_score_kernel<C, 2, RPI, false>;
+      case 4: return index_score_kernel<C, 4, RPI, false>;
+      case 8: return index_score_kernel<C, 8, RPI, false>;
     }
     return nullptr;
   }
@@ -325,13 +531,38 @@ KernelFn pick(int HL, int Hkv, int* tpi_out) {
   return pick_tpi<C, 1>(1);
 }
 
-KernelFn select_kernel(int C, int HL, int Hkv, int* tpi) {
+KernelFn select_kernel(int C, int HL, int Hkv, int* tpi, bool* mma) {
   switch (C) {
-    case 16: return pick<16>(HL, Hkv, tpi);
-    case 32: return pick<32>(HL, Hkv, tpi);
-    case 64: return pick<64>(HL, Hkv, tpi);
+    case 16: return pick<16>(HL, Hkv, tpi, mma);
+    case 32: return pick<32>(HL, Hkv, tpi, mma);
+    case 64: return pick<64>(HL, Hkv, tpi, mma);
   }
   return nullptr;
+}
+
+// Tensor map of a shared 64-wide bf16 key cache: rows = slots, 64 x 64 boxes
+// (one page), 128-byte swizzle. The encoder is the driver's, fetched once.
+cudaError_t key_tensor_map(CUtensorMap* map, const void* keys, long long slots) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return cudaErrorNotSupported;
+    encode = reinterpret_cast<Encode>(fn);
+  }
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(slots)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(keys), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // Sets the dynamic shared memory limit of a kernel once per (kernel, size) per device.
@@ -353,12 +584,14 @@ cudaError_t allow_smem(KernelFn fn, int bytes) {
 bool index_score_supported(int C, int HL, int Hkv, int G) {
   (void)G;
   int tpi = 0;
-  return select_kernel(C, HL, Hkv, &tpi) != nullptr;
+  bool mma = false;
+  return select_kernel(C, HL, Hkv, &tpi, &mma) != nullptr;
 }
 
 cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   int tpi = 0;
-  KernelFn fn = select_kernel(a.C, a.HL, a.Hkv, &tpi);
+  bool mma = false;
+  KernelFn fn = select_kernel(a.C, a.HL, a.Hkv, &tpi, &mma);
   if (!fn) return cudaErrorNotSupported;
   if (a.B == 0 || a.Tmax == 0) return cudaSuccess;
   const int rpi = 256 / a.C;
@@ -371,6 +604,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.scores = a.scores;
   p.err = a.err;
+  p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.HL = a.HL;
@@ -384,9 +618,14 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;
   p.upb = static_cast<int>(upb);
   p.units = static_cast<int>(units);
-  // Two CTAs per SM, each with a ring of 7 x 16 KB stages.
-  p.nst = 7;
-  const int smem = p.nst * kUnitBytes;
+  if (mma) {
+    const cudaError_t te = key_tensor_map(&p.tmap, a.label, static_cast<long long>(a.num_pages) * kPage);
+    if (te != cudaSuccess) return te;
+  }
+  // Two CTAs per SM, each with a ring of 7 x 16 KB stages (6 on the
+  // tensor-core path, which aligns the ring to 1024 bytes).
+  p.nst = mma ? 6 : 7;
+  const int smem = p.nst * kUnitBytes + (mma ? 1024 : 0);
   cudaError_t e = allow_smem(fn, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
