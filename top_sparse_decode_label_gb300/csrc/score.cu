@@ -10,25 +10,32 @@
 // lane first adds its group's proxy queries (fp32) and then needs one dot
 // product per (token, group).
 //
-// HBM-bound scan. The label cache is cut into 16 KB units: consecutive tokens
-// of one request, either whole token rows (HL*C*2 bytes <= 512) or one
-// 512-byte block of heads of each token (per-head label with many heads). A
-// persistent grid takes the units in request order: with a work counter
-// (chained call) each CTA's producer claims 4 units at a time with one
-// atomicAdd, so faster CTAs take more work and all CTAs finish together (the
-// last CTA to finish rearms the counter); without one each CTA takes a
-// contiguous range. In each CTA a producer warp streams its units into a ring
-// of shared-memory stages with
-// bulk (TMA) copies -- one per page span or head block -- that complete on the
-// stage's mbarrier; eight consumer warps wait on it, compute, and release the
-// stage through a second mbarrier, so copies run ahead by the ring depth with
-// no CTA-wide barrier per unit; each stage carries its unit number, and a
-// stage marked -1 ends the consumers. Each consumer warp reads 4 consecutive
-// 512-byte pieces of a unit: C/8 lanes hold one C-wide row, every lane keeps
-// the same (head, channel chunk) for the whole unit, its slice of the summed
-// query sits in registers, packed fp32 FMAs form the partial dot products, and
-// a transposed butterfly combines them across the row's lanes. Every mbarrier
-// wait is bounded: on timeout it sets DS_DEVERR_TIMEOUT and carries on.
+// HBM-bound scan. The label cache is cut into 16 KB units of whole token
+// rows (HL*C*2 bytes each) of one request. A persistent grid takes the units
+// in chunks of consecutive units: with a work counter (chained call) each
+// CTA's first chunk is fixed and later ones are claimed with one atomicAdd, a
+// chunk ahead, so faster CTAs take more work and all CTAs finish together
+// (the last CTA to finish rearms the counter); without one each CTA takes a
+// contiguous range. In each CTA a producer warp loads the page ids of a
+// chunk's pages together, a chunk before they are needed, and streams the
+// units into a ring of shared-memory stages with bulk copies -- one per page
+// span -- that complete on the stage's mbarrier; eight consumer warps wait on
+// it, compute, and release the stage through a second mbarrier, so copies run
+// ahead by the ring depth with no CTA-wide barrier per unit; each stage
+// carries its unit number, and a stage marked -1 ends the consumers.
+//
+// CUDA-core consumers: each warp reads 4 consecutive 512-byte pieces of a
+// unit; C/8 lanes hold one C-wide row (one head of one token), every lane
+// keeps the same (head block, channel chunk) for the whole unit, its slices of
+// the summed queries sit in registers, packed fp32 FMAs form the partial dot
+// products, and a transposed butterfly combines them across the row's lanes.
+//
+// Tensor-core consumers (shared 64-wide index keys): the producer copies
+// whole 64-token pages with tiled tensor copies that swizzle 16-byte chunks
+// by row, each consumer warp forms the scores of 16 tokens for every group
+// with ldmatrix and mma.sync (bf16 in, fp32 accumulate) against the group
+// queries held in registers. Every mbarrier wait is bounded: on timeout it
+// sets DS_DEVERR_TIMEOUT and carries on.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -56,10 +63,10 @@ struct ScoreParams {
   const int32_t* seq_lens;
   float* scores;
   unsigned* err;
-  int B, Hq, Hkv, HL, maxp, num_pages, Tmax, nhb;
+  int B, Hq, Hkv, HL, maxp, num_pages, Tmax;
   unsigned* work;   // [2]: next unit, finished CTAs (zero between calls); null: static unit ranges
-  int units;        // B * nhb * upb (< 2^31, checked on the host)
-  int upb;          // units per (request, head block)
+  int units;        // B * upb (< 2^31, checked on the host)
+  int upb;          // units per request
   int nst;          // ring stages
 };
 
@@ -71,18 +78,20 @@ __device__ __forceinline__ int clamp_len(const ScoreParams& p, int b) {
 
 // C: proxy width; NGR: groups fed by one label row (1 for a per-head label,
 // Hkv for a shared index key); TPI: tokens covered by one 512-byte piece.
-template <int C, int NGR, int TPI, bool MMA>
+template <int C, int NGR, int TPI, int PPT, bool MMA>
 __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
     index_score_kernel(const __grid_constant__ ScoreParams p) {
-  static_assert(!MMA || (C == 64 && TPI == 4), "tensor-core path: shared 64-wide keys");
+  static_assert(!MMA || (C == 64 && TPI == 4 && PPT == 1), "tensor-core path: shared 64-wide keys");
+  static_assert(PPT == 1 || (TPI == 1 && NGR == 1), "several pieces per token only for a per-head label");
   constexpr int LPR = C / 8;                             // lanes per C-wide row
   constexpr int RPI = 32 / LPR;                          // rows per 512-byte piece
   constexpr int HPB = RPI / TPI;                         // label heads per piece
-  constexpr int BR = 512 / TPI;                          // bytes of one token's block
+  constexpr int BR = 512 * PPT / TPI;                    // bytes of one token's label row
   constexpr int TPU = kUnitBytes / BR;                   // tokens per unit
   constexpr int U = kUnitBytes / 512 / kConsumerWarps;   // pieces per consumer warp per unit (4)
   constexpr int V = U * NGR;                             // partial sums per lane
   constexpr int PER = V >= LPR ? V / LPR : 1;            // finished sums per lane
+  constexpr int NQ = NGR > 1 ? NGR : (PPT < U ? PPT : U);  // query register sets per lane
 
   extern __shared__ __align__(128) unsigned char smem[];
   // Ring of stages. The tensor-core path aligns it to 1024 bytes for the
@@ -156,12 +165,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
     // Page id for lane l: page l % PPU of unit a + l / PPU (-1 past the sequence).
     auto load_pids = [&](int a, int e) -> int {
       const int u = a + lane / PPU;
-      const int bh = u / p.upb;
-      const int b = (p.nhb == 1) ? bh : bh / p.nhb;
+      const int b = u / p.upb;
       const int T = seq_len(u < e ? b : 0);
       int pid = -1;
       if (u < e) {
-        const int pg = (((u - bh * p.upb) * TPU) >> 6) + lane % PPU;
+        const int pg = (((u - b * p.upb) * TPU) >> 6) + lane % PPU;
         if (pg * kPage < T) pid = __ldg(p.page_table + b * p.maxp + pg);
       }
       return pid;
@@ -199,10 +207,8 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         }
         break;
       }
-      const int bh = unit / p.upb;
-      const int ui = unit - bh * p.upb;
-      const int b = (p.nhb == 1) ? bh : bh / p.nhb;
-      const int hb = bh - b * p.nhb;
+      const int b = unit / p.upb;
+      const int ui = unit - b * p.upb;
       const int T = seq_len(b);
       const int t0 = ui * TPU;
       const int t1 = min(T, t0 + TPU);
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
           ++fill;
         }
         continue;
-      } else if (p.nhb == 1) {
+      } else {
         // Whole token rows: one contiguous span per page of the unit.
         const int pid = __shfl_sync(kFull, cpid, (pbase + lane) & 31);
         const int pg = (t0 >> 6) + lane;
@@ -249,20 +255,6 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
             nbytes = static_cast<uint32_t>(te - ts) * BR;
             src = p.label + static_cast<long long>(pid * kPage + (ts & (kPage - 1))) * BR;
             dst_off = (ts - t0) * BR;
-          } else {
-            flag_error(p.err, 2u);
-          }
-        }
-      } else {
-        // One 512-byte block of heads per token (TPU == 32 tokens, one per
-        // lane, all in one page).
-        const int pid = __shfl_sync(kFull, cpid, pbase & 31);
-        const int t = t0 + lane;
-        if (lane < TPU && t < t1) {
-          if (pid >= 0 && pid < p.num_pages) {
-            nbytes = BR;
-            src = p.label + (static_cast<long long>(pid * kPage + (t & (kPage - 1))) * p.HL + hb * HPB) * (C * 2);
-            dst_off = lane * BR;
           } else {
             flag_error(p.err, 2u);
           }
@@ -304,11 +296,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         if (!ok && lane == 0) flag_error(p.err, 8u);
         const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
         if (unit < 0) break;
-        const int bh = unit / p.upb;
-        const int ui = unit - bh * p.upb;
-        if (bh != cur) {
-          cur = bh;
-          b = bh;
+        const int ub = unit / p.upb;
+        const int ui = unit - ub * p.upb;
+        if (ub != cur) {
+          cur = ub;
+          b = ub;
           T = clamp_len(p, b);
           if (tid == 0 && ui == 0) {
             const int raw = __ldg(p.seq_lens + b);
@@ -387,8 +379,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
     const int hin = rin % HPB;
     const int G = p.Hq / p.Hkv;
     int cur = -1;
-    int b = 0, T = 0, hl = 0;
-    float2 q[NGR][4];
+    int b = 0, T = 0;
+    float2 q[NQ][4];
+    // Label head of query set n (per-head label): piece warp * U + n of a unit
+    // holds head block (warp * U + n) % PPT of its token.
+    auto head_of = [&](int n) { return ((warp * U + n) % PPT) * HPB + hin; };
 
     int s = 0;
     uint32_t fill = 0;
@@ -397,21 +392,19 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
       if (!ok && lane == 0) flag_error(p.err, 8u);
       const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
       if (unit < 0) break;
-      const int bh = unit / p.upb;
-      const int ui = unit - bh * p.upb;
-      if (bh != cur) {
-        cur = bh;
-        b = (p.nhb == 1) ? bh : bh / p.nhb;
-        const int hb = bh - b * p.nhb;
-        hl = hb * HPB + hin;
+      const int ub = unit / p.upb;
+      const int ui = unit - ub * p.upb;
+      if (ub != cur) {
+        cur = ub;
+        b = ub;
         T = clamp_len(p, b);
-        if (tid == 0 && hb == 0 && ui == 0) {
+        if (tid == 0 && ui == 0) {
           const int raw = __ldg(p.seq_lens + b);
           if (raw < 0 || raw > min(p.Tmax, p.maxp * kPage)) flag_error(p.err, 1u);
         }
 #pragma unroll
-        for (int n = 0; n < NGR; ++n) {
-          const int g = (NGR == 1) ? hl : n;
+        for (int n = 0; n < NQ; ++n) {
+          const int g = (NGR == 1) ? head_of(n) : n;
           float qs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           for (int h = g * G; h < (g + 1) * G; ++h) {
             const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.qp + (static_cast<long long>(b) * p.Hq + h) * C + chunk * 8));
@@ -438,10 +431,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
           const float2 x3 = make_float2(bf16_lo(x.w), bf16_hi(x.w));
 #pragma unroll
           for (int n = 0; n < NGR; ++n) {
-            float2 a = make_float2(q[n][0].x * x0.x, q[n][0].y * x0.y);
-            a = __ffma2_rn(q[n][1], x1, a);
-            a = __ffma2_rn(q[n][2], x2, a);
-            a = __ffma2_rn(q[n][3], x3, a);
+            const int qi = NGR > 1 ? n : uu % NQ;
+            float2 a = make_float2(q[qi][0].x * x0.x, q[qi][0].y * x0.y);
+            a = __ffma2_rn(q[qi][1], x1, a);
+            a = __ffma2_rn(q[qi][2], x2, a);
+            a = __ffma2_rn(q[qi][3], x3, a);
             acc[uu * NGR + n] = a.x + a.y;
           }
         }
@@ -452,8 +446,8 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
           const bool writer = (V >= LPR) || ((chunk * V) % LPR == 0);
           const int uu = v / NGR;
           const int n = v % NGR;
-          const int t = tbase + (warp * U + uu) * TPI + tok_off;
-          const int g = (NGR == 1) ? hl : n;
+          const int t = tbase + ((warp * U + uu) / PPT) * TPI + tok_off;
+          const int g = (NGR == 1) ? head_of(uu) : n;
           if (writer && t < T) p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = acc[kk];
         }
       }
@@ -484,11 +478,11 @@ template <int C, int NGR>
 KernelFn pick_tpi(int tpi) {
   constexpr int RPI = 256 / C;
   switch (tpi) {
-    case 1: return index_score_kernel<C, NGR, 1, false>;
-    case 2: if constexpr (RPI >= 2) return index_score_kernel<C, NGR, 2, false>; break;
-    case 4: if constexpr (RPI >= 4) return index_score_kernel<C, NGR, 4, false>; break;
-    case 8: if constexpr (RPI >= 8) return index_score_kernel<C, NGR, 8, false>; break;
-    case 16: if constexpr (RPI >= 16) return index_score_kernel<C, NGR, 16, false>; break;
+    case 1: return index_score_kernel<C, NGR, 1, 1, false>;
+    case 2: if constexpr (RPI >= 2) return index_score_kernel<C, NGR, 2, 1, false>; break;
+    case 4: if constexpr (RPI >= 4) return index_score_kernel<C, NGR, 4, 1, false>; break;
+    case 8: if constexpr (RPI >= 8) return index_score_kernel<C, NGR, 8, 1, false>; break;
+    case 16: if constexpr (RPI >= 16) return index_score_kernel<C, NGR, 16, 1, false>; break;
   }
   return nullptr;
 }
@@ -504,18 +498,18 @@ KernelFn pick(int HL, int Hkv, int* tpi_out, bool* mma) {
     if constexpr (C == 64) {
       *mma = true;
       switch (Hkv) {
-        case 1: return index_score_kernel<C, 1, RPI, true>;
-        case 2: return index_score_kernel<C, 2, RPI, true>;
-        case 4: return index_score_kernel<C, 4, RPI, true>;
-        case 8: return index_score_kernel<C, 8, RPI, true>;
+        case 1: return index_score_kernel<C, 1, RPI, 1, true>;
+        case 2: return index_score_kernel<C, 2, RPI, 1, true>;
+        case 4: return index_score_kernel<C, 4, RPI, 1, true>;
+        case 8: return index_score_kernel<C, 8, RPI, 1, true>;
       }
       return nullptr;
     }
     switch (Hkv) {
-      case 1: return index_score_kernel<C, 1, RPI, false>;
-      case 2: return index_score_kernel<C, 2, RPI, false>;
-      case 4: return index_score_kernel<C, 4, RPI, false>;
-      case 8: return index_score_kernel<C, 8, RPI, false>;
+      case 1: return index_score_kernel<C, 1, RPI, 1, false>;
+      case 2: return index_score_kernel<C, 2, RPI, 1, false>;
+      case 4: return index_score_kernel<C, 4, RPI, 1, false>;
+      case 8: return index_score_kernel<C, 8, RPI, 1, false>;
     }
     return nullptr;
   }
@@ -526,9 +520,16 @@ KernelFn pick(int HL, int Hkv, int* tpi_out, bool* mma) {
     *tpi_out = RPI / HL;
     return pick_tpi<C, 1>(RPI / HL);
   }
+  // Rows of several 512-byte pieces: PPT pieces (head blocks) per token.
   if (HL % RPI) return nullptr;
   *tpi_out = 1;
-  return pick_tpi<C, 1>(1);
+  switch (HL / RPI) {
+    case 1: return index_score_kernel<C, 1, 1, 1, false>;
+    case 2: return index_score_kernel<C, 1, 1, 2, false>;
+    case 4: return index_score_kernel<C, 1, 1, 4, false>;
+    case 8: return index_score_kernel<C, 1, 1, 8, false>;
+  }
+  return nullptr;
 }
 
 KernelFn select_kernel(int C, int HL, int Hkv, int* tpi, bool* mma) {
@@ -594,9 +595,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   KernelFn fn = select_kernel(a.C, a.HL, a.Hkv, &tpi, &mma);
   if (!fn) return cudaErrorNotSupported;
   if (a.B == 0 || a.Tmax == 0) return cudaSuccess;
-  const int rpi = 256 / a.C;
-  const int nhb = (a.HL > rpi) ? a.HL / rpi : 1;
-  const int tpu = kUnitBytes / (512 / tpi);
+  const int tpu = kUnitBytes / (a.HL * a.C * 2);   // whole token rows per unit
   ScoreParams p{};
   p.qp = static_cast<const uint16_t*>(a.qp);
   p.label = static_cast<const uint8_t*>(a.label);
@@ -611,10 +610,9 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.maxp = a.maxp;
   p.num_pages = a.num_pages;
   p.Tmax = a.Tmax;
-  p.nhb = nhb;
   p.work = a.work;
   const long long upb = (static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu;
-  const long long units = static_cast<long long>(a.B) * nhb * upb;
+  const long long units = static_cast<long long>(a.B) * upb;
   if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;
   p.upb = static_cast<int>(upb);
   p.units = static_cast<int>(units);
