@@ -235,12 +235,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
   // ---- digit 1 (key bits 21..31) over the slice
   const int nb = (s1 - s0 + kBatch - 1) / kBatch;
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
+  // Passes over the slice with the next pass's loads in flight.
   uint32_t keys[kPer];
+  if (nb > 0) load_keys(s, s0 + tid * kPer, s1, keys);
   for (int bt = 0; bt < nb; ++bt) {
     const int t0 = s0 + bt * kBatch + tid * kPer;
-    load_keys(s, t0, s1, keys);
+    uint32_t cur[kPer];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, keys[i] >> 21, t0 + i < s1);
+    for (int i = 0; i < kPer; ++i) cur[i] = keys[i];
+    if (bt + 1 < nb) load_keys(s, t0 + kBatch, s1, keys);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, cur[i] >> 21, t0 + i < s1);
   }
   __syncthreads();
   cluster_wait();
@@ -288,25 +293,29 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
   uint2* lst = (M <= static_cast<unsigned>(kListCap)) ? S.list : p.list + static_cast<size_t>(row) * p.Tmax + s0;
   {
     unsigned base = 0;
+    if (nb > 1) load_keys(s, s0 + tid * kPer, s1, keys);
     for (int bt = 0; bt < nb; ++bt) {
       const int t0 = s0 + bt * kBatch + tid * kPer;
-      if (nb > 1) load_keys(s, t0, s1, keys);
+      uint32_t cur[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) cur[i] = keys[i];
+      if (bt + 1 < nb) load_keys(s, t0 + kBatch, s1, keys);
       unsigned flags = 0, cnt = 0;
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const bool valid = t0 + i < s1;
-        const unsigned d1 = keys[i] >> 21;
+        const unsigned d1 = cur[i] >> 21;
         if (valid && d1 >= b1) {
           flags |= 1u << i;
           ++cnt;
         }
-        warp_hist_add(S.h2, (keys[i] >> 10) & 2047u, valid && d1 == b1);
+        warp_hist_add(S.h2, (cur[i] >> 10) & 2047u, valid && d1 == b1);
       }
       unsigned tot;
       unsigned pos = base + block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &tot);
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
-        if ((flags >> i) & 1u) lst[pos++] = make_uint2(keys[i], static_cast<unsigned>(t0 + i));
+        if ((flags >> i) & 1u) lst[pos++] = make_uint2(cur[i], static_cast<unsigned>(t0 + i));
       base += tot;
     }
   }
@@ -468,15 +477,15 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.pre_wait = a.pre_wait;
   const int smem = static_cast<int>(sizeof(Smem));
   // Cluster size: one pass of kBatch scores per CTA where possible, but no
-  // more CTAs than the device keeps resident at once (a second wave would
+  // more clusters than the device keeps resident at once (a second wave would
   // double the latency-bound selection). The occupancy query assumes an empty
-  // GPU and ideal cluster placement; a quarter of headroom keeps the launch in
-  // one wave when clusters land on partly busy GPCs.
+  // GPU: the scan before this kernel has finished when its CTAs start work,
+  // and the attention after it is only scheduled once all of them run.
   if (resident_clusters(1, smem) <= 0) return cudaErrorNotSupported;
   int cs = 1;
   while (cs < kMaxCluster && static_cast<long long>(cs) * kBatch < a.Tmax) {
     const int n = resident_clusters(cs * 2, smem);
-    if (n <= 0 || 4LL * R > 3LL * n) break;
+    if (n <= 0 || R > n) break;
     cs *= 2;
   }
   if (static_cast<long long>(R) * cs > 0x7fffffffLL) return cudaErrorNotSupported;
