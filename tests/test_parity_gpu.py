@@ -117,6 +117,20 @@ def test_topk_real_valued_scores_with_nan_and_signed_zero():
         assert torch.equal(_topk_gpu(s, seq, k), oracle.topk(s, seq, k)), k
 
 
+def test_topk_periodic_blocks_of_ties():
+    # Blocks of 16 equal high scores every 400 tokens over a background of
+    # equal low scores: the k-th largest falls inside a tie class for k above
+    # and below the number of high scores (4096), so the lowest-index rule
+    # decides which ties are kept.
+    T = 512 * 200
+    s = torch.zeros((1, 1, T))
+    for j in range(256):
+        s[0, 0, 400 * j + 192:400 * j + 208] = 1.0
+    seq = torch.tensor([T], dtype=torch.int32)
+    for k in (5000, 4097, 4096, 100):
+        assert torch.equal(_topk_gpu(s, seq, k), oracle.topk(s, seq, k)), k
+
+
 def test_topk_rows_longer_than_one_bitmap_window():
     T = (1 << 20) + 70000
     s = _int_scores(1, 2, T, -3000, 3000, 11)
