@@ -49,6 +49,10 @@ def lib():
         _lib.oracle_sparse_attn.argtypes = ([I] * 7 + [P] * 8 + [I, ctypes.c_double, I, I, P, P, P])
         _lib.oracle_lse_merge.restype = I
         _lib.oracle_lse_merge.argtypes = [I, ctypes.c_longlong, I, P, P, P, P]
+        _lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        _lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        _lib.oracle_cache_append.restype = I
+        _lib.oracle_cache_append.argtypes = [I] * 7 + [P] * 8 + [I, I, P, P, P]
     return _lib
 
 
@@ -75,6 +79,41 @@ def bf16_value(bits: int) -> float:
 
 def e4m3_value(byte: int) -> float:
     return lib().oracle_e4m3_value(byte)
+
+
+def e4m3_encode(x: float) -> int:
+    """E4M3 code of x: nearest finite value, ties to even, saturated to +-448."""
+    return lib().oracle_e4m3_encode(float(x))
+
+
+def cache_append(k_new, v_new, k_cache, v_cache, k_scale, v_scale, page_table, positions, label,
+                 channels=None, index_key=None, page_size: int = 64):
+    """The cache-append step on CPU copies: returns (k_cache, v_cache, label) after writing the new tokens.
+
+    k_new, v_new bf16 [B, Hkv, D]; caches bf16 or uint8 (e4m3) [slots, Hkv, D]; label bf16 [slots, HL, C];
+    channels int32 [Hkv, C] (per-head label) or index_key bf16 [B, C] (shared key); positions int32 [B].
+    """
+    B, Hkv, D = k_new.shape
+    fp8 = k_cache.dtype == torch.uint8
+    kc = k_cache.cpu().contiguous().clone() if fp8 else _bits(k_cache).clone()
+    vc = v_cache.cpu().contiguous().clone() if fp8 else _bits(v_cache).clone()
+    ks = k_scale.float().cpu().contiguous() if fp8 else None
+    vs = v_scale.float().cpu().contiguous() if fp8 else None
+    pt = page_table.to(torch.int32).cpu().contiguous()
+    pos = positions.to(torch.int32).cpu().contiguous()
+    lb = _bits(label).clone()
+    HL, C = label.shape[1], label.shape[2]
+    ch = channels.to(torch.int32).cpu().contiguous() if channels is not None else None
+    ik = _bits(index_key) if index_key is not None else None
+    num_pages = kc.shape[0] // page_size
+    rc = lib().oracle_cache_append(B, Hkv, D, page_size, pt.shape[1], num_pages, int(fp8), _ptr(_bits(k_new)),
+                                   _ptr(_bits(v_new)), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(pt),
+                                   _ptr(pos), HL, C, _ptr(ch), _ptr(ik), _ptr(lb))
+    if rc != 0:
+        raise ValueError("oracle_cache_append: argument outside the definition")
+    if not fp8:
+        kc, vc = kc.view(torch.bfloat16), vc.view(torch.bfloat16)
+    return kc, vc, lb.view(torch.bfloat16)
 
 
 def index_score(qp, label, page_table, seq_lens, num_kv_heads: int, max_seq_len: int,

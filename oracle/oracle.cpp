@@ -38,6 +38,13 @@
 //   R7 FP8 values are e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
 //      bits, subnormals, S.1111.111 = NaN, no infinities) times one fp32 scale
 //      per physical page, separate for K and V.
+//   R8 appending a token to an FP8 cache stores e4m3(x / scale) with the
+//      page's scale: the fp32 quotient rounded to nearest even, saturated to
+//      +-448. The page's scale is set by whoever allocates the page.
+//   R9 the new token of request b goes to logical position positions[b]
+//      (a negative position skips the row); the DS label of a token is the
+//      per-head gather of its K at the heavy channels, taken from the bf16 K
+//      before any FP8 rounding; the QSA index key is an input, copied.
 //
 // All arithmetic is in double; the scores are rounded to float once, at the
 // end (the top-k ranks float scores, as the CUDA path does).
@@ -71,6 +78,27 @@ double e4m3_value(uint8_t byte) {
   else
     mag = std::ldexp(1.0 + static_cast<double>(man) / 8.0, exp - 7);  // normal
   return sign ? -mag : mag;
+}
+
+// E4M3 encoding of x (reading R8): the finite code whose value (R7) is
+// nearest to x, ties to the code with an even last mantissa bit (round to
+// nearest even); magnitudes past 448, the largest finite value, give 448
+// (saturation); NaN gives S.1111.111. Found by comparing against all 127
+// non-negative finite codes, in increasing order of value.
+uint8_t e4m3_encode(double x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  uint8_t best = 0;
+  double best_err = std::numeric_limits<double>::infinity();
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double err = std::fabs(a - e4m3_value(static_cast<uint8_t>(c)));
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = static_cast<uint8_t>(c);
+      best_err = err;
+    }
+  }
+  return sign | best;
 }
 
 long long slot_of(const int32_t* page_table, int max_pages, int page_size, int b, long long t) {
@@ -261,5 +289,63 @@ int oracle_lse_merge(int S, long long rows, int D, const double* o_part, const d
   }
   return 0;
 }
+
+// Cache append, the step before the path ([DS] review thread: the label is a
+// per-head gather of K's channels; [PLG] FP8 E4M3 paged KV; R3, R8, R9).
+//   k_new, v_new  bf16 bits [B, Hkv, D]
+//   k_cache, v_cache  [num_slots, Hkv, D]: bf16 bits (kv_fp8 = 0) or e4m3 bytes
+//   k_scale, v_scale  float [num_pages] (FP8 only)
+//   positions     int32 [B]: logical token index to write, < 0 skips the row
+//   label         bf16 bits [num_slots, HL, C]: HL == Hkv gathers
+//                 k_new[b, g, channels[g, c]]; HL == 1 copies index_key[b, c]
+// Rows whose position is past the page table or whose page id is outside
+// [0, num_pages) are skipped. Returns 0, or -1 on an argument outside the
+// definition.
+int oracle_cache_append(int B, int Hkv, int D, int page_size, int max_pages, int num_pages, int kv_fp8,
+                        const uint16_t* k_new, const uint16_t* v_new, void* k_cache, void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* page_table,
+                        const int32_t* positions, int HL, int C, const int32_t* channels,
+                        const uint16_t* index_key, uint16_t* label) {
+  if (HL != Hkv && HL != 1) return -1;
+  for (int b = 0; b < B; ++b) {
+    const long long t = positions[b];
+    if (t < 0 || t >= static_cast<long long>(max_pages) * page_size) continue;
+    const int page = page_table[static_cast<long long>(b) * max_pages + t / page_size];
+    if (page < 0 || page >= num_pages) continue;
+    const long long slot = slot_of(page_table, max_pages, page_size, b, t);
+    for (int g = 0; g < Hkv; ++g) {
+      for (int d = 0; d < D; ++d) {
+        const long long src = (static_cast<long long>(b) * Hkv + g) * D + d;
+        const long long dst = (slot * Hkv + g) * D + d;
+        if (kv_fp8) {
+          const float kq = static_cast<float>(bf16_value(k_new[src])) / k_scale[page];
+          const float vq = static_cast<float>(bf16_value(v_new[src])) / v_scale[page];
+          static_cast<uint8_t*>(k_cache)[dst] = e4m3_encode(kq);
+          static_cast<uint8_t*>(v_cache)[dst] = e4m3_encode(vq);
+        } else {
+          static_cast<uint16_t*>(k_cache)[dst] = k_new[src];
+          static_cast<uint16_t*>(v_cache)[dst] = v_new[src];
+        }
+      }
+    }
+    if (!label) continue;
+    for (int g = 0; g < HL; ++g) {
+      for (int c = 0; c < C; ++c) {
+        uint16_t v;
+        if (HL == Hkv && channels) {
+          const int ch = channels[g * C + c];
+          if (ch < 0 || ch >= D) return -1;
+          v = k_new[(static_cast<long long>(b) * Hkv + g) * D + ch];
+        } else {
+          v = index_key[static_cast<long long>(b) * C + c];
+        }
+        label[(slot * HL + g) * C + c] = v;
+      }
+    }
+  }
+  return 0;
+}
+
+uint8_t oracle_e4m3_encode(double x) { return e4m3_encode(x); }
 
 }  // extern "C"

@@ -40,6 +40,88 @@ def test_e4m3_decoder_matches_torch_on_every_code():
     assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x80] == 0.0
 
 
+def test_e4m3_encoder_matches_torch_rounding_within_range():
+    # Every code's value, every midpoint between neighbouring codes (the
+    # ties), and random values across the range including subnormals.
+    vals = sorted({oracle.e4m3_value(c) for c in range(0x7F)})
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    rnd = (dsgen.normal((4000,), 5, 1, dtype=torch.float32) * 60).clamp(-448, 448).tolist()
+    tiny = (dsgen.normal((1000,), 5, 2, dtype=torch.float32) * 2.0 ** -8).tolist()
+    xs = torch.tensor(vals + mids + [-v for v in vals + mids] + rnd + tiny, dtype=torch.float32)
+    ref = xs.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([oracle.e4m3_encode(float(x)) for x in xs.tolist()], dtype=torch.uint8)
+    assert torch.equal(got, ref)
+
+
+def test_e4m3_encoder_saturates_and_keeps_sign_zero_and_nan():
+    assert oracle.e4m3_encode(448.0) == 0x7E and oracle.e4m3_encode(449.0) == 0x7E
+    assert oracle.e4m3_encode(1e30) == 0x7E and oracle.e4m3_encode(-1e30) == 0xFE
+    assert oracle.e4m3_encode(0.0) == 0x00 and oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+    for c in range(256):                        # every finite code round-trips
+        v = oracle.e4m3_value(c)
+        if not math.isnan(v):
+            assert oracle.e4m3_encode(v) == c, c
+
+
+# ---------------------------------------------------------------- cache append
+
+def _append_case(kv_fp8: bool, per_head: bool, seed: int):
+    B, Hkv, D, C = 3, 2, 128, 16
+    pages_per_req = 3
+    pt, num_pages = _shuffled_table(B, pages_per_req, seed)
+    k_new = dsgen.normal((B, Hkv, D), seed, 1, dtype=torch.bfloat16)
+    v_new = dsgen.normal((B, Hkv, D), seed, 2, dtype=torch.bfloat16)
+    slots = num_pages * P
+    if kv_fp8:
+        kc = dsgen.uniform_int((slots, Hkv, D), 0, 126, seed, 3, dtype=torch.int32).to(torch.uint8)
+        vc = dsgen.uniform_int((slots, Hkv, D), 0, 126, seed, 4, dtype=torch.int32).to(torch.uint8)
+        ks = dsgen.uniform_float((num_pages,), 0.25, 4.0, seed, 5)
+        vs = dsgen.uniform_float((num_pages,), 0.25, 4.0, seed, 6)
+    else:
+        kc = dsgen.normal((slots, Hkv, D), seed, 3, dtype=torch.bfloat16)
+        vc = dsgen.normal((slots, Hkv, D), seed, 4, dtype=torch.bfloat16)
+        ks = vs = None
+    HL = Hkv if per_head else 1
+    label = dsgen.normal((slots, HL, C), seed, 7, dtype=torch.bfloat16)
+    channels = dsgen.uniform_int((Hkv, C), 0, D - 1, seed, 8, dtype=torch.int32) if per_head else None
+    index_key = None if per_head else dsgen.normal((B, C), seed, 9, dtype=torch.bfloat16)
+    positions = torch.tensor([63, 64, -1], dtype=torch.int32)        # last slot of a page, first of the next, skipped
+    return dict(k_new=k_new, v_new=v_new, kc=kc, vc=vc, ks=ks, vs=vs, pt=pt, positions=positions, label=label,
+                channels=channels, index_key=index_key)
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True])
+@pytest.mark.parametrize("per_head", [True, False])
+def test_cache_append_writes_the_slot_and_gathers_the_label(kv_fp8, per_head):
+    c = _append_case(kv_fp8, per_head, 40 + 2 * kv_fp8 + per_head)
+    kc, vc, lb = oracle.cache_append(c["k_new"], c["v_new"], c["kc"], c["vc"], c["ks"], c["vs"], c["pt"],
+                                     c["positions"], c["label"], channels=c["channels"], index_key=c["index_key"])
+    touched = set()
+    for b in range(c["k_new"].shape[0]):
+        t = int(c["positions"][b])
+        if t < 0:
+            continue
+        page = int(c["pt"][b, t // P])
+        slot = page * P + t % P
+        touched.add(slot)
+        if kv_fp8:
+            # torch's own float -> e4m3 conversion of the fp32 quotient (|x / scale| < 448 here)
+            kq = (c["k_new"][b].float() / c["ks"][page]).to(torch.float8_e4m3fn).view(torch.uint8)
+            vq = (c["v_new"][b].float() / c["vs"][page]).to(torch.float8_e4m3fn).view(torch.uint8)
+            assert torch.equal(kc[slot], kq) and torch.equal(vc[slot], vq)
+        else:
+            assert torch.equal(kc[slot], c["k_new"][b]) and torch.equal(vc[slot], c["v_new"][b])
+        if per_head:
+            ref = torch.gather(c["k_new"][b], 1, c["channels"].long())
+            assert torch.equal(lb[slot], ref)
+        else:
+            assert torch.equal(lb[slot, 0], c["index_key"][b])
+    others = torch.tensor([s for s in range(kc.shape[0]) if s not in touched])
+    assert torch.equal(kc[others].view(torch.uint8), c["kc"][others].view(torch.uint8))
+    assert torch.equal(lb[others].view(torch.int16), c["label"][others].view(torch.int16))
+
+
 # ---------------------------------------------------------------- helpers
 
 def _paged(dense: torch.Tensor, page_table: torch.Tensor, num_pages: int) -> torch.Tensor:
