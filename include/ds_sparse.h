@@ -69,6 +69,7 @@ typedef enum {
 #define DS_DEVERR_PAGE_ID   2u   /* a page-table entry outside [0, num_pages); its tokens were skipped */
 #define DS_DEVERR_TOKEN_IDX 4u   /* an index entry outside [0, seq_lens[b]) before the -1 padding; skipped */
 #define DS_DEVERR_TIMEOUT   8u   /* a bounded wait for an asynchronous copy gave up; the call's results are invalid */
+#define DS_DEVERR_CHANNEL   16u  /* ds_cache_append: a heavy-channel id outside [0, head_dim); that label entry skipped */
 
 typedef struct {
   int batch;             /* B, requests in the step (>= 0) */
@@ -194,6 +195,39 @@ ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void
  */
 ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_part,
                        const float* lse_part, void* out, float* lse, ds_stream_t stream);
+
+/*
+ * The step before the path: append each request's new token to the caches
+ * ("Support double sparsity", review thread: the label cache is the per-head
+ * gather of K at the heavy channels; "QSA HiSparse - SGLang plugin",
+ * "Supported versions": FP8 E4M3 paged KV, page size 64; sglang PR #39721:
+ * the indexer stores each token's raw index key).
+ *
+ * Request b's new token sits at logical position t = positions[b] (usually
+ * the sequence length before this step; negative: the request is skipped)
+ * and goes to slot page_table[b][t / 64] * 64 + t % 64, whose page the
+ * caller has allocated (and, for FP8, given its scales):
+ *   K, V rows  bf16 copied; e4m3 = the fp32 quotient x / k_scale[page]
+ *              (v_scale for V) rounded to nearest even, saturated to +-448
+ *   label row  label_heads == Hkv: label[slot, g, c] = k_new[b, g, channels[g, c]]
+ *              (the bf16 K, before any FP8 rounding);
+ *              label_heads == 1:   label[slot, 0, :] = index_key[b, :]
+ *
+ *   k_new, v_new  bf16 [B, Hkv, 128]
+ *   k_cache, v_cache, k_scale, v_scale  as in ds_sparse_decode_attn (written)
+ *   page_table    int32 [B, max_pages_per_req]; positions int32 [B]
+ *   label         bf16 [num_pages * 64, label_heads, proxy_dim], or NULL to
+ *                 write K and V only
+ *   channels      int32 [Hkv, proxy_dim], each in [0, 128) (per-head label), or NULL
+ *   index_key     bf16 [B, proxy_dim] (shared key; used when channels is NULL)
+ * A position at or past max_pages_per_req * 64 (DS_DEVERR_SEQ_LEN), a page id
+ * outside [0, num_pages) (DS_DEVERR_PAGE_ID) or a channel outside [0, 128)
+ * (DS_DEVERR_CHANNEL) is skipped and flagged. Requests must not share a slot.
+ */
+ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* v_new, ds_kv_dtype kv_dtype,
+                          void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* page_table, const int32_t* positions, int proxy_dim, int label_heads,
+                          const int32_t* channels, const void* index_key, void* label, ds_stream_t stream);
 
 /* Arguments of the chained call (meanings as in the stages above). */
 typedef struct {

@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_select_static", "ds_topk_workspace_bytes",
-    "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes",
+    "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes", "ds_cache_append",
     "ds_device_errors", "ds_decode_kernel_launches", "ds_decode_num_splits", "lib", "LIB_PATH",
 ]
 
@@ -72,6 +72,7 @@ def lib():
         L.ds_topk_select_static.restype = I
         L.ds_sparse_decode_attn.argtypes = [SP, P, P, P, I, P, P, P, P, P, I, ctypes.c_float, I, I, P, P, P, P, P]
         L.ds_lse_merge.argtypes = [I, I, I, P, P, P, P, P]
+        L.ds_cache_append.argtypes = [SP, P, P, I, P, P, P, P, P, P, I, I, P, P, P, P]
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
         L.ds_decode_workspace_bytes.restype = Z
         L.ds_sparse_decode.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P]
@@ -85,7 +86,7 @@ def lib():
         L.ds_error_string.restype = ctypes.c_char_p
         L.ds_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("ds_index_score", "ds_topk_select", "ds_sparse_decode_attn", "ds_lse_merge",
-                     "ds_sparse_decode", "ds_device_errors"):
+                     "ds_sparse_decode", "ds_device_errors", "ds_cache_append"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -172,6 +173,19 @@ def ds_lse_merge(o_part, lse_part, out, lse=None, stream=None) -> None:
     rows = lse_part[0].numel()
     _check(lib().ds_lse_merge(S, rows, D, _p(o_part), _p(lse_part), _p(out), _p(lse), _stream(stream)),
            "ds_lse_merge")
+
+
+def ds_cache_append(shape: Shape, k_new, v_new, k_cache, v_cache, k_scale, v_scale, page_table, positions,
+                    label=None, channels=None, index_key=None, stream=None) -> None:
+    """The step before the path (ds_cache_append): each request's new token into its slot, K/V and label."""
+    fp8 = k_cache.dtype == torch.uint8
+    proxy_dim = label.shape[-1] if label is not None else 0
+    label_heads = label.shape[1] if label is not None else 0
+    _check(lib().ds_cache_append(ctypes.byref(shape), _p(k_new), _p(v_new), DS_KV_FP8_E4M3 if fp8 else DS_KV_BF16,
+                                 _p(k_cache), _p(v_cache), _p(k_scale) if fp8 else None,
+                                 _p(v_scale) if fp8 else None, _p(page_table), _p(positions), proxy_dim,
+                                 label_heads, _p(channels), _p(index_key), _p(label), _stream(stream)),
+           "ds_cache_append")
 
 
 def ds_decode_workspace_bytes(shape: Shape, proxy_dim: int, k: int) -> int:

@@ -219,6 +219,36 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* v_new, ds_kv_dtype kv_dtype,
+                          void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* page_table, const int32_t* positions, int proxy_dim, int label_heads,
+                          const int32_t* channels, const void* index_key, void* label, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (kv_dtype != DS_KV_BF16 && kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
+  if (shape->batch == 0) return DS_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !page_table || !positions) return DS_ERR_INVALID_ARG;
+  if (kv_dtype == DS_KV_FP8_E4M3 && (!k_scale || !v_scale)) return DS_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return DS_ERR_INVALID_ARG;
+  if (label) {
+    if (proxy_dim != 16 && proxy_dim != 32 && proxy_dim != 64) return DS_ERR_UNSUPPORTED;
+    if (channels) {
+      if (label_heads != shape->num_kv_heads) return DS_ERR_INVALID_ARG;
+    } else {
+      if (label_heads != 1 || !index_key) return DS_ERR_INVALID_ARG;
+    }
+    if (!aligned(label, 16)) return DS_ERR_INVALID_ARG;
+  }
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  AppendArgs a{k_new, v_new, k_cache, v_cache, k_scale, v_scale, page_table, positions,
+               label ? channels : nullptr, label ? index_key : nullptr, label, err, shape->batch,
+               shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
+               kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, label ? label_heads : 0, label ? proxy_dim : 0};
+  return from_cuda(launch_cache_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 namespace {
 
 // Workspace of the chained call: the scan's unit counters (zero before the

@@ -84,6 +84,23 @@ bool sparse_attn_supported(int G);
 // when it cannot be determined).
 int sparse_attn_resident_clusters(int G, int fp8, int S);
 
+struct AppendArgs {
+  const void* k_new;       // bf16 [B, Hkv, 128]
+  const void* v_new;
+  void* k_cache;           // [slots, Hkv, 128] bf16 or e4m3
+  void* v_cache;
+  const float* k_scale;    // [num_pages], e4m3 only
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* positions;
+  const int32_t* channels; // [Hkv, C]: per-head label gathered from K; null: index_key copied
+  const void* index_key;   // bf16 [B, C]
+  void* label;             // bf16 [slots, HL, C] or null
+  unsigned* err;
+  int B, Hkv, maxp, num_pages, fp8, HL, C;
+};
+cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t stream);
+
 cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const float* lse_part,
                              void* out, float* lse, cudaStream_t stream);
 
