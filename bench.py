@@ -399,6 +399,49 @@ def run_ours(args):
     e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(ee0, ee1)) / 1e3, world)
     e2e_value = world * args.steps / e2e_s
 
+    # ---- the step before the path: appending each request's new token (its
+    # last position is rewritten with fresh rows; launch-latency-bound).
+    append_us = None
+    try:
+        gen = torch.Generator(device="cpu").manual_seed(7)
+        k_new = torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((B, Hkv, D), generator=gen).to(torch.bfloat16).to(dev)
+        pos = (inp.seq_lens - 1).clamp(min=-1).to(torch.int32)
+        if w.label_heads == Hkv:
+            channels = torch.stack([torch.randperm(D, generator=gen)[:w.proxy_dim] for _ in range(Hkv)])
+            channels, index_key = channels.to(torch.int32).to(dev), None
+        else:
+            channels = None
+            index_key = torch.randn((B, w.proxy_dim), generator=gen).to(torch.bfloat16).to(dev)
+        def append():
+            ds.ds_cache_append(shape, k_new, v_new, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                               inp.page_table, pos, label=inp.label, channels=channels, index_key=index_key)
+
+        # Device time per call: 200 calls captured in a CUDA graph (host launch cost excluded).
+        reps = 200
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                append()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                append()
+        graph.replay()
+        torch.cuda.synchronize()
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ea[0].record(stream)
+        graph.replay()
+        ea[1].record(stream)
+        torch.cuda.synchronize()
+        append_us = ea[0].elapsed_time(ea[1]) * 1e3 / reps
+        if ds.ds_device_errors() != 0:
+            raise RuntimeError("device error word set by the cache append")
+    except Exception as e:  # reported, never hides the main measurement
+        append_us = f"failed: {e}"
+
     # ---- roofline
     peak, peak_src = measured_peak()
     ab = alg_bytes(w)
@@ -428,6 +471,7 @@ def run_ours(args):
         "step_hbm": {"alg_bytes_per_call": ab["total"], "bytes_breakdown": ab, "achieved_gbs": step_gbs,
                      "frac_of_peak": step_gbs / peak},
         "stage_us": stage_us, "internal_splits": S,
+        "cache_append_us": append_us,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "H2D of q, qp, page_table, seq_lens from pinned host memory; the chained call; "
