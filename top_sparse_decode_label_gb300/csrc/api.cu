@@ -89,7 +89,7 @@ int decode_splits(const ds_shape* s, int k) {
   const int G = s->num_q_heads / s->num_kv_heads;
   while (S > 1) {
     const int resident = sparse_attn_resident_clusters(G, 1, S);
-    if (resident == 0 || 4LL * rows <= 3LL * resident) break;   // unknown device, or one wave with headroom
+    if (resident == 0 || rows <= resident) break;   // unknown device, or every cluster resident at once
     S /= 2;
   }
   return S;
