@@ -49,6 +49,8 @@ def lib():
         _lib.oracle_sparse_attn.argtypes = ([I] * 7 + [P] * 8 + [I, ctypes.c_double, I, I, P, P, P])
         _lib.oracle_lse_merge.restype = I
         _lib.oracle_lse_merge.argtypes = [I, ctypes.c_longlong, I, P, P, P, P]
+        _lib.oracle_topk_sharded.restype = I
+        _lib.oracle_topk_sharded.argtypes = [I, I, I, P, P, I, I, I, P]
         _lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         _lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         _lib.oracle_cache_append.restype = I
@@ -143,6 +145,17 @@ def topk(scores, seq_lens, k: int, row_mask=None) -> torch.Tensor:
     if rc != 0:
         raise ValueError("oracle_topk: argument outside the definition")
     return out
+
+
+def topk_sharded(scores, seq_lens, k: int, num_shards: int, page_size: int = 64) -> torch.Tensor:
+    """Top-k by shard-local selection and a global merge (int32 [B, Hkv, k]); equals topk() by construction."""
+    B, Hkv, Tmax = scores.shape
+    sc = scores.float().cpu().contiguous()
+    sl = seq_lens.to(torch.int32).cpu().contiguous()
+    idx = torch.empty((B, Hkv, k), dtype=torch.int32)
+    if lib().oracle_topk_sharded(B, Hkv, Tmax, _ptr(sc), _ptr(sl), k, num_shards, page_size, _ptr(idx)) != 0:
+        raise ValueError("oracle_topk_sharded: argument outside the definition")
+    return idx
 
 
 def sparse_attn(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx,

@@ -45,6 +45,9 @@
 //      (a negative position skips the row); the DS label of a token is the
 //      per-head gather of its K at the heavy channels, taken from the bf16 K
 //      before any FP8 rounding; the QSA index key is an input, copied.
+//   R14 shard ownership of pages is page-interleaved: logical page p of a
+//      request belongs to shard p mod S (the placement the attention's split
+//      mode 1 also uses).
 //
 // All arithmetic is in double; the scores are rounded to float once, at the
 // end (the top-k ranks float scores, as the CUDA path does).
@@ -341,6 +344,46 @@ int oracle_cache_append(int B, int Hkv, int D, int page_size, int max_pages, int
         }
         label[(slot * HL + g) * C + c] = v;
       }
+    }
+  }
+  return 0;
+}
+
+// Exact top-k computed as the cache-sharding page describes it ([QSA]
+// "QSA cache placement", "Distributed QSA execution"; reading R14): every
+// page of a request is owned by one of S shards (logical page p by shard
+// p mod S); each shard takes the local top-k of its own tokens; the local
+// candidates are merged into the global top-k, equal scores going to the
+// smaller global token index. Same output layout as oracle_topk.
+int oracle_topk_sharded(int B, int Hkv, int Tmax, const float* scores, const int32_t* seq_lens, int k,
+                        int num_shards, int page_size, int32_t* idx) {
+  if (k < 0 || num_shards < 1 || page_size < 1) return -1;
+  for (int b = 0; b < B; ++b) {
+    const int T = seq_lens[b];
+    if (T < 0 || T > Tmax) return -1;
+    for (int g = 0; g < Hkv; ++g) {
+      const float* s = scores + (static_cast<long long>(b) * Hkv + g) * Tmax;
+      auto before = [s](int32_t x, int32_t y) {   // (score descending, token ascending), NaN last
+        const bool nx = std::isnan(s[x]), ny = std::isnan(s[y]);
+        if (nx != ny) return ny;
+        if (!nx && s[x] != s[y]) return s[x] > s[y];
+        return x < y;
+      };
+      std::vector<int32_t> candidates;
+      for (int j = 0; j < num_shards; ++j) {
+        std::vector<int32_t> local;   // this shard's tokens
+        for (int t = 0; t < T; ++t)
+          if ((t / page_size) % num_shards == j) local.push_back(t);
+        std::sort(local.begin(), local.end(), before);
+        const int kj = std::min(k, static_cast<int>(local.size()));
+        candidates.insert(candidates.end(), local.begin(), local.begin() + kj);
+      }
+      std::sort(candidates.begin(), candidates.end(), before);
+      const int keff = std::min(k, static_cast<int>(candidates.size()));
+      std::vector<int32_t> chosen(candidates.begin(), candidates.begin() + keff);
+      std::sort(chosen.begin(), chosen.end());
+      int32_t* out = idx + (static_cast<long long>(b) * Hkv + g) * k;
+      for (int i = 0; i < k; ++i) out[i] = (i < keff) ? chosen[i] : -1;
     }
   }
   return 0;

@@ -233,6 +233,18 @@ def test_topk_equals_brute_force_sort(T, k, lo, hi):
             assert idx[b, g].tolist() == _brute_topk(s[b, g].tolist(), int(seq[b]), k)
 
 
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 16])
+def test_sharded_topk_equals_the_unsharded_topk(S):
+    # The page's claim for its distributed selection: shard-local top-k plus
+    # a merge with token-id tie-breaking gives the unsharded result. Integer
+    # scores with many ties, ragged lengths, k above and below a shard's size.
+    s = dsgen.uniform_int((2, 3, 1500), -6, 6, 17, S, dtype=torch.float32)
+    s[1, 2, ::5] = float("nan")
+    seq = torch.tensor([1500, 611], dtype=torch.int32)
+    for k in (1, 64, 130, 700, 1499, 2000):
+        assert torch.equal(oracle.topk_sharded(s, seq, k, S), oracle.topk(s, seq, k)), (S, k)
+
+
 def test_topk_all_ties_take_the_lowest_indices():
     s = torch.full((1, 1, 1000), 3.0)
     idx = oracle.topk(s, torch.tensor([1000], dtype=torch.int32), 10)
