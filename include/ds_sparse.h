@@ -151,6 +151,26 @@ ds_status ds_topk_select_static(const ds_shape* shape, const float* scores, cons
                                 int32_t* idx, ds_stream_t stream);
 
 /*
+ * ds_topk_select computed the way the QSA cache-sharding page distributes it
+ * (sglang PR #43527, "QSA cache placement": each cache page has one owner;
+ * "Distributed QSA execution": each shard selects local candidates, merged
+ * into an exact global Top-K with deterministic global token-ID
+ * tie-breaking), emulated on one GPU: logical page p of a request belongs to
+ * shard p mod num_shards; each shard takes the local top-k of its tokens; the
+ * merge takes the top-k of the union, equal scores to the smaller token
+ * index. The result equals ds_topk_select's (same arguments and layout).
+ *
+ *   num_shards  1 .. 64 (num_shards * B * Hkv <= 65535)
+ *   workspace   at least ds_topk_sharded_workspace_bytes(shape, k, num_shards)
+ *               bytes, 256-byte aligned; needs no initialisation (the call
+ *               clears what it needs with an asynchronous memset)
+ */
+size_t ds_topk_sharded_workspace_bytes(const ds_shape* shape, int k, int num_shards);
+ds_status ds_topk_select_sharded(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
+                                 int num_shards, int32_t* idx, void* workspace, size_t workspace_bytes,
+                                 ds_stream_t stream);
+
+/*
  * Stage 3: sparse GQA decode attention over the selected tokens (PR #1459
  * sparse decode attention; PR #39721 sparse_gqa; FP8 E4M3 paged KV of the
  * QSA HiSparse plugin).

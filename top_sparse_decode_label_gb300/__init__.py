@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_select_static", "ds_topk_workspace_bytes",
     "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes", "ds_cache_append",
+    "ds_topk_select_sharded", "ds_topk_sharded_workspace_bytes",
     "ds_device_errors", "ds_decode_kernel_launches", "ds_decode_num_splits", "lib", "LIB_PATH",
 ]
 
@@ -73,6 +74,9 @@ def lib():
         L.ds_sparse_decode_attn.argtypes = [SP, P, P, P, I, P, P, P, P, P, I, ctypes.c_float, I, I, P, P, P, P, P]
         L.ds_lse_merge.argtypes = [I, I, I, P, P, P, P, P]
         L.ds_cache_append.argtypes = [SP, P, P, I, P, P, P, P, P, P, I, I, P, P, P, P]
+        L.ds_topk_sharded_workspace_bytes.argtypes = [SP, I, I]
+        L.ds_topk_sharded_workspace_bytes.restype = Z
+        L.ds_topk_select_sharded.argtypes = [SP, P, P, I, I, P, P, Z, P]
         L.ds_decode_workspace_bytes.argtypes = [SP, I, I]
         L.ds_decode_workspace_bytes.restype = Z
         L.ds_sparse_decode.argtypes = [SP, ctypes.POINTER(DecodeArgs), P, Z, P]
@@ -86,7 +90,7 @@ def lib():
         L.ds_error_string.restype = ctypes.c_char_p
         L.ds_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("ds_index_score", "ds_topk_select", "ds_sparse_decode_attn", "ds_lse_merge",
-                     "ds_sparse_decode", "ds_device_errors", "ds_cache_append"):
+                     "ds_sparse_decode", "ds_device_errors", "ds_cache_append", "ds_topk_select_sharded"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -173,6 +177,18 @@ def ds_lse_merge(o_part, lse_part, out, lse=None, stream=None) -> None:
     rows = lse_part[0].numel()
     _check(lib().ds_lse_merge(S, rows, D, _p(o_part), _p(lse_part), _p(out), _p(lse), _stream(stream)),
            "ds_lse_merge")
+
+
+def ds_topk_sharded_workspace_bytes(shape: Shape, k: int, num_shards: int) -> int:
+    return lib().ds_topk_sharded_workspace_bytes(ctypes.byref(shape), k, num_shards)
+
+
+def ds_topk_select_sharded(shape: Shape, scores, seq_lens, k: int, num_shards: int, idx, workspace,
+                           stream=None) -> None:
+    """ds_topk_select by page-interleaved shards and an exact merge (ds_topk_select_sharded); same result."""
+    _check(lib().ds_topk_select_sharded(ctypes.byref(shape), _p(scores), _p(seq_lens), k, num_shards, _p(idx),
+                                        _p(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "ds_topk_select_sharded")
 
 
 def ds_cache_append(shape: Shape, k_new, v_new, k_cache, v_cache, k_scale, v_scale, page_table, positions,

@@ -17,6 +17,7 @@ namespace ds {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxShards = 64;   // virtual shards of ds_topk_select_sharded
 
 int current_device() {
   int dev = -1;
@@ -217,6 +218,31 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
   if (!aligned(o_part, 16) || !aligned(out, 8) || !aligned(lse_part, 4)) return DS_ERR_INVALID_ARG;
   return from_cuda(launch_lse_merge(num_splits, rows, head_dim, o_part, lse_part, out, lse,
                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t ds_topk_sharded_workspace_bytes(const ds_shape* shape, int k, int num_shards) {
+  if (check_shape(shape) != DS_OK || k < 0 || num_shards < 1 || num_shards > kMaxShards) return 0;
+  return topk_sharded_workspace_bytes(shape->batch * shape->num_kv_heads, shape->max_seq_len, k, num_shards);
+}
+
+ds_status ds_topk_select_sharded(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,
+                                 int num_shards, int32_t* idx, void* workspace, size_t workspace_bytes,
+                                 ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (k < 0 || num_shards < 1) return DS_ERR_INVALID_ARG;
+  if (num_shards > kMaxShards) return DS_ERR_UNSUPPORTED;
+  if (shape->batch == 0 || k == 0) return DS_OK;
+  if (!seq_lens || !idx || (shape->max_seq_len > 0 && !scores)) return DS_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || (scores && !aligned(scores, 4))) return DS_ERR_INVALID_ARG;
+  const size_t need = topk_sharded_workspace_bytes(shape->batch * shape->num_kv_heads, shape->max_seq_len, k,
+                                                   num_shards);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  return from_cuda(launch_topk_sharded(scores, seq_lens, shape->batch, shape->num_kv_heads, shape->max_seq_len,
+                                       shape->max_pages_per_req * shape->page_size, k, num_shards, idx, workspace,
+                                       err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* v_new, ds_kv_dtype kv_dtype,

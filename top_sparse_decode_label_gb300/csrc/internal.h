@@ -57,6 +57,11 @@ struct TopkArgs {
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
+// Top-k by S page-interleaved shards and an exact merge (ds_topk_select_sharded).
+size_t topk_sharded_workspace_bytes(int R, int Tmax, int k, int S);
+cudaError_t launch_topk_sharded(const float* scores, const int32_t* seq_lens, int B, int Hkv, int Tmax, int lim,
+                                int k, int S, int32_t* idx, void* ws, unsigned* err, cudaStream_t stream);
+
 struct AttnArgs {
   const void* q;           // bf16 [B, Hq, D]
   const void* k_cache;     // [slots, Hkv, D]
