@@ -442,6 +442,35 @@ def run_ours(args):
     except Exception as e:  # reported, never hides the main measurement
         append_us = f"failed: {e}"
 
+    # ---- the shard-emulated top-k (4 page-interleaved shards, as the QSA
+    # cache-sharding page runs it) beside the single-pass top-k, on this
+    # workload's scores (no L2 flush: both read the scores from L2).
+    sharded = None
+    try:
+        scores = torch.empty((B, Hkv, w.max_seq_len), dtype=torch.float32, device=dev)
+        ds.ds_index_score(shape, inp.qp, inp.label, inp.page_table, inp.seq_lens, scores, stream=stream)
+        idx1 = torch.empty((B, Hkv, k), dtype=torch.int32, device=dev)
+        idx2 = torch.empty_like(idx1)
+        ws1 = torch.empty(ds.ds_topk_workspace_bytes(shape, k), dtype=torch.uint8, device=dev)
+        ws2 = torch.empty(ds.ds_topk_sharded_workspace_bytes(shape, k, 4), dtype=torch.uint8, device=dev)
+        times = {}
+        for name, fn in (("single_pass", lambda: ds.ds_topk_select(shape, scores, inp.seq_lens, k, idx1, ws1,
+                                                                    stream=stream)),
+                         ("sharded_4", lambda: ds.ds_topk_select_sharded(shape, scores, inp.seq_lens, k, 4, idx2,
+                                                                          ws2, stream=stream))):
+            for _ in range(5):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(50):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[name] = e0.elapsed_time(e1) * 1e3 / 50
+        sharded = {"topk_us": times, "equal": bool(torch.equal(idx1, idx2))}
+    except Exception as e:
+        sharded = f"failed: {e}"
+
     # ---- roofline
     peak, peak_src = measured_peak()
     ab = alg_bytes(w)
@@ -472,6 +501,7 @@ def run_ours(args):
                      "frac_of_peak": step_gbs / peak},
         "stage_us": stage_us, "internal_splits": S,
         "cache_append_us": append_us,
+        "sharded_topk": sharded,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "H2D of q, qp, page_table, seq_lens from pinned host memory; the chained call; "
