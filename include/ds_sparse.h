@@ -75,7 +75,8 @@ typedef struct {
   int batch;             /* B, requests in the step (>= 0) */
   int num_q_heads;       /* Hq, a multiple of num_kv_heads; Hq / Hkv in {1, 2, 4, 8} */
   int num_kv_heads;      /* Hkv (>= 1) */
-  int head_dim;          /* D; this build supports 128 */
+  int head_dim;          /* D; this build supports 128 and 256 (the QSA model's shape on Blackwell,
+                            sglang PR #43527 review thread: BF16 queries, head dimension 256) */
   int page_size;         /* P; this build supports 64 */
   int max_pages_per_req; /* row stride of page_table (>= 1) */
   int num_pages;         /* physical pages in the pool; valid page ids are [0, num_pages) */
@@ -233,15 +234,15 @@ ds_status ds_lse_merge(int num_splits, int rows, int head_dim, const float* o_pa
  *              (the bf16 K, before any FP8 rounding);
  *              label_heads == 1:   label[slot, 0, :] = index_key[b, :]
  *
- *   k_new, v_new  bf16 [B, Hkv, 128]
+ *   k_new, v_new  bf16 [B, Hkv, D]
  *   k_cache, v_cache, k_scale, v_scale  as in ds_sparse_decode_attn (written)
  *   page_table    int32 [B, max_pages_per_req]; positions int32 [B]
  *   label         bf16 [num_pages * 64, label_heads, proxy_dim], or NULL to
  *                 write K and V only
- *   channels      int32 [Hkv, proxy_dim], each in [0, 128) (per-head label), or NULL
+ *   channels      int32 [Hkv, proxy_dim], each in [0, D) (per-head label), or NULL
  *   index_key     bf16 [B, proxy_dim] (shared key; used when channels is NULL)
  * A position at or past max_pages_per_req * 64 (DS_DEVERR_SEQ_LEN), a page id
- * outside [0, num_pages) (DS_DEVERR_PAGE_ID) or a channel outside [0, 128)
+ * outside [0, num_pages) (DS_DEVERR_PAGE_ID) or a channel outside [0, D)
  * (DS_DEVERR_CHANNEL) is skipped and flagged. Requests must not share a slot.
  */
 ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* v_new, ds_kv_dtype kv_dtype,

@@ -45,8 +45,8 @@ def shape_of(inp):
     return ds.Shape(**dsgen.shape_kwargs(inp))
 
 
-def workload(name, B, Hq, Hkv, T, C, HL, k, kv="bf16", shuffle=True, seed=5, from_q=None):
-    return dsgen.Workload(name=name, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+def workload(name, B, Hq, Hkv, T, C, HL, k, kv="bf16", shuffle=True, seed=5, from_q=None, head_dim=128):
+    return dsgen.Workload(name=name, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=head_dim,
                           seq_lens=list(T), proxy_dim=C, label_heads=HL, top_k=k, kv_dtype=kv,
                           shuffle_pages=shuffle, seed=seed,
                           proxy_from_query=(HL != 1 or Hkv == 1) if from_q is None else from_q)

@@ -40,10 +40,11 @@ def _new_token(w, seed):
 
 
 def _positions(w, skip_row=None):
+    # The next token when the request's last page has room, else its last
+    # token again (the generator allocates only the pages a request uses).
     pos = []
     for b, T in enumerate(w.seq_lens):
-        cap = -(-w.max_seq_len // w.page_size) * w.page_size
-        t = T if T < cap else T - 1          # the next token, or the last one when the table is full
+        t = T if T % w.page_size else T - 1
         pos.append(-1 if b == skip_row else t)
     return torch.tensor(pos, dtype=torch.int32)
 
@@ -55,13 +56,16 @@ APPEND_CASES = [
     ("ds_bf16_single_kv", 2, 4, 1, [128, 77], 16, 1, "bf16"),
     ("qsa_fp8_hkv4_c64", 4, 32, 4, [2000, 1024, 5, 4095], 64, 1, "fp8_e4m3"),
     ("ds_fp8_hkv2_c32", 2, 8, 2, [300, 257], 32, 2, "fp8_e4m3"),
+    ("qsa_fp8_d256", 2, 16, 2, [700, 64], 64, 1, "fp8_e4m3", 256),
+    ("ds_bf16_d256", 2, 8, 4, [300, 129], 32, 4, "bf16", 256),
 ]
 
 
 @pytest.mark.parametrize("case", APPEND_CASES, ids=[c[0] for c in APPEND_CASES])
 def test_cache_append_bit_exact(case):
-    name, B, Hq, Hkv, T, C, HL, kv = case
-    w = workload(name, B, Hq, Hkv, T, C, HL, 16, kv=kv, seed=77)
+    name, B, Hq, Hkv, T, C, HL, kv = case[:8]
+    D = case[8] if len(case) > 8 else 128
+    w = workload(name, B, Hq, Hkv, T, C, HL, 16, kv=kv, seed=77, head_dim=D)
     inp = dsgen.make_inputs(w)
     g = inp.to(DEV)
     k_new, v_new, ch, ikey = _new_token(w, 31)

@@ -199,6 +199,43 @@ def test_sparse_attention_partials_match_oracle(case, S, mode):
         assert_lse_close(lse, l1[0], "merged lse")
 
 
+ATTN_CASES_256 = [
+    # name, B, Hq, Hkv, T, kv, k -- head dimension 256 (the QSA model's shape on Blackwell)
+    ("d256_g8_fp8", 2, 32, 4, [2000, 700], "fp8_e4m3", 300),
+    ("d256_g4_bf16", 2, 16, 4, [1000, 333], "bf16", 200),
+    ("d256_g1_bf16", 1, 2, 2, [515], "bf16", 97),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES_256, ids=[c[0] for c in ATTN_CASES_256])
+@pytest.mark.parametrize("S,mode", [(1, 0), (3, 0), (4, 1)])
+def test_sparse_attention_head_dim_256(case, S, mode):
+    name, B, Hq, Hkv, T, kv, k = case
+    HL = 1 if kv == "fp8_e4m3" else Hkv
+    w = workload(name, B, Hq, Hkv, T, 64 if HL == 1 else 32, HL, k, kv, head_dim=256)
+    inp = dsgen.make_inputs(w)
+    _, idx, _, _ = oracle.decode(inp, k=k)
+    g = inp.to(DEV)
+    D = 256
+    o_ref, l_ref = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale, inp.page_table,
+                                      inp.seq_lens, idx, None, S, mode)
+    o_part = torch.full((S, B, Hq, D), float("nan"), device=DEV)
+    l_part = torch.full((S, B, Hq), float("nan"), device=DEV)
+    if S == 1:
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((B, Hq), float("nan"), device=DEV)
+        _ds().ds_sparse_decode_attn(shape_of(inp), g.q, g.k_cache, g.v_cache, g.k_scale, g.v_scale, g.page_table,
+                                    g.seq_lens, idx.to(DEV), out=out, lse=lse)
+        assert_close(out, o_ref[0], atol_for(w), "out")
+        assert_lse_close(lse, l_ref[0], "lse")
+    else:
+        _ds().ds_sparse_decode_attn(shape_of(inp), g.q, g.k_cache, g.v_cache, g.k_scale, g.v_scale, g.page_table,
+                                    g.seq_lens, idx.to(DEV), num_splits=S, split_mode=mode, o_part=o_part,
+                                    lse_part=l_part)
+        assert_close(o_part, o_ref, atol_for(w), "o_part")
+        assert_lse_close(l_part, l_ref, "lse_part")
+
+
 def test_attention_with_padded_and_empty_rows():
     w = workload("pad", 3, 8, 2, [100, 0, 37], 32, 2, 64)
     inp = dsgen.make_inputs(w)
@@ -238,6 +275,8 @@ CHAIN_CASES = [
     ("longchat_ds_small", dsgen.WORKLOADS[2].scaled(batch=2, seq_lens=[2000, 1999], top_k=128)),
     ("qsa_small", dsgen.WORKLOADS[3].scaled(batch=3, seq_lens=[9000, 6401, 4096], top_k=512)),
     ("qsa_1m_small", dsgen.WORKLOADS[4].scaled(seq_lens=[40000], top_k=2048)),
+    ("qsa_d256_small", dsgen.WORKLOADS[3].scaled(batch=2, seq_lens=[9000, 4097], top_k=512, head_dim=256)),
+    ("llama_ds_d256_small", dsgen.WORKLOADS[1].scaled(batch=2, seq_lens=[5000, 77], top_k=300, head_dim=256)),
 ]
 
 

@@ -56,7 +56,7 @@ ds_status check_shape(const ds_shape* s) {
   if (s->num_q_heads % s->num_kv_heads) return DS_ERR_INVALID_ARG;
   const int G = s->num_q_heads / s->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return DS_ERR_UNSUPPORTED;
-  if (s->head_dim != kHeadDimSupported || s->page_size != kPageSupported) return DS_ERR_UNSUPPORTED;
+  if ((s->head_dim != 128 && s->head_dim != kHeadDimMax) || s->page_size != kPageSupported) return DS_ERR_UNSUPPORTED;
   // Slot and element offsets are 64-bit; page ids and token indices are int32.
   if (static_cast<long long>(s->num_pages) * s->page_size > 0x7fffffffLL) return DS_ERR_UNSUPPORTED;
   return DS_OK;
@@ -89,7 +89,7 @@ int decode_splits(const ds_shape* s, int k) {
   while (S < 16 && 2 * S <= cap && rows * 2 * S <= kDecodeTargetCtas) S *= 2;
   const int G = s->num_q_heads / s->num_kv_heads;
   while (S > 1) {
-    const int resident = sparse_attn_resident_clusters(G, 1, S);
+    const int resident = sparse_attn_resident_clusters(G, 1, S, s->head_dim);
     if (resident == 0 || rows <= resident) break;   // unknown device, or every cluster resident at once
     S /= 2;
   }
@@ -179,7 +179,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   if (k < 0 || num_splits < 1 || (split_mode != DS_SPLIT_CONTIGUOUS && split_mode != DS_SPLIT_PAGE_INTERLEAVED))
     return DS_ERR_INVALID_ARG;
   if (!(sm_scale == sm_scale)) return DS_ERR_INVALID_ARG;
-  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads)) return DS_ERR_UNSUPPORTED;
+  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads, shape->head_dim)) return DS_ERR_UNSUPPORTED;
   if (shape->batch == 0) return DS_OK;
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || (k > 0 && !idx)) return DS_ERR_INVALID_ARG;
   if (kv_dtype == DS_KV_FP8_E4M3 && (!k_scale || !v_scale)) return DS_ERR_INVALID_ARG;
@@ -195,7 +195,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   AttnArgs a{q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx, o_part, lse_part, out, lse, err,
              shape->batch, shape->num_q_heads, shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
              shape->max_seq_len, k, num_splits, split_mode, kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, sm_scale,
-             slots, n_from_seq_len, cluster_merge, pre_wait};
+             slots, n_from_seq_len, cluster_merge, pre_wait, shape->head_dim};
   return from_cuda(launch_sparse_attn(a, stream));
 }
 
@@ -271,7 +271,8 @@ ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* 
   AppendArgs a{k_new, v_new, k_cache, v_cache, k_scale, v_scale, page_table, positions,
                label ? channels : nullptr, label ? index_key : nullptr, label, err, shape->batch,
                shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
-               kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, label ? label_heads : 0, label ? proxy_dim : 0};
+               kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, label ? label_heads : 0, label ? proxy_dim : 0,
+               shape->head_dim};
   return from_cuda(launch_cache_append(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -350,7 +351,7 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (!args->q || !args->k_cache || !args->v_cache) return DS_ERR_INVALID_ARG;
   if (!aligned(args->q, 16) || !aligned(args->k_cache, 16) || !aligned(args->v_cache, 16)) return DS_ERR_INVALID_ARG;
   if (args->kv_dtype == DS_KV_FP8_E4M3 && (!args->k_scale || !args->v_scale)) return DS_ERR_INVALID_ARG;
-  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads)) return DS_ERR_UNSUPPORTED;
+  if (!sparse_attn_supported(shape->num_q_heads / shape->num_kv_heads, shape->head_dim)) return DS_ERR_UNSUPPORTED;
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -10,8 +10,7 @@
 // page_table[b][t / 64] * 64 + t % 64: its K and V rows (bf16 copied; e4m3 as
 // the fp32 quotient by the page's scale rounded to nearest even and
 // saturated to +-448) and its label row -- K[g, channels[g, c]] per KV head,
-// or the given index key. One CTA of 128 threads per (request, KV head),
-// thread d on element d of the rows. A negative position skips the request; a position
+// or the given index key. One CTA of 128 threads per (request, KV head). A negative position skips the request; a position
 // past the page table, a page id outside the pool or a channel outside
 // [0, 128) is skipped and flagged in the device error word.
 #include <cuda_fp8.h>
@@ -36,28 +35,30 @@ struct AppendParams {
   const uint16_t* index_key; // [B, C] or null
   uint16_t* label;           // [slots, HL, C] or null
   unsigned* err;
-  int Hkv, maxp, num_pages, fp8, HL, C;
+  int Hkv, maxp, num_pages, fp8, HL, C, D;
 };
 
-__global__ void __launch_bounds__(kHeadDim) cache_append_kernel(const AppendParams p) {
+constexpr int kAppendThreads = 128;
+
+__global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(const AppendParams p) {
   const int b = blockIdx.x;
   const int g = blockIdx.y;
-  const int d = threadIdx.x;
+  const int tid = threadIdx.x;
   const int t = __ldg(p.positions + b);
   if (t < 0) return;
   if (t >= p.maxp * kPage) {
-    if (d == 0 && g == 0) flag_error(p.err, 1u);
+    if (tid == 0 && g == 0) flag_error(p.err, 1u);
     return;
   }
   const int pid = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + (t >> 6));
   if (pid < 0 || pid >= p.num_pages) {
-    if (d == 0 && g == 0) flag_error(p.err, 2u);
+    if (tid == 0 && g == 0) flag_error(p.err, 2u);
     return;
   }
   const long long slot = static_cast<long long>(pid) * kPage + (t & (kPage - 1));
-  {
-    const long long src = (static_cast<long long>(b) * p.Hkv + g) * kHeadDim + d;
-    const long long dst = (slot * p.Hkv + g) * kHeadDim + d;
+  for (int d = tid; d < p.D; d += kAppendThreads) {
+    const long long src = (static_cast<long long>(b) * p.Hkv + g) * p.D + d;
+    const long long dst = (slot * p.Hkv + g) * p.D + d;
     const uint16_t kb = __ldg(p.k_new + src), vb = __ldg(p.v_new + src);
     if (p.fp8) {
       const float kq = __fdiv_rn(__uint_as_float(static_cast<uint32_t>(kb) << 16), __ldg(p.ks + pid));
@@ -71,15 +72,15 @@ __global__ void __launch_bounds__(kHeadDim) cache_append_kernel(const AppendPara
   }
   // Label row of this KV head (a shared index key: written by head 0's CTA).
   if (!p.label || g >= p.HL) return;
-  for (int c = d; c < p.C; c += kHeadDim) {
+  for (int c = tid; c < p.C; c += kAppendThreads) {
     uint16_t v;
     if (p.channels) {
       const int ch = __ldg(p.channels + g * p.C + c);
-      if (ch < 0 || ch >= kHeadDim) {
+      if (ch < 0 || ch >= p.D) {
         flag_error(p.err, 16u);
         continue;
       }
-      v = __ldg(p.k_new + (static_cast<long long>(b) * p.Hkv + g) * kHeadDim + ch);
+      v = __ldg(p.k_new + (static_cast<long long>(b) * p.Hkv + g) * p.D + ch);
     } else {
       v = __ldg(p.index_key + static_cast<long long>(b) * p.C + c);
     }
@@ -110,8 +111,9 @@ cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t stream) {
   p.fp8 = a.fp8;
   p.HL = a.HL;
   p.C = a.C;
+  p.D = a.D;
   if (a.Hkv > 65535) return cudaErrorNotSupported;
-  cache_append_kernel<<<dim3(a.B, a.Hkv), kHeadDim, 0, stream>>>(p);
+  cache_append_kernel<<<dim3(a.B, a.Hkv), kAppendThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

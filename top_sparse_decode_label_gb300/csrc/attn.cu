@@ -67,18 +67,19 @@ struct AttnParams {
   float qscale;        // sm_scale * log2(e)
 };
 
-template <bool FP8>
+template <bool FP8, int D>
 struct Cfg {
-  static constexpr int ROWB = FP8 ? kHeadDim : kHeadDim * 2;   // bytes per K or V row
+  static constexpr int ROWB = FP8 ? D : D * 2;   // bytes per K or V row
   static constexpr int NST = FP8 ? 4 : 2;                       // ring stages per warp
   static constexpr int STAGE = 2 * kTok * ROWB;                 // K tile then V tile
   static constexpr int RING = kWarps * NST * STAGE;
   static constexpr int SMEM = RING + kSeg * 4 + (FP8 ? kSeg * 8 : 0);
 };
 
-template <int G, bool FP8>
+template <int G, bool FP8, int D>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams p) {
-  using C = Cfg<FP8>;
+  using C = Cfg<FP8, D>;
+  constexpr int KS = D / 16;              // 16-wide steps over the head dimension
   constexpr int ROWB = C::ROWB;
   constexpr int NST = C::NST;
   constexpr int CPR = ROWB / 16;          // 16-byte chunks per row
@@ -105,14 +106,14 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   const int b = bg / p.Hkv;
 
   // ---- query B fragments: head pr of the group (0 past G), 8 k-steps.
-  uint32_t qb[8][2];
+  uint32_t qb[KS][2];
   float qs = p.qscale;
   auto load_q = [&]() {
-    float qv[8][4];
+    float qv[KS][4];
     const bool hv = pr < G;
-    const uint16_t* qrow = p.q + (static_cast<long long>(b) * p.Hq + g * G + (hv ? pr : 0)) * kHeadDim;
+    const uint16_t* qrow = p.q + (static_cast<long long>(b) * p.Hq + g * G + (hv ? pr : 0)) * D;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < KS; ++kk) {
       // bf16: dims 16kk + 2qc (+1) and +8; e4m3 order: dims 16kk + 4qc .. 4qc + 3
       const int d0 = FP8 ? 16 * kk + 4 * qc : 16 * kk + 2 * qc;
       const int d1 = FP8 ? d0 + 2 : d0 + 8;
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       // [2^13, 2^14): f16 keeps every bf16 mantissa there without overflow.
       float mx = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[kk][i]));
 #pragma unroll
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);   // 2^sh, exact
       qs = p.qscale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < KS; ++kk) {
         qb[kk][0] = pack_f16(qv[kk][0] * up, qv[kk][1] * up);
         qb[kk][1] = pack_f16(qv[kk][2] * up, qv[kk][3] * up);
       }
@@ -181,9 +182,9 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
 
   float m0 = -INFINITY, m1 = -INFINITY;   // running max of heads 2qc, 2qc+1 (log2 units)
   float l0 = 0.f, l1 = 0.f;                // this lane's share of the running sums
-  float acc[8][4];
+  float acc[KS][4];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+  for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
 
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
         const uint32_t rb = kb + r * ROWB;
         const int x = (lane >> 4) ^ (r & 7);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < KS; ++kk) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4(rb + (((2 * kk) ^ x) << 4), a0, a1, a2, a3);
           mma_bf16(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
         const uint32_t rb = kb + r * ROWB;
         const int x = (mi >> 1) ^ (lane & 7);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < KS / 2; ++cc) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(rb + (((2 * cc) ^ x) << 4), r0, r1, r2, r3);
           mma_f16(sa, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       l0 = l0 * c0 + e0 + e2;
       l1 = l1 * c1 + e1 + e3;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
+      for (int mt = 0; mt < KS; ++mt) {
         acc[mt][0] *= c0;
         acc[mt][1] *= c1;
         acc[mt][2] *= c0;
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
           const uint32_t rb = vb + ((lane & 7) + 8 * (mi >> 1)) * ROWB;
           const int x = (mi & 1) ^ (lane & 7);
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
+          for (int mt = 0; mt < KS; ++mt) {
             uint32_t a0, a1, a2, a3;
             ldsm_x4_t(rb + (((2 * mt) ^ x) << 4), a0, a1, a2, a3);
             mma_bf16(acc[mt], a0, a1, a2, a3, pb0, pb1);
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
           const uint32_t rb8 = vb + r8 * ROWB;
           const int x = (mi >> 1) ^ (lane & 7);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < KS / 2; ++cc) {
             uint32_t r0, r1, r2, r3;
             ldsm_x4_t(rb8 + (((2 * cc) ^ x) << 4), r0, r1, r2, r3);
             // (token 2qc, dims 2pr, 2pr+1), (token 2qc+1, ...) -> per-dim token pairs
@@ -401,20 +402,20 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
     l0 += __shfl_xor_sync(kFull, l0, o);
     l1 += __shfl_xor_sync(kFull, l1, o);
   }
-  float* wo = reinterpret_cast<float*>(ring);   // [kWarps][G][kHeadDim]
+  float* wo = reinterpret_cast<float*>(ring);   // [kWarps][G][D]
   const int h0 = 2 * qc, h1 = 2 * qc + 1;
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
+  for (int mt = 0; mt < KS; ++mt) {
     // bf16: rows pr / pr + 8 are dims 16mt + pr / + 8; e4m3: dims 16mt + 2pr / + 1
     const int da = FP8 ? 16 * mt + 2 * pr : 16 * mt + pr;
     const int db = FP8 ? da + 1 : da + 8;
     if (h0 < G) {
-      wo[(warp * G + h0) * kHeadDim + da] = acc[mt][0];
-      wo[(warp * G + h0) * kHeadDim + db] = acc[mt][2];
+      wo[(warp * G + h0) * D + da] = acc[mt][0];
+      wo[(warp * G + h0) * D + db] = acc[mt][2];
     }
     if (h1 < G) {
-      wo[(warp * G + h1) * kHeadDim + da] = acc[mt][1];
-      wo[(warp * G + h1) * kHeadDim + db] = acc[mt][3];
+      wo[(warp * G + h1) * D + da] = acc[mt][1];
+      wo[(warp * G + h1) * D + db] = acc[mt][3];
     }
   }
   if (pr == 0) {
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   __syncthreads();
 
   // ---- combine the warps: state (M, L, O unnormalised) per (head, dim)
-  float* co = wo + kWarps * G * kHeadDim;   // [G][kHeadDim]
+  float* co = wo + kWarps * G * D;   // [G][D]
   if (tid < G) {
     float M = -INFINITY;
 #pragma unroll
@@ -443,25 +444,25 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
     cl[tid] = L;
   }
   __syncthreads();
-  for (int e = tid; e < G * kHeadDim; e += kThreads) {
-    const int h = e / kHeadDim;
-    const int d = e % kHeadDim;
+  for (int e = tid; e < G * D; e += kThreads) {
+    const int h = e / D;
+    const int d = e % D;
     const float M = cm[h];
     float acc_o = 0.f;
     if (M != -INFINITY)
 #pragma unroll
       for (int w = 0; w < kWarps; ++w)
-        acc_o += (wm[w][h] == -INFINITY) ? 0.f : exp2f(wm[w][h] - M) * wo[(w * G + h) * kHeadDim + d];
+        acc_o += (wm[w][h] == -INFINITY) ? 0.f : exp2f(wm[w][h] - M) * wo[(w * G + h) * D + d];
     const float L = cl[h];
     const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
     if (p.cluster_merge) {
       co[e] = acc_o;
     } else if (p.S == 1) {
-      p.out[qrow * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? acc_o / L : 0.f);
+      p.out[qrow * D + d] = __float2bfloat16_rn(L > 0.f ? acc_o / L : 0.f);
       if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     } else {
       const long long prow = static_cast<long long>(j) * p.B * p.Hq + qrow;
-      p.o_part[prow * kHeadDim + d] = L > 0.f ? acc_o / L : 0.f;
+      p.o_part[prow * D + d] = L > 0.f ? acc_o / L : 0.f;
       if (d == 0) p.lse_part[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
   }
@@ -469,11 +470,11 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
 
   // ---- merge the cluster's S splits: CTA j finishes elements [e0, e1)
   cluster_sync();
-  const int E = G * kHeadDim;
+  const int E = G * D;
   const int e0 = j * E / p.S, e1 = (j + 1) * E / p.S;
   for (int e = e0 + tid; e < e1; e += kThreads) {
-    const int h = e / kHeadDim;
-    const int d = e % kHeadDim;
+    const int h = e / D;
+    const int d = e % D;
     float Ms[16], Ls[16], Os[16];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       }
     }
     const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
-    p.out[qrow * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    p.out[qrow * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   cluster_sync();   // keep this CTA's shared memory until every CTA has read it
@@ -507,15 +508,26 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
 
 using KernelFn = void (*)(const AttnParams);
 
-template <bool FP8>
-KernelFn pick(int G) {
+template <bool FP8, int D>
+KernelFn pick_g(int G) {
   switch (G) {
-    case 1: return sparse_attn_kernel<1, FP8>;
-    case 2: return sparse_attn_kernel<2, FP8>;
-    case 4: return sparse_attn_kernel<4, FP8>;
-    case 8: return sparse_attn_kernel<8, FP8>;
+    case 1: return sparse_attn_kernel<1, FP8, D>;
+    case 2: return sparse_attn_kernel<2, FP8, D>;
+    case 4: return sparse_attn_kernel<4, FP8, D>;
+    case 8: return sparse_attn_kernel<8, FP8, D>;
   }
   return nullptr;
+}
+
+KernelFn pick(int G, int fp8, int D) {
+  if (D == 128) return fp8 ? pick_g<true, 128>(G) : pick_g<false, 128>(G);
+  if (D == 256) return fp8 ? pick_g<true, 256>(G) : pick_g<false, 256>(G);
+  return nullptr;
+}
+
+int smem_bytes(int fp8, int D) {
+  if (D == 256) return fp8 ? Cfg<true, 256>::SMEM : Cfg<false, 256>::SMEM;
+  return fp8 ? Cfg<true, 128>::SMEM : Cfg<false, 128>::SMEM;
 }
 
 cudaError_t prepare(KernelFn fn, int bytes) {
@@ -538,13 +550,11 @@ cudaError_t prepare(KernelFn fn, int bytes) {
 
 }  // namespace
 
-bool sparse_attn_supported(int G) { return pick<false>(G) != nullptr; }
-
-int sparse_attn_smem_bytes(int fp8) { return fp8 ? Cfg<true>::SMEM : Cfg<false>::SMEM; }
+bool sparse_attn_supported(int G, int D) { return pick(G, 0, D) != nullptr; }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
-  KernelFn fn = a.fp8 ? pick<true>(G) : pick<false>(G);
+  KernelFn fn = pick(G, a.fp8, a.D);
   if (!fn) return cudaErrorNotSupported;
   const long long blocks = static_cast<long long>(a.B) * a.Hkv * a.S;
   if (blocks == 0) return cudaSuccess;
@@ -577,7 +587,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.n_known = a.n_from_seq_len;
   p.cluster_merge = a.cluster_merge;
   p.pre_wait = a.pre_wait;
-  const int smem = sparse_attn_smem_bytes(a.fp8);
+  const int smem = smem_bytes(a.fp8, a.D);
   cudaError_t e = prepare(fn, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -599,8 +609,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int sparse_attn_resident_clusters(int G, int fp8, int S) {
-  static int cache[2][9][5][64] = {};
+int sparse_attn_resident_clusters(int G, int fp8, int S, int D) {
+  static int cache[2][2][9][5][64] = {};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) {
     cudaGetLastError();
@@ -608,11 +618,12 @@ int sparse_attn_resident_clusters(int G, int fp8, int S) {
   }
   const int si = S == 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : S == 16 ? 4 : -1;
   if (si < 0) return 0;
-  int& c = cache[fp8 ? 1 : 0][G][si][dev];
+  if (D != 128 && D != 256) return 0;
+  int& c = cache[D == 256 ? 1 : 0][fp8 ? 1 : 0][G][si][dev];
   if (c) return c > 0 ? c : 0;
-  KernelFn fn = fp8 ? pick<true>(G) : pick<false>(G);
+  KernelFn fn = pick(G, fp8, D);
   if (!fn) return 0;
-  const int smem = sparse_attn_smem_bytes(fp8);
+  const int smem = smem_bytes(fp8, D);
   if (prepare(fn, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S);

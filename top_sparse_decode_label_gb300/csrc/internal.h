@@ -9,7 +9,7 @@
 
 namespace ds {
 
-constexpr int kHeadDimSupported = 128;
+constexpr int kHeadDimMax = 256;  // head dimensions: 128 and 256
 constexpr int kPageSupported = 64;
 constexpr long long kDecodeTargetCtas = 456;  // attention CTAs the chained call aims for (3 per SM)
 
@@ -82,12 +82,13 @@ struct AttnArgs {
   int n_from_seq_len;      // 1: each idx row holds exactly min(k, seq_len) valid entries (top-k output)
   int cluster_merge;       // 1: the S (<= 16) splits of a (b, g) run as one cluster and merge into out
   int pre_wait;            // 1: q may be read before the previous kernel of the stream completes
+  int D;                   // head dimension: 128 or 256
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
-bool sparse_attn_supported(int G);
+bool sparse_attn_supported(int G, int D);
 // Clusters of S attention CTAs the current device keeps resident at once (0
 // when it cannot be determined).
-int sparse_attn_resident_clusters(int G, int fp8, int S);
+int sparse_attn_resident_clusters(int G, int fp8, int S, int D);
 
 struct AppendArgs {
   const void* k_new;       // bf16 [B, Hkv, 128]
@@ -102,7 +103,7 @@ struct AppendArgs {
   const void* index_key;   // bf16 [B, C]
   void* label;             // bf16 [slots, HL, C] or null
   unsigned* err;
-  int B, Hkv, maxp, num_pages, fp8, HL, C;
+  int B, Hkv, maxp, num_pages, fp8, HL, C, D;
 };
 cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t stream);
 
