@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="index into dsgen.WORKLOADS")
+    ap.add_argument("--head-dim", type=int, default=None, help="override the workload's head dimension (128, 256)")
     ap.add_argument("--flush-mib", type=int, default=256)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,6 +193,14 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def workload_of(args) -> dsgen.Workload:
+    """The workload of --config, with --head-dim applied (its name then says so)."""
+    w = dsgen.WORKLOADS[args.config]
+    if args.head_dim is not None and args.head_dim != w.head_dim:
+        w = w.scaled(head_dim=args.head_dim, name=f"{w.name}_d{args.head_dim}")
+    return w
+
+
 def workload_config(w: dsgen.Workload, world: int, flush_mib: int) -> dict:
     """The `config` object of the JSON line; the same for both arms."""
     return {"workload": w.name, "batch": w.batch, "seq_len": w.max_seq_len, "num_q_heads": w.num_q_heads,
@@ -242,7 +251,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    w = dsgen.WORKLOADS[args.config]
+    w = workload_of(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = dsgen.make_inputs(w, device=dev).to("cpu")
     rows_per_call = w.batch * w.num_kv_heads
@@ -282,7 +291,7 @@ def run_ours(args):
     world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = dsgen.WORKLOADS[args.config]
+    w = workload_of(args)
     inp = dsgen.make_inputs(w, device=dev)
     shape = ds.Shape(**dsgen.shape_kwargs(inp))
     k = w.top_k
