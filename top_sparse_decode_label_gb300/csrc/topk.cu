@@ -23,6 +23,19 @@
 // kept, a CTA keeps its keys > thr and its equal keys whose rank in the row's
 // token order is below r; the counts of the CTAs before it give its output
 // offset. No global atomics, no completion counters, nothing to clear.
+//
+// Long rows with a small k (slices of two passes or more, K_eff <= T/128) try
+// one filtered pass first (a kernel variant with one CTA per SM, launched
+// when full-length rows qualify). Each CTA samples the largest of each lane's
+// first 32 keys and takes as its filter bin the first-digit bin where those maxima,
+// counted from the top, reach twice its share of K_eff scaled to the sample;
+// each warp then streams its own contiguous part of the slice once, adding to
+// the digit-1 histogram and to its token-ordered candidate list only the keys
+// whose first digit reaches the filter bin. The histogram is exact from the
+// highest filter bin of the cluster up, so a crossing found there is the true
+// digit 1 and the lists hold every key that can be kept; otherwise (or when a
+// warp's list overflows) the cluster clears its histograms and takes the two
+// passes above.
 #include "common.cuh"
 #include "internal.h"
 #include "topk_common.cuh"
@@ -37,6 +50,10 @@ constexpr int kBatch = kThreads * kPer;       // scores per CTA pass
 constexpr int kListCap = 4096;                // kept (key, token) pairs in shared memory
 constexpr int kMaxCluster = 16;
 constexpr int kPtCap = 1040;                  // page-table entries of a slice kept in shared memory
+constexpr int kWarps = kThreads / 32;
+constexpr int kPerF = 32;                     // scores per lane per step of the filtered pass
+constexpr int kStep = 32 * kPerF;             // keys of one warp step of the filtered pass
+constexpr int kWarpCap = kListCap / kWarps;   // (key, token) pairs one warp keeps in the filtered pass
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -68,29 +85,57 @@ struct __align__(16) Smem {
   unsigned long long scan[33];
   unsigned cnt[2];       // this CTA's keys above the threshold, equal to it
   unsigned res[4];
+  unsigned lmax;         // filtered pass: the highest filter bin of the cluster (rank 0's copy)
+  unsigned wcnt[kThreads / 32];   // filtered pass: candidates of each warp's token range
+  unsigned woff[kThreads / 32];
   int pt[kPtCap];        // page-table entries of this CTA's slice (chained call)
   uint2 list[kListCap];
 };
 constexpr int kZeroWords = 4 * kBins1 + 2 * kBins3;   // h1 .. t3
 
-// Keys of scores [t0, t0 + kPer) of a row (only t < c1 is meaningful); four
-// 16-byte loads in flight when aligned, else scalar loads.
-__device__ __forceinline__ void load_keys(const float* s, int t0, int c1, uint32_t (&keys)[kPer]) {
-  if (((reinterpret_cast<uintptr_t>(s + t0) & 15u) == 0) && (t0 + kPer <= c1)) {
-    float4 v[kPer / 4];
+// Keys of one thread's share of a tile of NT threads x N scores starting at
+// token `base` of a row: group i (4 consecutive scores) of thread r is tokens
+// base + 4 (i NT + r) .. + 3, so each 16-byte load instruction of a warp reads
+// 512 contiguous bytes (only tokens < c1 are meaningful; scalar loads where a
+// row is not 16-byte aligned or at its end).
+// The scores stay raw in registers until the tile is processed, so the loads
+// of the next tile are in flight while the current one is.
+template <int G, int NT>
+__device__ __forceinline__ void load_tile(const float* s, int base, int r, int c1, float4 (&v)[G]) {
+  const bool al = (reinterpret_cast<uintptr_t>(s + base) & 15u) == 0;
 #pragma unroll
-    for (int i = 0; i < kPer / 4; ++i) v[i] = __ldcg(reinterpret_cast<const float4*>(s + t0 + 4 * i));
-#pragma unroll
-    for (int i = 0; i < kPer / 4; ++i) {
-      keys[4 * i] = order_key(v[i].x);
-      keys[4 * i + 1] = order_key(v[i].y);
-      keys[4 * i + 2] = order_key(v[i].z);
-      keys[4 * i + 3] = order_key(v[i].w);
+  for (int i = 0; i < G; ++i) {
+    const int t = base + 4 * (i * NT + r);
+    if (al && t + 4 <= c1) {
+      v[i] = __ldcg(reinterpret_cast<const float4*>(s + t));
+    } else {
+      v[i].x = t < c1 ? __ldcg(s + t) : 0.f;
+      v[i].y = t + 1 < c1 ? __ldcg(s + t + 1) : 0.f;
+      v[i].z = t + 2 < c1 ? __ldcg(s + t + 2) : 0.f;
+      v[i].w = t + 3 < c1 ? __ldcg(s + t + 3) : 0.f;
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) keys[i] = (t0 + i < c1) ? order_key(__ldcg(s + t0 + i)) : 0u;
   }
+}
+template <int G>
+__device__ __forceinline__ void tile_keys(const float4 (&v)[G], uint32_t (&keys)[4 * G]) {
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    keys[4 * i] = order_key(v[i].x);
+    keys[4 * i + 1] = order_key(v[i].y);
+    keys[4 * i + 2] = order_key(v[i].z);
+    keys[4 * i + 3] = order_key(v[i].w);
+  }
+}
+// Token of key q of thread r in that tile.
+template <int NT>
+__device__ __forceinline__ int tile_token(int base, int r, int q) {
+  return base + 4 * ((q >> 2) * NT + r) + (q & 3);
+}
+
+// Rows that try the filtered pass: CTA slices of two passes or more, and at
+// most 1/128 of the row kept.
+__host__ __device__ __forceinline__ bool filtered_row(int slice, long long keff, int T) {
+  return slice >= 2 * kBatch && keff * 128 <= T;
 }
 
 // Adds this CTA's histogram h (nbins bins, slots hslot) into the owners'
@@ -186,7 +231,11 @@ __device__ __forceinline__ void emit(const TopkParams& p, const Smem& S, int row
   p.slots[static_cast<size_t>(row) * p.k + pos] = slot;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkParams p) {
+// FILT: the variant that tries the filtered pass first (one CTA per SM, so
+// that its deeper loads keep their registers); the other one runs two CTAs
+// per SM.
+template <bool FILT>
+__global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(const TopkParams p) {
   extern __shared__ __align__(16) unsigned char dsm[];
   Smem& S = *reinterpret_cast<Smem*>(dsm);
   const int tid = threadIdx.x;
@@ -196,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
   {
     uint4* z = reinterpret_cast<uint4*>(S.h1);
     for (int i = tid; i < kZeroWords / 4; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+      S.lmax = 0u;
+      S.res[0] = 0u;
+    }
   }
   const int b = row / p.Hkv;
   const int g = row - b * p.Hkv;
@@ -232,93 +285,285 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
   }
   cluster_arrive();   // this CTA's totals are zero: owners may receive adds
 
-  // ---- digit 1 (key bits 21..31) over the slice
-  const int nb = (s1 - s0 + kBatch - 1) / kBatch;
   const float* s = p.scores + static_cast<long long>(row) * p.Tmax;
-  // Passes over the slice with the next pass's loads in flight.
-  uint32_t keys[kPer];
-  if (nb > 0) load_keys(s, s0 + tid * kPer, s1, keys);
-  for (int bt = 0; bt < nb; ++bt) {
-    const int t0 = s0 + bt * kBatch + tid * kPer;
-    uint32_t cur[kPer];
+  unsigned b1 = 0, above1 = 0, M = 0;
+  uint2* lst = S.list;
+  bool filtered = false;
+  // Rows whose CTA slices span two passes or more and that keep at most
+  // 1/128 of their tokens first try one filtered pass: a lower bound on the
+  // threshold's first digit, guessed from a sample, lets only the keys at or
+  // above it into the histogram and the candidate list. The guess is checked
+  // exactly afterwards; when it fails every CTA of the cluster falls back to
+  // the two passes below.
+  const int SLr = ((T + static_cast<int>(cs) - 1) / static_cast<int>(cs) + 15) & ~15;
+  if (FILT && filtered_row(SLr, keff, T)) {
+    const int warp = tid >> 5, lane = tid & 31;
+    const int len = s1 - s0;
+    // Warp w owns the contiguous token range [w0, w1) of the slice, in tiles
+    // of kStep keys (kPerF per lane), so each warp appends its candidates in
+    // token order without block-wide barriers.
+    const int SW = ((len + kWarps - 1) / kWarps + kStep - 1) / kStep * kStep;
+    const int w0 = min(s1, s0 + warp * SW), w1 = min(s1, w0 + SW);
+    const int nst = (w1 - w0 + kStep - 1) / kStep;
+    float4 raw[kPerF / 4];
+    uint32_t cur[kPerF];
+    if (nst > 0) load_tile<kPerF / 4, 32>(s, w0, lane, w1, raw);
+    tile_keys(raw, cur);
+    // Sample: the largest key of each lane's share of the first tile. The filter bin
+    // is where the sampled maxima, counted from the top, reach twice this
+    // slice's share of K_eff scaled to a pass of kBatch keys (0, no filter,
+    // when they never do). Fewer maxima than keys lie above any bin, so the
+    // guess errs low.
+    {
+      unsigned mx = 0;
+      bool any = false;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) cur[i] = keys[i];
-    if (bt + 1 < nb) load_keys(s, t0 + kBatch, s1, keys);
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, cur[i] >> 21, t0 + i < s1);
-  }
-  __syncthreads();
-  cluster_wait();
-  push_bins<kBins1>(S.h1, S.t1, cs);
-  cluster_sync();
-  unsigned b1, above1, M;
-  {
-    // Row totals and this CTA's own counts scanned together (lo | own << 32).
-    unsigned c[4], l[4];
-    read_totals<kBins1, 4>(S.t1, cs, c);
-    const int hi = kBins1 - 4 * tid;
-    unsigned sc = 0, sl = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      l[j] = S.h1[hslot(hi - 1 - j)];
-      sc += c[j];
-      sl += l[j];
-    }
-    const unsigned long long v = static_cast<unsigned long long>(sc) | (static_cast<unsigned long long>(sl) << 32);
-    const unsigned long long before = block_excl_scan64(v, S.scan, nullptr);
-    unsigned run = static_cast<unsigned>(before), lrun = static_cast<unsigned>(before >> 32);
-    const unsigned need = static_cast<unsigned>(keff);
-    if (run < need && run + sc >= need) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (run + c[j] >= need) {
-          S.res[0] = static_cast<unsigned>(hi - 1 - j);
-          S.res[1] = run;
-          S.res[2] = lrun + l[j];   // this CTA's keys with digit 1 >= the threshold's
-          break;
+      for (int i = 0; i < kPerF; ++i) {
+        if (tile_token<32>(w0, lane, i) < w1) {
+          mx = max(mx, cur[i]);
+          any = true;
         }
-        run += c[j];
-        lrun += l[j];
       }
+      warp_hist_add(S.h2, mx >> 21, any);
     }
     __syncthreads();
+    const unsigned want =
+        len > 0 ? static_cast<unsigned>((2LL * keff * kThreads * kPerF + static_cast<long long>(cs) * len - 1) /
+                                        (static_cast<long long>(cs) * len))
+                : 0u;
+    {
+      const int hi = kBins1 - 4 * tid;
+      unsigned c[4], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c[j] = S.h2[hslot(hi - 1 - j)];
+        sum += c[j];
+      }
+      unsigned tot;
+      unsigned run = block_excl_scan(sum, reinterpret_cast<unsigned*>(S.scan), &tot);
+      if (want > 0 && run < want && run + sum >= want) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (run + c[j] >= want) {
+            S.res[0] = static_cast<unsigned>(hi - 1 - j);
+            break;
+          }
+          run += c[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) S.h2[hslot(hi - 1 - j)] = 0u;   // digit 2 starts from zero
+    }
+    __syncthreads();
+    const unsigned lbin = S.res[0];
+    const uint32_t lb = lbin << 21;
+    // ---- the filtered pass: the candidate list of the keys >= lb, then their digit-1 histogram
+    uint2* sub = S.list + warp * kWarpCap;
+    unsigned n = 0;   // this warp's candidates so far (only the first kWarpCap are kept)
+    for (int st = 0; st < nst; ++st) {
+      const int tb = w0 + st * kStep;
+      if (st > 0) tile_keys(raw, cur);
+      if (st + 1 < nst) load_tile<kPerF / 4, 32>(s, tb + kStep, lane, w1, raw);
+      // Group g of the tile (4 keys per lane) is 128 contiguous tokens, lane
+      // by lane: a warp ballot per key index gives every lane the number of
+      // candidates before its own, and groups without any are skipped.
+      const bool full = tb + kStep <= w1;
+#pragma unroll
+      for (int g = 0; g < kPerF / 4; ++g) {
+        bool tk[4];
+        unsigned bal[4], any = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tk[j] = cur[4 * g + j] >= lb && (full || tile_token<32>(tb, lane, 4 * g + j) < w1);
+          bal[j] = __ballot_sync(kFull, tk[j]);
+          any |= bal[j];
+        }
+        if (any) {
+          const unsigned lt = (1u << lane) - 1u;
+          unsigned q = n, tot = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            q += __popc(bal[j] & lt);
+            tot += __popc(bal[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (tk[j]) {
+              if (q < static_cast<unsigned>(kWarpCap))
+                sub[q] = make_uint2(cur[4 * g + j], static_cast<unsigned>(tile_token<32>(tb, lane, 4 * g + j)));
+              ++q;
+            }
+          }
+          n += tot;
+        }
+      }
+    }
+    // Digit-1 histogram of the candidates (an overflowing list is not used).
+    for (unsigned e = static_cast<unsigned>(lane); e < min(n, static_cast<unsigned>(kWarpCap)); e += 32)
+      atomicAdd(S.h1 + hslot(static_cast<int>(sub[e].x >> 21)), 1u);
+    if (lane == 0) S.wcnt[warp] = n;
+    __syncthreads();
+    cluster_wait();
+    push_bins<kBins1>(S.h1, S.t1, cs);
+    if (tid == 0) {
+      // This CTA's filter bin into rank 0's maximum; a warp list that
+      // overflowed posts one past the last bin, which fails the check.
+      bool over = false;
+      for (int w = 0; w < kWarps; ++w) over |= S.wcnt[w] > static_cast<unsigned>(kWarpCap);
+      cluster_red_max(cluster_map(smem_u32(&S.lmax), 0u), over ? static_cast<unsigned>(kBins1) : lbin);
+      S.res[0] = 0xffffffffu;   // no crossing yet
+    }
+    cluster_sync();
+    const unsigned lmax = cluster_ld(cluster_map(smem_u32(&S.lmax), 0u));
+    {
+      unsigned c[4];
+      read_totals<kBins1, 4>(S.t1, cs, c);
+      find_crossing<kBins1, 4>(c, static_cast<unsigned>(keff), S);
+    }
     b1 = S.res[0];
     above1 = S.res[1];
-    M = S.res[2];
-  }
-  const unsigned need1 = static_cast<unsigned>(keff) - above1;
-
-  // ---- compaction of the candidates (digit 1 >= b1), token order; digit 2
-  // (bits 10..20) histogram of the keys whose digit 1 equals b1
-  uint2* lst = (M <= static_cast<unsigned>(kListCap)) ? S.list : p.list + static_cast<size_t>(row) * p.Tmax + s0;
-  {
-    unsigned base = 0;
-    if (nb > 1) load_keys(s, s0 + tid * kPer, s1, keys);
-    for (int bt = 0; bt < nb; ++bt) {
-      const int t0 = s0 + bt * kBatch + tid * kPer;
-      uint32_t cur[kPer];
+    // Every CTA counted every key of the bins >= its own filter bin, so the
+    // totals are exact from lmax up; a crossing there is the true one, and
+    // every list holds all keys of its slice whose first digit reaches it.
+    filtered = b1 != 0xffffffffu && b1 >= lmax;
+    if (filtered) {
+      // The warps' lists, concatenated in warp (= token) order.
+      if (warp == 0) {
+        const unsigned v = lane < kWarps ? S.wcnt[lane] : 0u;
+        const unsigned inc = warp_incl_scan(v);
+        if (lane < kWarps) S.woff[lane] = inc - v;
+        if (lane == 31) S.res[2] = inc;
+      }
+      __syncthreads();
+      M = S.res[2];
+      // In place, through registers: a warp's destination may cover another
+      // warp's entries, so every entry is read before any is written.
+      const unsigned o = S.woff[warp];
+      uint2 v[kWarpCap / 32];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) cur[i] = keys[i];
-      if (bt + 1 < nb) load_keys(s, t0 + kBatch, s1, keys);
-      unsigned flags = 0, cnt = 0;
+      for (int j = 0; j < kWarpCap / 32; ++j) {
+        const unsigned e = static_cast<unsigned>(j * 32 + lane);
+        v[j] = e < n ? sub[e] : make_uint2(0u, 0u);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kWarpCap / 32; ++j) {
+        const unsigned e = static_cast<unsigned>(j * 32 + lane);
+        if (e < n) S.list[o + e] = v[j];
+      }
+      __syncthreads();
+      // digit 2 (bits 10..20) of the candidates whose first digit is b1
+      for (int e = tid; e < static_cast<int>(M); e += kThreads) {
+        const uint32_t key = S.list[e].x;
+        warp_hist_add(S.h2, (key >> 10) & 2047u, (key >> 21) == b1);
+      }
+    } else {
+      // Back to the two passes: clear the digit-1 histogram and, once every
+      // CTA has read its totals, the owners' totals.
+      uint4* z = reinterpret_cast<uint4*>(S.h1);
+      for (int i = tid; i < kBins1 / 4; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+      cluster_sync();
+      uint4* zt = reinterpret_cast<uint4*>(S.t1);
+      for (int i = tid; i < kBins1 / 4; i += kThreads) zt[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      cluster_arrive();
+    }
+  }
+
+  if (!filtered) {
+    // ---- digit 1 (key bits 21..31) over the slice
+    const int nb = (s1 - s0 + kBatch - 1) / kBatch;
+    // Passes over the slice with the next pass's loads in flight.
+    float4 raw[kPer / 4];
+    uint32_t cur[kPer];
+    if (nb > 0) load_tile<kPer / 4, kThreads>(s, s0, tid, s1, raw);
+    for (int bt = 0; bt < nb; ++bt) {
+      const int tb = s0 + bt * kBatch;
+      tile_keys(raw, cur);
+      if (bt + 1 < nb) load_tile<kPer / 4, kThreads>(s, tb + kBatch, tid, s1, raw);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, cur[i] >> 21, tile_token<kThreads>(tb, tid, i) < s1);
+    }
+    __syncthreads();
+    cluster_wait();
+    push_bins<kBins1>(S.h1, S.t1, cs);
+    cluster_sync();
+    {
+      // Row totals and this CTA's own counts scanned together (lo | own << 32).
+      unsigned c[4], l[4];
+      read_totals<kBins1, 4>(S.t1, cs, c);
+      const int hi = kBins1 - 4 * tid;
+      unsigned sc = 0, sl = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        l[j] = S.h1[hslot(hi - 1 - j)];
+        sc += c[j];
+        sl += l[j];
+      }
+      const unsigned long long v = static_cast<unsigned long long>(sc) | (static_cast<unsigned long long>(sl) << 32);
+      const unsigned long long before = block_excl_scan64(v, S.scan, nullptr);
+      unsigned run = static_cast<unsigned>(before), lrun = static_cast<unsigned>(before >> 32);
+      const unsigned need = static_cast<unsigned>(keff);
+      if (run < need && run + sc >= need) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (run + c[j] >= need) {
+            S.res[0] = static_cast<unsigned>(hi - 1 - j);
+            S.res[1] = run;
+            S.res[2] = lrun + l[j];   // this CTA's keys with digit 1 >= the threshold's
+            break;
+          }
+          run += c[j];
+          lrun += l[j];
+        }
+      }
+      __syncthreads();
+      b1 = S.res[0];
+      above1 = S.res[1];
+      M = S.res[2];
+    }
+
+    // ---- compaction of the candidates (digit 1 >= b1), token order; digit 2
+    // (bits 10..20) histogram of the keys whose digit 1 equals b1
+    lst = (M <= static_cast<unsigned>(kListCap)) ? S.list : p.list + static_cast<size_t>(row) * p.Tmax + s0;
+    unsigned base = 0;
+    // (with one pass, raw still holds it)
+    if (nb > 1) load_tile<kPer / 4, kThreads>(s, s0, tid, s1, raw);
+    for (int bt = 0; bt < nb; ++bt) {
+      const int tb = s0 + bt * kBatch;
+      tile_keys(raw, cur);
+      if (bt + 1 < nb) load_tile<kPer / 4, kThreads>(s, tb + kBatch, tid, s1, raw);
+      // Candidates per group of 4 (group g = 2048 contiguous tokens of the
+      // pass), packed 16 bits per group: one block scan orders them.
+      unsigned flags = 0;
+      unsigned long long packed = 0;
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const bool valid = t0 + i < s1;
+        const bool valid = tile_token<kThreads>(tb, tid, i) < s1;
         const unsigned d1 = cur[i] >> 21;
         if (valid && d1 >= b1) {
           flags |= 1u << i;
-          ++cnt;
+          packed += 1ull << (16 * (i >> 2));
         }
         warp_hist_add(S.h2, (cur[i] >> 10) & 2047u, valid && d1 == b1);
       }
-      unsigned tot;
-      unsigned pos = base + block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &tot);
+      unsigned long long tot;
+      const unsigned long long ex = block_excl_scan64(packed, S.scan, &tot);
+      unsigned gbase = base;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if ((flags >> i) & 1u) lst[pos++] = make_uint2(cur[i], static_cast<unsigned>(t0 + i));
-      base += tot;
+      for (int g = 0; g < kPer / 4; ++g) {
+        unsigned pos = gbase + static_cast<unsigned>((ex >> (16 * g)) & 65535u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * g + j;
+          if ((flags >> i) & 1u) lst[pos++] = make_uint2(cur[i], static_cast<unsigned>(tile_token<kThreads>(tb, tid, i)));
+        }
+        gbase += static_cast<unsigned>((tot >> (16 * g)) & 65535u);
+      }
+      base = gbase;
     }
   }
+  const unsigned need1 = static_cast<unsigned>(keff) - above1;
   __syncthreads();
   push_bins<kBins1>(S.h2, S.t2, cs);
   cluster_sync();
@@ -408,17 +653,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkPar
   cluster_wait();   // keep this CTA's shared memory until every CTA is done with it
 }
 
-// Clusters of `cs` top-k CTAs the current device keeps resident at once
-// (cached per device; 0 if unknown). Also sets the kernel's attributes.
+// Clusters of `cs` CTAs of variant FILT the current device keeps resident at
+// once (cached per device; 0 if unknown). Also sets the kernel's attributes.
+template <bool FILT>
 int resident_clusters(int cs, int smem) {
   static int cache[64][5] = {};
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
       return 0;
-    if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
       cudaGetLastError();
     attr_done[dev] = true;
   }
@@ -437,7 +685,7 @@ int resident_clusters(int cs, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel, &cfg) != cudaSuccess || n < 0) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<FILT>, &cfg) != cudaSuccess || n < 0) n = 0;
   cudaGetLastError();
   c = n > 0 ? n : -1;
   return n;
@@ -481,12 +729,27 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   // double the latency-bound selection). The occupancy query assumes an empty
   // GPU: the scan before this kernel has finished when its CTAs start work,
   // and the attention after it is only scheduled once all of them run.
-  if (resident_clusters(1, smem) <= 0) return cudaErrorNotSupported;
+  auto cluster_size = [&](auto resident) {
+    int cs = 1;
+    while (cs < kMaxCluster && static_cast<long long>(cs) * kBatch < a.Tmax) {
+      const int n = resident(cs * 2);
+      if (n <= 0 || R > n) break;
+      cs *= 2;
+    }
+    return cs;
+  };
+  // The filtered variant when full-length rows would take the filtered pass
+  // with its cluster size; otherwise the two-CTA-per-SM variant.
+  bool filt = false;
   int cs = 1;
-  while (cs < kMaxCluster && static_cast<long long>(cs) * kBatch < a.Tmax) {
-    const int n = resident_clusters(cs * 2, smem);
-    if (n <= 0 || R > n) break;
-    cs *= 2;
+  const long long keff_max = a.k < a.Tmax ? a.k : a.Tmax;
+  if (filtered_row(2 * kBatch, keff_max, a.Tmax) && resident_clusters<true>(1, smem) > 0) {
+    cs = cluster_size([&](int c) { return resident_clusters<true>(c, smem); });
+    filt = filtered_row(((a.Tmax + cs - 1) / cs + 15) & ~15, keff_max, a.Tmax);
+  }
+  if (!filt) {
+    if (resident_clusters<false>(1, smem) <= 0) return cudaErrorNotSupported;
+    cs = cluster_size([&](int c) { return resident_clusters<false>(c, smem); });
   }
   if (static_cast<long long>(R) * cs > 0x7fffffffLL) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
@@ -503,7 +766,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, p);
+  cudaError_t e = filt ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, p)
+                       : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
