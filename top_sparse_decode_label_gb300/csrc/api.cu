@@ -163,7 +163,7 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
   unsigned* err = error_word();
   if (!err) return DS_ERR_CUDA;
   TopkArgs a{scores, seq_lens, idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
-             shape->max_pages_per_req * shape->page_size, k, L, nullptr, nullptr, nullptr, nullptr, 0, 0, 0, 0};
+             shape->max_pages_per_req * shape->page_size, k, L, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, 0};
   return from_cuda(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -171,7 +171,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
                              ds_kv_dtype kv_dtype, const float* k_scale, const float* v_scale,
                              const int32_t* page_table, const int32_t* seq_lens, const int32_t* idx, int k,
                              float sm_scale, int num_splits, int split_mode, float* o_part, float* lse_part,
-                             void* out, float* lse, const int32_t* slots, int n_from_seq_len,
+                             void* out, float* lse, const int32_t* slots, const float2* sscale, int n_from_seq_len,
                              int cluster_merge, int pre_wait, cudaStream_t stream) {
   ds_status st = check_shape(shape);
   if (st != DS_OK) return st;
@@ -195,7 +195,7 @@ static ds_status attn_common(const ds_shape* shape, const void* q, const void* k
   AttnArgs a{q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, idx, o_part, lse_part, out, lse, err,
              shape->batch, shape->num_q_heads, shape->num_kv_heads, shape->max_pages_per_req, shape->num_pages,
              shape->max_seq_len, k, num_splits, split_mode, kv_dtype == DS_KV_FP8_E4M3 ? 1 : 0, sm_scale,
-             slots, n_from_seq_len, cluster_merge, pre_wait, shape->head_dim};
+             slots, sscale, n_from_seq_len, cluster_merge, pre_wait, shape->head_dim};
   return from_cuda(launch_sparse_attn(a, stream));
 }
 
@@ -206,7 +206,8 @@ ds_status ds_sparse_decode_attn(const ds_shape* shape, const void* q, const void
                                 int num_splits, ds_split_mode split_mode, float* o_part,
                                 float* lse_part, void* out, float* lse, ds_stream_t stream) {
   return attn_common(shape, q, k_cache, v_cache, kv_dtype, k_scale, v_scale, page_table, seq_lens, idx, k,
-                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, nullptr, 0, 0, 0,
+                     sm_scale, num_splits, static_cast<int>(split_mode), o_part, lse_part, out, lse, nullptr, nullptr, 0,
+                     0, 0,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -286,6 +287,7 @@ struct DecodeLayout {
   float* scores;
   TopkLayout topk;
   int32_t* slots;   // [B, Hkv, k]
+  float2* sscale;   // [B, Hkv, k] (K, V) page scales of the kept tokens (FP8 caches)
   size_t bytes;
 };
 
@@ -302,6 +304,8 @@ DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
   off = align256(off + L.topk.bytes);
   L.slots = reinterpret_cast<int32_t*>(p + off);
   off = align256(off + static_cast<size_t>(R) * (k > 0 ? k : 1) * 4);
+  L.sscale = reinterpret_cast<float2*>(p + off);
+  off = align256(off + static_cast<size_t>(R) * (k > 0 ? k : 1) * 8);
   L.bytes = off;
   return L;
 }
@@ -345,8 +349,8 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
     return DS_ERR_UNSUPPORTED;
   if (!args->qp || !args->label || !args->page_table || !args->seq_lens) return DS_ERR_INVALID_ARG;
   if (!aligned(args->qp, 16) || !aligned(args->label, 16)) return DS_ERR_INVALID_ARG;
-  // The caches are also touched by the top-k stage (L2 prefetch of the kept
-  // rows): check them before anything is launched.
+  // The cache arguments (and the FP8 page scales, which the top-k stage reads)
+  // are checked before anything is launched.
   if (args->kv_dtype != DS_KV_BF16 && args->kv_dtype != DS_KV_FP8_E4M3) return DS_ERR_INVALID_ARG;
   if (!args->q || !args->k_cache || !args->v_cache) return DS_ERR_INVALID_ARG;
   if (!aligned(args->q, 16) || !aligned(args->k_cache, 16) || !aligned(args->v_cache, 16)) return DS_ERR_INVALID_ARG;
@@ -370,18 +374,19 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   }
   if (mark(1) != cudaSuccess) return DS_ERR_CUDA;
   if (k > 0) {
-    const int row_bytes = shape->head_dim * (args->kv_dtype == DS_KV_FP8_E4M3 ? 1 : 2);
+    const bool fp8 = args->kv_dtype == DS_KV_FP8_E4M3;
     TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
                 shape->max_pages_per_req * shape->page_size, k, L.topk, L.slots, args->page_table,
-                args->k_cache, args->v_cache, row_bytes, shape->max_pages_per_req, shape->num_pages,
-                shape->max_seq_len > 0 ? 1 : 0};
+                fp8 ? args->k_scale : nullptr, fp8 ? args->v_scale : nullptr, fp8 ? L.sscale : nullptr,
+                shape->max_pages_per_req, shape->num_pages, shape->max_seq_len > 0 ? 1 : 0};
     st = from_cuda(launch_topk(ta, s));
     if (st != DS_OK) return st;
   }
   if (mark(2) != cudaSuccess) return DS_ERR_CUDA;
   st = attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
                    args->page_table, args->seq_lens, args->idx, k, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
-                   nullptr, nullptr, args->out, args->lse, k > 0 ? L.slots : nullptr, 1, S > 1 ? 1 : 0,
+                   nullptr, nullptr, args->out, args->lse, k > 0 ? L.slots : nullptr,
+                   (k > 0 && args->kv_dtype == DS_KV_FP8_E4M3) ? L.sscale : nullptr, 1, S > 1 ? 1 : 0,
                    (shape->max_seq_len > 0 || k > 0) ? 1 : 0, s);
   if (st != DS_OK) return st;
   return mark(3) == cudaSuccess ? DS_OK : DS_ERR_CUDA;

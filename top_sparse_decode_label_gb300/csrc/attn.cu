@@ -56,6 +56,7 @@ struct AttnParams {
   const int32_t* seq_lens;
   const int32_t* idx;
   const int32_t* slots;   // non-null: physical slot per selected position (-1 = skip); idx unused
+  const float2* sscale;   // with slots and FP8: (K, V) page scales per selected position
   float* o_part;
   float* lse_part;
   __nv_bfloat16* out;
@@ -207,9 +208,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
       sc_v[i] = make_float2(1.f, 1.f);
       if (pos < se && p.slots) {
         const int sv = __ldcg(p.slots + static_cast<long long>(bg) * p.k + pos);
+        // Loaded with the slot, not after it: one round trip for both.
+        const float2 given = (FP8 && p.sscale) ? __ldcg(p.sscale + static_cast<long long>(bg) * p.k + pos)
+                                               : make_float2(1.f, 1.f);
         if (sv >= 0) {
           slot_v[i] = sv;
-          if (FP8) sc_v[i] = make_float2(__ldg(p.ks + sv / kPage), __ldg(p.vs + sv / kPage));
+          if (FP8) sc_v[i] = p.sscale ? given : make_float2(__ldg(p.ks + sv / kPage), __ldg(p.vs + sv / kPage));
           ++cnt;
         }
       } else if (pos < se) {
@@ -569,6 +573,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.idx = a.idx;
   p.slots = a.slots;
+  p.sscale = a.sscale;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
   p.out = static_cast<__nv_bfloat16*>(a.out);

@@ -47,12 +47,14 @@ struct TopkArgs {
   int B, Hkv, Tmax, maxp_tokens, k;
   TopkLayout L;
   // Chained call only (slots == nullptr otherwise): physical slots of the kept
-  // tokens ([B, Hkv, k], -1 past K_eff) and L2 prefetch of their K/V rows.
+  // tokens ([B, Hkv, k], -1 past K_eff) and, with an FP8 cache (sscale
+  // non-null), the (K, V) scales of their pages.
   int32_t* slots;
   const int32_t* page_table;
-  const void* k_cache;
-  const void* v_cache;
-  int row_bytes, maxp, num_pages;
+  const float* k_scale;
+  const float* v_scale;
+  float2* sscale;          // [B, Hkv, k]
+  int maxp, num_pages;
   int pre_wait;            // inputs may be read before the previous kernel completes
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
@@ -79,6 +81,7 @@ struct AttnArgs {
   int B, Hq, Hkv, maxp, num_pages, Tmax, k, S, split_mode, fp8;
   float sm_scale;
   const int32_t* slots;    // non-null: physical slots per selected position ([B, Hkv, k], -1 = skip), idx unused
+  const float2* sscale;    // with slots and an FP8 cache: the (K, V) page scales per selected position
   int n_from_seq_len;      // 1: each idx row holds exactly min(k, seq_len) valid entries (top-k output)
   int cluster_merge;       // 1: the S (<= 16) splits of a (b, g) run as one cluster and merge into out
   int pre_wait;            // 1: q may be read before the previous kernel of the stream completes

@@ -65,13 +65,14 @@ struct TopkParams {
   uint2* list;     // [R, Tmax] overflow lists
   int Hkv, Tmax, lim, k;
   // Chained call only (slots == nullptr otherwise): the physical slot of each
-  // kept token, and an L2 prefetch of its K and V rows for the attention.
+  // kept token and, for an FP8 cache (sscale non-null), its page's K and V
+  // scales, so that the attention resolves both with one load.
   const int32_t* page_table;
   int32_t* slots;  // [R, k]
-  const uint8_t* kc;
-  const uint8_t* vc;
-  long long slot_stride;   // bytes per slot (Hkv rows)
-  int rowb, maxp, num_pages;
+  const float* ks;
+  const float* vs;
+  float2* sscale;  // [R, k]
+  int maxp, num_pages;
   int pre_wait;    // inputs may be read before the previous kernel completes
 };
 
@@ -89,6 +90,7 @@ struct __align__(16) Smem {
   unsigned wcnt[kThreads / 32];   // filtered pass: candidates of each warp's token range
   unsigned woff[kThreads / 32];
   int pt[kPtCap];        // page-table entries of this CTA's slice (chained call)
+  float2 psc[kPtCap];    // and, for an FP8 cache, the (K, V) scales of those pages
   uint2 list[kListCap];
 };
 constexpr int kZeroWords = 4 * kBins1 + 2 * kBins3;   // h1 .. t3
@@ -208,27 +210,25 @@ __device__ __forceinline__ int row_len(const TopkParams& p, int b, bool flag) {
 }
 
 // Writes kept token t at output position pos; in the chained call also its
-// physical slot, and prefetches its K and V rows into L2.
-__device__ __forceinline__ void emit(const TopkParams& p, const Smem& S, int row, int b, int g, int pg0, int npg,
-                                     int pos, int t) {
-  p.idx[static_cast<size_t>(row) * p.k + pos] = t;
+// physical slot and, for an FP8 cache, its page's (K, V) scales.
+__device__ __forceinline__ void emit(const TopkParams& p, const Smem& S, int row, int b, int pg0, int npg, int pos,
+                                     int t) {
+  const size_t o = static_cast<size_t>(row) * p.k + pos;
+  p.idx[o] = t;
   if (!p.slots) return;
   const int pg = t >> 6;
-  const int pid = (npg <= kPtCap && pg - pg0 < npg) ? S.pt[pg - pg0]
-                                                     : __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg);
+  const bool cached = npg <= kPtCap && pg - pg0 < npg;
+  const int pid = cached ? S.pt[pg - pg0] : __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg);
   int slot = -1;
+  float2 sc = make_float2(1.f, 1.f);
   if (pid < 0 || pid >= p.num_pages) {
     flag_error(p.err, 2u);
   } else {
     slot = pid * kPage + (t & (kPage - 1));
-    const long long off = static_cast<long long>(slot) * p.slot_stride + static_cast<long long>(g) * p.rowb;
-    const uintptr_t k0 = reinterpret_cast<uintptr_t>(p.kc + off), v0 = reinterpret_cast<uintptr_t>(p.vc + off);
-    for (uintptr_t a = k0 & ~static_cast<uintptr_t>(127); a < k0 + p.rowb; a += 128)
-      prefetch_l2(reinterpret_cast<const void*>(a));
-    for (uintptr_t a = v0 & ~static_cast<uintptr_t>(127); a < v0 + p.rowb; a += 128)
-      prefetch_l2(reinterpret_cast<const void*>(a));
+    if (p.sscale) sc = cached ? S.psc[pg - pg0] : make_float2(__ldg(p.ks + pid), __ldg(p.vs + pid));
   }
-  p.slots[static_cast<size_t>(row) * p.k + pos] = slot;
+  p.slots[o] = slot;
+  if (p.sscale) p.sscale[o] = sc;
 }
 
 // FILT: the variant that tries the filtered pass first (one CTA per SM, so
@@ -262,8 +262,15 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     if (p.slots && s1 > s0) {
       pg0 = s0 >> 6;
       npg = ((s1 - 1) >> 6) - pg0 + 1;
-      if (npg <= kPtCap)
-        for (int i = tid; i < npg; i += kThreads) S.pt[i] = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg0 + i);
+      if (npg <= kPtCap) {
+        for (int i = tid; i < npg; i += kThreads) {
+          const int pid = __ldg(p.page_table + static_cast<long long>(b) * p.maxp + pg0 + i);
+          S.pt[i] = pid;
+          if (p.sscale)
+            S.psc[i] = (pid >= 0 && pid < p.num_pages) ? make_float2(__ldg(p.ks + pid), __ldg(p.vs + pid))
+                                                       : make_float2(1.f, 1.f);
+        }
+      }
     }
   };
   if (p.pre_wait) setup();
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
   if (!needs_selection(p.k, T)) {
     // The whole cluster takes this branch (same row): no shared memory is
     // exchanged, so CTAs leave independently. Every token is kept.
-    for (int t = s0 + tid; t < min(s1, p.k); t += kThreads) emit(p, S, row, b, g, pg0, npg, t, t);
+    for (int t = s0 + tid; t < min(s1, p.k); t += kThreads) emit(p, S, row, b, pg0, npg, t, t);
     for (int i = keff + static_cast<int>(q) * kThreads + tid; i < p.k; i += static_cast<int>(cs) * kThreads) {
       out[i] = -1;
       if (p.slots) p.slots[static_cast<size_t>(row) * p.k + i] = -1;
@@ -642,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       ++eqr;
     }
     if (keep) {
-      if (pos < static_cast<unsigned>(p.k)) emit(p, S, row, b, g, pg0, npg, static_cast<int>(pos), static_cast<int>(v.y));
+      if (pos < static_cast<unsigned>(p.k)) emit(p, S, row, b, pg0, npg, static_cast<int>(pos), static_cast<int>(v.y));
       ++pos;
     }
   }
@@ -716,10 +723,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.k = a.k;
   p.page_table = a.page_table;
   p.slots = a.slots;
-  p.kc = static_cast<const uint8_t*>(a.k_cache);
-  p.vc = static_cast<const uint8_t*>(a.v_cache);
-  p.rowb = a.row_bytes;
-  p.slot_stride = static_cast<long long>(a.Hkv) * a.row_bytes;
+  p.ks = a.k_scale;
+  p.vs = a.v_scale;
+  p.sscale = a.sscale;
   p.maxp = a.maxp;
   p.num_pages = a.num_pages;
   p.pre_wait = a.pre_wait;
