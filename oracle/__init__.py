@@ -55,6 +55,12 @@ def lib():
         _lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         _lib.oracle_cache_append.restype = I
         _lib.oracle_cache_append.argtypes = [I] * 7 + [P] * 8 + [I, I, P, P, P]
+        _lib.oracle_block_compress.restype = I
+        _lib.oracle_block_compress.argtypes = [I] * 5 + [P] * 4
+        _lib.oracle_block_score.restype = I
+        _lib.oracle_block_score.argtypes = [I] * 7 + [P] * 5
+        _lib.oracle_block_expand.restype = I
+        _lib.oracle_block_expand.argtypes = [I] * 4 + [P] * 3
     return _lib
 
 
@@ -144,6 +150,43 @@ def topk(scores, seq_lens, k: int, row_mask=None) -> torch.Tensor:
     rc = lib().oracle_topk(B, Hkv, Tmax, _ptr(s), _ptr(sl), k, _ptr(m), _ptr(out))
     if rc != 0:
         raise ValueError("oracle_topk: argument outside the definition")
+    return out
+
+
+def block_compress(keys, page_table, seq_lens, num_pages: int, page_size: int = 64) -> torch.Tensor:
+    """Compressed block keys bf16 [num_pages, C] (readings R15, R16); pages no request uses stay zero."""
+    C = keys.shape[-1]
+    kb = _bits(keys.reshape(-1, C))
+    pt = page_table.to(torch.int32).cpu().contiguous()
+    sl = seq_lens.to(torch.int32).cpu().contiguous()
+    out = torch.zeros((num_pages, C), dtype=torch.int16)
+    if lib().oracle_block_compress(pt.shape[0], C, page_size, pt.shape[1], num_pages, _ptr(kb), _ptr(pt), _ptr(sl),
+                                   _ptr(out)) != 0:
+        raise ValueError("oracle_block_compress: argument outside the definition")
+    return out.view(torch.bfloat16)
+
+
+def block_score(qp, block_keys, page_table, seq_lens, num_kv_heads: int, page_size: int = 64) -> torch.Tensor:
+    """Block scores float32 [B, Hkv, max_pages]; blocks past ceil(T_b / 64) hold NaN."""
+    B, Hq, C = qp.shape
+    pt = page_table.to(torch.int32).cpu().contiguous()
+    sl = seq_lens.to(torch.int32).cpu().contiguous()
+    nbm = pt.shape[1]
+    out = torch.full((B, num_kv_heads, nbm), float("nan"), dtype=torch.float32)
+    if lib().oracle_block_score(B, Hq, num_kv_heads, C, page_size, pt.shape[1], nbm, _ptr(_bits(qp)),
+                                _ptr(_bits(block_keys)), _ptr(pt), _ptr(sl), _ptr(out)) != 0:
+        raise ValueError("oracle_block_score: argument outside the definition")
+    return out
+
+
+def block_expand(blocks, seq_lens, page_size: int = 64) -> torch.Tensor:
+    """Tokens of the kept blocks int32 [B, Hkv, kb * 64], ascending, -1 padded (reading R17)."""
+    B, Hkv, kb = blocks.shape
+    bl = blocks.to(torch.int32).cpu().contiguous()
+    sl = seq_lens.to(torch.int32).cpu().contiguous()
+    out = torch.empty((B, Hkv, kb * page_size), dtype=torch.int32)
+    if lib().oracle_block_expand(B, Hkv, kb, page_size, _ptr(bl), _ptr(sl), _ptr(out)) != 0:
+        raise ValueError("oracle_block_expand: argument outside the definition")
     return out
 
 

@@ -48,6 +48,16 @@
 //   R14 shard ownership of pages is page-interleaved: logical page p of a
 //      request belongs to shard p mod S (the placement the attention's split
 //      mode 1 also uses).
+//   R15 a compressed block of [QSA] "Summary" (the QSA compressed cache) and
+//      the review thread ("choose 512 of 1024 blocks") is one KV page of a
+//      request: block j covers logical tokens [64j, 64j + 64) below T_b.
+//   R16 a block's compressed index key is the per-channel mean of its tokens'
+//      index keys: their sum in double in token order, divided by the number
+//      of tokens present, rounded to bfloat16 (nearest, ties to even), stored
+//      per physical page. A block is scored like a token (R1) with its key.
+//   R17 block selection keeps the top-k blocks of each (request, KV head) by
+//      the R4 rule (ties to the lower block index); the attended tokens are
+//      every token below T_b of the kept blocks, ascending, then -1.
 //
 // All arithmetic is in double; the scores are rounded to float once, at the
 // end (the top-k ranks float scores, as the CUDA path does).
@@ -107,6 +117,22 @@ uint8_t e4m3_encode(double x) {
 long long slot_of(const int32_t* page_table, int max_pages, int page_size, int b, long long t) {
   const long long page = page_table[static_cast<long long>(b) * max_pages + t / page_size];
   return page * page_size + t % page_size;
+}
+
+// Nearest bfloat16 to x, ties to the even significand (R16): bfloat16 has the
+// exponent range of binary32 and 8 significant bits, so the spacing of values
+// near x = m 2^e (0.5 <= |m| < 1) is 2^(e-8), and never below 2^-133, the
+// smallest subnormal. Finite results only (block means of finite keys).
+uint16_t bf16_round(double x) {
+  if (x == 0.0) return std::signbit(x) ? 0x8000u : 0u;
+  int e = 0;
+  std::frexp(x, &e);
+  const int qexp = std::max(e - 8, -133);
+  const double r = std::nearbyint(std::ldexp(x, -qexp));   // default rounding: nearest, ties to even
+  const float v = static_cast<float>(std::ldexp(r, qexp));  // exact: r has at most 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  return static_cast<uint16_t>(u >> 16);
 }
 
 }  // namespace
@@ -390,5 +416,76 @@ int oracle_topk_sharded(int B, int Hkv, int Tmax, const float* scores, const int
 }
 
 uint8_t oracle_e4m3_encode(double x) { return e4m3_encode(x); }
+
+// f3, block compression (R15, R16): the compressed key of every logical page
+// j < ceil(T_b / 64) of every request, written at its physical page.
+//   keys        bf16 bits [num_slots, 1, C] (the shared index-key cache)
+//   block_keys  bf16 bits [num_pages, C]; pages outside every request untouched
+int oracle_block_compress(int B, int C, int page_size, int max_pages, int num_pages, const uint16_t* keys,
+                          const int32_t* page_table, const int32_t* seq_lens, uint16_t* block_keys) {
+  for (int b = 0; b < B; ++b) {
+    const long long T = seq_lens[b];
+    if (T < 0 || T > static_cast<long long>(max_pages) * page_size) return -1;
+    for (long long j = 0; j * page_size < T; ++j) {
+      const int32_t pid = page_table[static_cast<long long>(b) * max_pages + j];
+      if (pid < 0 || pid >= num_pages) return -1;
+      const long long t0 = j * page_size, t1 = std::min(T, t0 + page_size);
+      for (int c = 0; c < C; ++c) {
+        double sum = 0.0;
+        for (long long t = t0; t < t1; ++t) sum += bf16_value(keys[slot_of(page_table, max_pages, page_size, b, t) * C + c]);
+        block_keys[static_cast<long long>(pid) * C + c] = bf16_round(sum / static_cast<double>(t1 - t0));
+      }
+    }
+  }
+  return 0;
+}
+
+// f3, block scores (R1 with the block key, R15): scores float [B, Hkv, nb_max]
+// for blocks j < ceil(T_b / 64).
+int oracle_block_score(int B, int Hq, int Hkv, int C, int page_size, int max_pages, int nb_max, const uint16_t* qp,
+                       const uint16_t* block_keys, const int32_t* page_table, const int32_t* seq_lens,
+                       float* scores) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+  const int G = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    const long long T = seq_lens[b];
+    const long long nb = (T + page_size - 1) / page_size;
+    if (T < 0 || nb > nb_max || nb > max_pages) return -1;
+    for (int g = 0; g < Hkv; ++g) {
+      for (long long j = 0; j < nb; ++j) {
+        const long long pid = page_table[static_cast<long long>(b) * max_pages + j];
+        double s = 0.0;
+        for (int h = g * G; h < (g + 1) * G; ++h)
+          for (int c = 0; c < C; ++c)
+            s += bf16_value(qp[(static_cast<long long>(b) * Hq + h) * C + c]) * bf16_value(block_keys[pid * C + c]);
+        scores[(static_cast<long long>(b) * Hkv + g) * nb_max + j] = static_cast<float>(s);
+      }
+    }
+  }
+  return 0;
+}
+
+// f3, the tokens of the kept blocks (R17): blocks int32 [B, Hkv, kb] (ascending,
+// -1 padded) -> idx int32 [B, Hkv, kb * 64]: the tokens below T_b of each kept
+// block in ascending order, then -1.
+int oracle_block_expand(int B, int Hkv, int kb, int page_size, const int32_t* blocks, const int32_t* seq_lens,
+                        int32_t* idx) {
+  const long long width = static_cast<long long>(kb) * page_size;
+  for (int b = 0; b < B; ++b) {
+    const long long T = seq_lens[b];
+    for (int g = 0; g < Hkv; ++g) {
+      const int32_t* blk = blocks + (static_cast<long long>(b) * Hkv + g) * kb;
+      int32_t* out = idx + (static_cast<long long>(b) * Hkv + g) * width;
+      long long n = 0;
+      for (int i = 0; i < kb; ++i) {
+        if (blk[i] < 0) continue;
+        for (long long t = static_cast<long long>(blk[i]) * page_size; t < (blk[i] + 1LL) * page_size && t < T; ++t)
+          out[n++] = static_cast<int32_t>(t);
+      }
+      for (; n < width; ++n) out[n] = -1;
+    }
+  }
+  return 0;
+}
 
 }  // extern "C"

@@ -383,3 +383,93 @@ def test_merge_single_split_is_identity_and_all_empty_is_empty():
     out, lse = oracle.lse_merge(torch.zeros(3, 2, 4, dtype=torch.float64),
                                 torch.full((3, 2), -math.inf, dtype=torch.float64))
     assert torch.equal(out, torch.zeros(2, 4, dtype=torch.float64)) and torch.isinf(lse).all()
+
+
+# ---------------------------------------------------------------- block-compressed selection (f3)
+
+def _nearest_bf16_exact(x):
+    """Nearest bfloat16 to the rational x, ties to the even code, by exact comparison of its two neighbours."""
+    from fractions import Fraction
+    import struct
+    if x == 0:
+        return 0
+    f = float(x)                                   # within a float ulp of x
+    bits = struct.unpack("<I", struct.pack("<f", f))[0] >> 16
+    cands = []
+    for d in (-2, -1, 0, 1, 2):
+        c = (bits + d) & 0xFFFF
+        v = struct.unpack("<f", struct.pack("<I", c << 16))[0]
+        if math.isfinite(v) and (v > 0) == (x > 0):
+            cands.append((abs(Fraction(v) - x), c & 1, c))
+    cands.sort()
+    best = [c for c in cands if c[0] == cands[0][0]]
+    return min(best, key=lambda c: c[1])[2]        # a tie goes to the even significand
+
+
+def _block_case(seed, B=2, T=(200, 64 * 3), C=16, scale=1.0):
+    P_ = (max(T) + P - 1) // P
+    pt = torch.stack([dsgen.permutation(P_ * B, seed, 50)[b * P_:(b + 1) * P_] for b in range(B)]).to(torch.int32)
+    keys = (dsgen.normal((P_ * B * P, 1, C), seed, 51, dtype=torch.float32) * scale).to(torch.bfloat16)
+    return keys, pt, torch.tensor(T, dtype=torch.int32), P_ * B
+
+
+def test_block_keys_are_the_exactly_rounded_means_of_their_tokens():
+    from fractions import Fraction
+    keys, pt, sl, npages = _block_case(3)
+    bk = oracle.block_compress(keys, pt, sl, npages)
+    kb = keys.view(torch.int16)
+    for b in range(pt.shape[0]):
+        T = int(sl[b])
+        for j in range((T + P - 1) // P):
+            pid = int(pt[b, j])
+            toks = range(j * P, min(T, j * P + P))
+            for c in range(keys.shape[-1]):
+                mean = sum(Fraction(float(keys[pid * P + t % P, 0, c])) for t in toks) / len(toks)
+                assert int(bk[pid, c].view(torch.int16)) & 0xFFFF == _nearest_bf16_exact(mean), (b, j, c)
+
+
+def test_block_key_rounding_ties_go_to_the_even_code():
+    # Pages holding two tokens: the means 1 + 2^-8 and 1 + 3 * 2^-8 lie halfway between neighbouring bfloat16
+    # values; the even significands are 1.0 and 1 + 2^-6.
+    keys = torch.zeros((2 * P, 1, 2), dtype=torch.bfloat16)
+    keys[0, 0, 0], keys[1, 0, 0] = 1.0, 1.0 + 2 ** -7
+    keys[0, 0, 1], keys[1, 0, 1] = 1.0 + 2 ** -7, 1.0 + 2 ** -6
+    keys[P, 0, 0], keys[P + 1, 0, 0] = -1.0, -(1.0 + 2 ** -7)
+    pt = torch.tensor([[0], [1]], dtype=torch.int32)
+    bk = oracle.block_compress(keys, pt, torch.tensor([2, 2], dtype=torch.int32), 2).float()
+    assert bk[0, 0] == 1.0 and bk[0, 1] == 1.0 + 2 ** -6 and bk[1, 0] == -1.0
+
+
+def test_block_key_of_a_constant_page_is_that_key():
+    keys = torch.zeros((3 * P, 1, 4), dtype=torch.bfloat16)
+    keys[:P] = 0.3
+    keys[P:2 * P] = -7.5
+    keys[2 * P:] = 1e-30
+    pt = torch.tensor([[2, 0, 1]], dtype=torch.int32)   # logical pages 0, 1, 2 -> physical 2, 0, 1 (5 tokens in 2)
+    bk = oracle.block_compress(keys, pt, torch.tensor([2 * P + 5], dtype=torch.int32), 3)
+    assert torch.equal(bk[0], keys[0, 0]) and torch.equal(bk[1], keys[P, 0]) and torch.equal(bk[2], keys[2 * P, 0])
+
+
+def test_block_scores_match_a_library_contraction_of_the_block_keys():
+    keys, pt, sl, npages = _block_case(5, C=64)
+    bk = oracle.block_compress(keys, pt, sl, npages)
+    B, Hq, Hkv = 2, 8, 2
+    qp = dsgen.normal((B, Hq, 64), 5, 52)
+    s = oracle.block_score(qp, bk, pt, sl, Hkv)
+    qg = qp.double().view(B, Hkv, Hq // Hkv, 64).sum(2)
+    for b in range(B):
+        nb = (int(sl[b]) + P - 1) // P
+        ref = torch.einsum("gc,jc->gj", qg[b], bk[pt[b, :nb].long()].double()).float()
+        assert torch.equal(s[b, :, :nb], ref)
+        assert torch.isnan(s[b, :, nb:]).all()
+
+
+def test_block_expansion_lists_the_kept_blocks_tokens_below_the_length():
+    blocks = torch.tensor([[[0, 2, 3, -1]], [[1, -1, -1, -1]]], dtype=torch.int32)
+    sl = torch.tensor([3 * P + 10, 64], dtype=torch.int32)
+    idx = oracle.block_expand(blocks, sl)
+    want0 = list(range(0, P)) + list(range(2 * P, 3 * P)) + list(range(3 * P, 3 * P + 10))
+    assert idx[0, 0, :len(want0)].tolist() == want0 and (idx[0, 0, len(want0):] == -1).all()
+    assert (idx[1, 0] == -1).all()          # block 1 lies past the 64-token sequence
+    all_blocks = torch.arange(4, dtype=torch.int32).view(1, 1, 4)
+    assert torch.equal(oracle.block_expand(all_blocks, sl[:1])[0, 0, :3 * P + 10], torch.arange(3 * P + 10, dtype=torch.int32))
