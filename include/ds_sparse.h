@@ -299,6 +299,68 @@ ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, vo
 ds_status ds_sparse_decode_profiled(const ds_shape* shape, const ds_decode_args* args, void* workspace,
                                     size_t workspace_bytes, ds_stream_t stream, void* const* events);
 
+/* ------------------------------------------------------------------------
+ * Block-compressed selection (sglang PR #43527 "QSA cache sharding",
+ * "Summary": the QSA state keeps a compressed cache beside the raw K/V
+ * history, and the review thread has the merge "choose 512 of 1024 blocks").
+ * The pages do not define a block or its compressed key; this library's
+ * reading: a block is one 64-token page of a request, and its key is the
+ * per-channel mean of its tokens' index keys (summed in double in token
+ * order, divided by the tokens present, rounded to nearest-even bf16).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Compressed keys of the blocks of every request, written at each block's
+ * physical page:
+ *   index_key   bf16 [num_pages * page_size, 1, proxy_dim], the shared
+ *               per-token index keys (16-byte aligned); proxy_dim 16, 32, 64
+ *   page_table  int32 [B, max_pages_per_req]; seq_lens int32 [B]
+ *   block_keys  out: bf16 [num_pages, proxy_dim] (16-byte aligned); entries of
+ *               pages outside every request's first ceil(T_b / 64) pages are
+ *               not written
+ *   last_page_only  nonzero: only the page holding token T_b - 1 of each
+ *               request (the one an append changes)
+ * A sequence length outside [0, max_pages_per_req * 64] is flagged
+ * (DS_DEVERR_SEQ_LEN) and its request skipped; a page id outside
+ * [0, num_pages) is flagged (DS_DEVERR_PAGE_ID) and its block skipped.
+ */
+ds_status ds_block_compress(const ds_shape* shape, const void* index_key, int proxy_dim, const int32_t* page_table,
+                            const int32_t* seq_lens, int last_page_only, void* block_keys, ds_stream_t stream);
+
+typedef struct ds_block_decode_args {
+  const void* q;             /* bf16 [B, Hq, D] attention queries */
+  const void* qp;            /* bf16 [B, Hq, proxy_dim] index queries */
+  int proxy_dim;             /* 16, 32 or 64 */
+  const void* block_keys;    /* bf16 [num_pages, proxy_dim], from ds_block_compress */
+  const void* k_cache;       /* [num_pages * 64, Hkv, D] bf16 or e4m3 */
+  const void* v_cache;
+  ds_kv_dtype kv_dtype;
+  const float* k_scale;      /* fp32 [num_pages] (e4m3 only) */
+  const float* v_scale;
+  const int32_t* page_table; /* int32 [B, max_pages_per_req] */
+  const int32_t* seq_lens;   /* int32 [B] */
+  int kb;                    /* blocks kept per (request, KV head) */
+  float sm_scale;
+  int32_t* blocks;           /* out: int32 [B, Hkv, kb] kept blocks, ascending, -1 padded */
+  void* out;                 /* out: bf16 [B, Hq, D] */
+  float* lse;                /* out: fp32 [B, Hq] (may be NULL) */
+} ds_block_decode_args;
+
+/*
+ * The block-level decode step: block scores s[b,g,j] = sum over the group's
+ * query heads and channels of qp * block key (the ds_index_score sum with the
+ * block key in place of the token key), the exact top-kb blocks of each
+ * (request, KV head) with ties to the lower block index (the ds_topk_select
+ * rule on block rows of ceil(T_b / 64) entries), then sparse attention with
+ * the fused LSE merge over every token below T_b of the kept blocks (at most
+ * kb * 64 tokens). `workspace`: at least ds_block_decode_workspace_bytes
+ * bytes, 256-byte aligned, no initialisation; calls sharing it must not
+ * overlap. No host synchronisation, no allocation.
+ */
+size_t ds_block_decode_workspace_bytes(const ds_shape* shape, int kb);
+ds_status ds_sparse_decode_blocks(const ds_shape* shape, const ds_block_decode_args* args, void* workspace,
+                                  size_t workspace_bytes, ds_stream_t stream);
+
 /*
  * Kernel launches one ds_sparse_decode call makes for this shape and k (not
  * counting the one cudaMemsetAsync of the top-k counters); 0 when the

@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "Shape", "DsError", "ds_index_score", "ds_topk_select", "ds_topk_select_static", "ds_topk_workspace_bytes",
     "ds_sparse_decode_attn", "ds_lse_merge", "ds_sparse_decode", "ds_decode_workspace_bytes", "ds_cache_append",
-    "ds_topk_select_sharded", "ds_topk_sharded_workspace_bytes",
+    "ds_topk_select_sharded", "ds_topk_sharded_workspace_bytes", "ds_block_compress",
+    "ds_block_decode_workspace_bytes", "ds_sparse_decode_blocks",
     "ds_device_errors", "ds_decode_kernel_launches", "ds_decode_num_splits", "lib", "LIB_PATH",
 ]
 
@@ -43,6 +44,16 @@ class DecodeArgs(ctypes.Structure):
                 ("v_scale", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
                 ("k", ctypes.c_int), ("sm_scale", ctypes.c_float), ("idx", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
+class BlockDecodeArgs(ctypes.Structure):
+    """ds_block_decode_args: the block-level decode step's tensors."""
+    _fields_ = [("q", ctypes.c_void_p), ("qp", ctypes.c_void_p), ("proxy_dim", ctypes.c_int),
+                ("block_keys", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("kb", ctypes.c_int),
+                ("sm_scale", ctypes.c_float), ("blocks", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p)]
 
 
 class DsError(RuntimeError):
@@ -86,11 +97,16 @@ def lib():
         L.ds_decode_num_splits.restype = I
         L.ds_decode_kernel_launches.argtypes = [SP, I]
         L.ds_decode_kernel_launches.restype = I
+        L.ds_block_compress.argtypes = [SP, P, I, P, P, I, P, P]
+        L.ds_block_decode_workspace_bytes.argtypes = [SP, I]
+        L.ds_block_decode_workspace_bytes.restype = Z
+        L.ds_sparse_decode_blocks.argtypes = [SP, ctypes.POINTER(BlockDecodeArgs), P, Z, P]
         L.ds_error_string.argtypes = [I]
         L.ds_error_string.restype = ctypes.c_char_p
         L.ds_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("ds_index_score", "ds_topk_select", "ds_sparse_decode_attn", "ds_lse_merge",
-                     "ds_sparse_decode", "ds_device_errors", "ds_cache_append", "ds_topk_select_sharded"):
+                     "ds_sparse_decode", "ds_device_errors", "ds_cache_append", "ds_topk_select_sharded",
+                     "ds_block_compress", "ds_sparse_decode_blocks"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -238,6 +254,33 @@ def ds_sparse_decode(shape: Shape, q, qp, label, k_cache, v_cache, k_scale, v_sc
         st = lib().ds_sparse_decode_profiled(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes,
                                              _stream(stream), handles)
     _check(st, "ds_sparse_decode")
+
+
+def ds_block_compress(shape: Shape, index_key, page_table, seq_lens, block_keys, last_page_only: bool = False,
+                      stream=None) -> None:
+    """Compressed block keys (ds_block_compress): bf16 [num_pages, C] from the index keys [slots, 1, C]."""
+    _check(lib().ds_block_compress(ctypes.byref(shape), _p(index_key), index_key.shape[-1], _p(page_table),
+                                   _p(seq_lens), 1 if last_page_only else 0, _p(block_keys), _stream(stream)),
+           "ds_block_compress")
+
+
+def ds_block_decode_workspace_bytes(shape: Shape, kb: int) -> int:
+    return lib().ds_block_decode_workspace_bytes(ctypes.byref(shape), kb)
+
+
+def ds_sparse_decode_blocks(shape: Shape, q, qp, block_keys, k_cache, v_cache, k_scale, v_scale, page_table,
+                            seq_lens, kb: int, blocks, out, lse=None, workspace=None,
+                            sm_scale: Optional[float] = None, stream=None) -> None:
+    """The block-level decode step (ds_sparse_decode_blocks): kept blocks, out and lse."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(shape.head_dim)
+    a = BlockDecodeArgs(q=_p(q), qp=_p(qp), proxy_dim=qp.shape[-1], block_keys=_p(block_keys), k_cache=_p(k_cache),
+                        v_cache=_p(v_cache), kv_dtype=_kv_dtype(k_cache), k_scale=_p(k_scale),
+                        v_scale=_p(v_scale), page_table=_p(page_table), seq_lens=_p(seq_lens), kb=kb,
+                        sm_scale=float(sm_scale), blocks=_p(blocks), out=_p(out), lse=_p(lse))
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), _p(workspace), nbytes,
+                                         _stream(stream)), "ds_sparse_decode_blocks")
 
 
 def ds_decode_kernel_launches(shape: Shape, k: int) -> int:

@@ -4,6 +4,7 @@
 // ds_device_errors which is documented to synchronise.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "ds_sparse.h"
@@ -395,6 +396,101 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
 ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,
                            size_t workspace_bytes, ds_stream_t stream) {
   return decode_impl(shape, args, workspace, workspace_bytes, stream, nullptr);
+}
+
+// ---- block-compressed selection
+
+ds_status ds_block_compress(const ds_shape* shape, const void* index_key, int proxy_dim, const int32_t* page_table,
+                            const int32_t* seq_lens, int last_page_only, void* block_keys, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (proxy_dim != 16 && proxy_dim != 32 && proxy_dim != 64) return DS_ERR_UNSUPPORTED;
+  if (shape->batch == 0) return DS_OK;
+  if (!index_key || !page_table || !seq_lens || !block_keys) return DS_ERR_INVALID_ARG;
+  if (!aligned(index_key, 16) || !aligned(block_keys, 16)) return DS_ERR_INVALID_ARG;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  return from_cuda(launch_block_compress(index_key, page_table, seq_lens, shape->batch, proxy_dim,
+                                         shape->max_pages_per_req, shape->num_pages, last_page_only ? 1 : 0,
+                                         block_keys, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+// Workspace of the block decode: block scores, block counts, the top-k's
+// overflow lists and the expanded token lists.
+struct BlockLayout {
+  float* scores;     // [R, maxp]
+  int32_t* nblocks;  // [B]
+  TopkLayout topk;
+  int32_t* tokens;   // [R, kb * 64]
+  size_t bytes;
+};
+
+BlockLayout block_layout(const ds_shape* s, int kb, void* base) {
+  BlockLayout L;
+  char* p = static_cast<char*>(base);
+  const int R = s->batch * s->num_kv_heads;
+  const int nbm = s->max_pages_per_req;
+  size_t off = 0;
+  L.scores = reinterpret_cast<float*>(p + off);
+  off = align256(off + static_cast<size_t>(R) * nbm * 4);
+  L.nblocks = reinterpret_cast<int32_t*>(p + off);
+  off = align256(off + static_cast<size_t>(s->batch > 0 ? s->batch : 1) * 4);
+  L.topk = topk_layout(p + off, R, nbm);
+  off = align256(off + L.topk.bytes);
+  L.tokens = reinterpret_cast<int32_t*>(p + off);
+  off = align256(off + static_cast<size_t>(R) * (kb > 0 ? kb : 1) * s->page_size * 4);
+  L.bytes = off;
+  return L;
+}
+
+}  // namespace
+
+size_t ds_block_decode_workspace_bytes(const ds_shape* shape, int kb) {
+  if (check_shape(shape) != DS_OK || kb < 0) return 0;
+  return block_layout(shape, kb, nullptr).bytes;
+}
+
+ds_status ds_sparse_decode_blocks(const ds_shape* shape, const ds_block_decode_args* args, void* workspace,
+                                  size_t workspace_bytes, ds_stream_t stream) {
+  ds_status st = check_shape(shape);
+  if (st != DS_OK) return st;
+  if (!args || args->kb < 0) return DS_ERR_INVALID_ARG;
+  if (shape->batch == 0) return DS_OK;
+  const int pd = args->proxy_dim;
+  if (pd != 16 && pd != 32 && pd != 64) return DS_ERR_UNSUPPORTED;
+  if (static_cast<long long>(args->kb) * shape->page_size > 0x7fffffffLL / 2) return DS_ERR_UNSUPPORTED;
+  if (!args->qp || !args->block_keys || !args->page_table || !args->seq_lens || !args->blocks || !args->out)
+    return DS_ERR_INVALID_ARG;
+  if (!aligned(args->qp, 4) || !aligned(args->block_keys, 16) || !aligned(args->blocks, 4)) return DS_ERR_INVALID_ARG;
+  const BlockLayout L = block_layout(shape, args->kb, workspace);
+  if (!workspace || workspace_bytes < L.bytes || !aligned(workspace, 256)) return DS_ERR_WORKSPACE;
+  unsigned* err = error_word();
+  if (!err) return DS_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int kb = args->kb;
+  const int ktok = kb * shape->page_size;
+  const int nbm = shape->max_pages_per_req;
+  const int lim = static_cast<int>(std::min<long long>(shape->max_seq_len, static_cast<long long>(nbm) * shape->page_size));
+  st = from_cuda(launch_block_score(args->qp, args->block_keys, args->page_table, args->seq_lens, shape->batch,
+                                    shape->num_q_heads, shape->num_kv_heads, pd, nbm, shape->num_pages, lim, L.scores,
+                                    L.nblocks, err, s));
+  if (st != DS_OK) return st;
+  if (kb > 0) {
+    // pre_wait 0: the block counts come from the block scores' kernel.
+    TopkArgs ta{L.scores, L.nblocks, args->blocks, err, shape->batch, shape->num_kv_heads, nbm, nbm, kb, L.topk,
+                nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, 0};
+    st = from_cuda(launch_topk(ta, s));
+    if (st != DS_OK) return st;
+    st = from_cuda(launch_block_expand(args->blocks, args->seq_lens, shape->batch, shape->num_kv_heads, kb, lim,
+                                       L.tokens, s));
+    if (st != DS_OK) return st;
+  }
+  const int S = decode_splits(shape, ktok);
+  return attn_common(shape, args->q, args->k_cache, args->v_cache, args->kv_dtype, args->k_scale, args->v_scale,
+                     args->page_table, args->seq_lens, L.tokens, ktok, args->sm_scale, S, DS_SPLIT_CONTIGUOUS,
+                     nullptr, nullptr, args->out, args->lse, nullptr, nullptr, 0, S > 1 ? 1 : 0, 1, s);
 }
 
 ds_status ds_sparse_decode_profiled(const ds_shape* shape, const ds_decode_args* args, void* workspace,

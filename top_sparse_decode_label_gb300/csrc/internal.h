@@ -113,6 +113,16 @@ cudaError_t launch_cache_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_lse_merge(int S, int rows, int D, const float* o_part, const float* lse_part,
                              void* out, float* lse, cudaStream_t stream);
 
+// Block-compressed selection: compressed keys, block scores, kept blocks -> tokens.
+cudaError_t launch_block_compress(const void* keys, const int32_t* page_table, const int32_t* seq_lens, int B,
+                                  int C, int maxp, int num_pages, int last_only, void* block_keys, unsigned* err,
+                                  cudaStream_t stream);
+cudaError_t launch_block_score(const void* qp, const void* block_keys, const int32_t* page_table,
+                               const int32_t* seq_lens, int B, int Hq, int Hkv, int C, int maxp, int num_pages,
+                               int lim, float* scores, int32_t* nblocks, unsigned* err, cudaStream_t stream);
+cudaError_t launch_block_expand(const int32_t* blocks, const int32_t* seq_lens, int B, int Hkv, int kb, int lim,
+                                int32_t* idx, cudaStream_t stream);
+
 }  // namespace ds
 
 namespace ds {
