@@ -67,11 +67,19 @@ __global__ void __launch_bounds__(32) block_compress_kernel(const uint16_t* keys
   const int c = 2 * lane;
   if (c >= C) return;
   const uint32_t* rows = reinterpret_cast<const uint32_t*>(keys + static_cast<long long>(pid) * kPage * C) + lane;
+  // Rows in batches of 16 loads in flight; the sums stay in token order.
   double s0 = 0.0, s1 = 0.0;
-  for (int t = 0; t < n; ++t) {
-    const uint32_t w = __ldg(rows + static_cast<long long>(t) * (C / 2));
-    s0 += static_cast<double>(bf16_lo(w));
-    s1 += static_cast<double>(bf16_hi(w));
+  for (int t0b = 0; t0b < n; t0b += 16) {
+    uint32_t w[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) w[u] = t0b + u < n ? __ldg(rows + static_cast<long long>(t0b + u) * (C / 2)) : 0u;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (t0b + u < n) {
+        s0 += static_cast<double>(bf16_lo(w[u]));
+        s1 += static_cast<double>(bf16_hi(w[u]));
+      }
+    }
   }
   const uint32_t lo = bf16_from_double(__ddiv_rn(s0, static_cast<double>(n)));
   const uint32_t hi = bf16_from_double(__ddiv_rn(s1, static_cast<double>(n)));
