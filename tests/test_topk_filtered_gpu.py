@@ -59,6 +59,11 @@ def _scores(kind, B, H, T, seed):
         s[..., :64] += 40.0
         s[..., -1024:] += 3.0
         return s
+    if kind == "neg_inf":     # -inf everywhere but 5000 finite scores: the sample's maxima are -inf
+        s = torch.full((B, H, T), float("-inf"))
+        pos = dsgen.permutation(T, seed, 6)[:5000]
+        s[..., pos] = dsgen.normal((B, H, 5000), seed, 7, dtype=torch.float32)
+        return s
     if kind == "nan_zero":
         s = dsgen.normal((B, H, T), seed, 5, dtype=torch.float32)
         s[..., 1000:1500] = float("nan")
@@ -79,6 +84,7 @@ CASES = [
     ("increasing", 1, 2, 300000, [300000], 2048),
     ("sink_recent", 2, 2, 300000, [300000, 200000], 1500),
     ("nan_zero", 1, 2, 300000, [300000], 4000),
+    ("neg_inf", 1, 2, 300000, [300000], 2048),
 ]
 
 

@@ -312,26 +312,38 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     const int SW = ((len + kWarps - 1) / kWarps + kStep - 1) / kStep * kStep;
     const int w0 = min(s1, s0 + warp * SW), w1 = min(s1, w0 + SW);
     const int nst = (w1 - w0 + kStep - 1) / kStep;
+    // The tiles stay raw floats: order_key is monotone, so key >= lb is
+    // compared as score >= the float of key lb, and only candidates are
+    // converted.
     float4 raw[kPerF / 4];
-    uint32_t cur[kPerF];
+    float cur[kPerF];
+    auto tile_floats = [&]() {
+#pragma unroll
+      for (int i = 0; i < kPerF / 4; ++i) {
+        cur[4 * i] = raw[i].x;
+        cur[4 * i + 1] = raw[i].y;
+        cur[4 * i + 2] = raw[i].z;
+        cur[4 * i + 3] = raw[i].w;
+      }
+    };
     if (nst > 0) load_tile<kPerF / 4, 32>(s, w0, lane, w1, raw);
-    tile_keys(raw, cur);
+    tile_floats();
     // Sample: the largest key of each lane's share of the first tile. The filter bin
     // is where the sampled maxima, counted from the top, reach twice this
     // slice's share of K_eff scaled to a pass of kBatch keys (0, no filter,
     // when they never do). Fewer maxima than keys lie above any bin, so the
     // guess errs low.
     {
-      unsigned mx = 0;
+      float mx = __int_as_float(0x7fffffff);   // NaN: fmaxf keeps the other operand
       bool any = false;
 #pragma unroll
       for (int i = 0; i < kPerF; ++i) {
         if (tile_token<32>(w0, lane, i) < w1) {
-          mx = max(mx, cur[i]);
+          mx = fmaxf(mx, cur[i]);
           any = true;
         }
       }
-      warp_hist_add(S.h2, mx >> 21, any);
+      warp_hist_add(S.h2, order_key(mx) >> 21, any);
     }
     __syncthreads();
     const unsigned want =
@@ -364,12 +376,18 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     __syncthreads();
     const unsigned lbin = S.res[0];
     const uint32_t lb = lbin << 21;
+    // The smallest score whose key is lb. For bins 1..3 that float is a NaN
+    // bit pattern, while every score but NaN has a key in bin 3 or above
+    // (-inf's key is 0x007fffff): those bins, like bin 0 (no filter), take
+    // every key.
+    const float flb = __uint_as_float((lb & 0x80000000u) ? (lb & 0x7fffffffu) : ~lb);
+    const bool take_all = lbin < 4u;
     // ---- the filtered pass: the candidate list of the keys >= lb, then their digit-1 histogram
     uint2* sub = S.list + warp * kWarpCap;
     unsigned n = 0;   // this warp's candidates so far (only the first kWarpCap are kept)
     for (int st = 0; st < nst; ++st) {
       const int tb = w0 + st * kStep;
-      if (st > 0) tile_keys(raw, cur);
+      if (st > 0) tile_floats();
       if (st + 1 < nst) load_tile<kPerF / 4, 32>(s, tb + kStep, lane, w1, raw);
       // Group g of the tile (4 keys per lane) is 128 contiguous tokens, lane
       // by lane: a warp ballot per key index gives every lane the number of
@@ -381,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
         unsigned bal[4], any = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          tk[j] = cur[4 * g + j] >= lb && (full || tile_token<32>(tb, lane, 4 * g + j) < w1);
+          tk[j] = (take_all || cur[4 * g + j] >= flb) && (full || tile_token<32>(tb, lane, 4 * g + j) < w1);
           bal[j] = __ballot_sync(kFull, tk[j]);
           any |= bal[j];
         }
@@ -397,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
           for (int j = 0; j < 4; ++j) {
             if (tk[j]) {
               if (q < static_cast<unsigned>(kWarpCap))
-                sub[q] = make_uint2(cur[4 * g + j], static_cast<unsigned>(tile_token<32>(tb, lane, 4 * g + j)));
+                sub[q] = make_uint2(order_key(cur[4 * g + j]),
+                                    static_cast<unsigned>(tile_token<32>(tb, lane, 4 * g + j)));
               ++q;
             }
           }
