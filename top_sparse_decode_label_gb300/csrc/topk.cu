@@ -453,30 +453,39 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     // every list holds all keys of its slice whose first digit reaches it.
     filtered = b1 != 0xffffffffu && b1 >= lmax;
     if (filtered) {
-      // The warps' lists, concatenated in warp (= token) order.
-      if (warp == 0) {
-        const unsigned v = lane < kWarps ? S.wcnt[lane] : 0u;
-        const unsigned inc = warp_incl_scan(v);
-        if (lane < kWarps) S.woff[lane] = inc - v;
-        if (lane == 31) S.res[2] = inc;
-      }
-      __syncthreads();
-      M = S.res[2];
-      // In place, through registers: a warp's destination may cover another
-      // warp's entries, so every entry is read before any is written.
-      const unsigned o = S.woff[warp];
+      // The warps' lists, concatenated in warp (= token) order, keeping only
+      // the entries whose first digit reaches b1 (the filter bin may lie
+      // below it). In place, through registers: a warp's destination may
+      // cover another warp's entries, so every entry is read before any is
+      // written.
+      const unsigned lt = (1u << lane) - 1u;
       uint2 v[kWarpCap / 32];
+      unsigned pos[kWarpCap / 32];
+      unsigned kept = 0, keepbits = 0;
 #pragma unroll
       for (int j = 0; j < kWarpCap / 32; ++j) {
         const unsigned e = static_cast<unsigned>(j * 32 + lane);
         v[j] = e < n ? sub[e] : make_uint2(0u, 0u);
+        const bool kp = e < n && (v[j].x >> 21) >= b1;
+        const unsigned bal = __ballot_sync(kFull, kp);
+        pos[j] = kept + __popc(bal & lt);
+        kept += __popc(bal);
+        keepbits |= static_cast<unsigned>(kp) << j;
+      }
+      if (lane == 0) S.wcnt[warp] = kept;
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned c = lane < kWarps ? S.wcnt[lane] : 0u;
+        const unsigned inc = warp_incl_scan(c);
+        if (lane < kWarps) S.woff[lane] = inc - c;
+        if (lane == 31) S.res[2] = inc;
       }
       __syncthreads();
+      M = S.res[2];
+      const unsigned o = S.woff[warp];
 #pragma unroll
-      for (int j = 0; j < kWarpCap / 32; ++j) {
-        const unsigned e = static_cast<unsigned>(j * 32 + lane);
-        if (e < n) S.list[o + e] = v[j];
-      }
+      for (int j = 0; j < kWarpCap / 32; ++j)
+        if ((keepbits >> j) & 1u) S.list[o + pos[j]] = v[j];
       __syncthreads();
       // digit 2 (bits 10..20) of the candidates whose first digit is b1
       for (int e = tid; e < static_cast<int>(M); e += kThreads) {
