@@ -33,8 +33,8 @@ def _no_device_errors():
         assert _ds().ds_device_errors() == 0
 
 
-def _inputs(name, B, Hq, Hkv, T, C, kv, seed, key_range=None):
-    w = workload(name, B, Hq, Hkv, T, C, 1, 64, kv=kv, seed=seed)
+def _inputs(name, B, Hq, Hkv, T, C, kv, seed, key_range=None, head_dim=128):
+    w = workload(name, B, Hq, Hkv, T, C, 1, 64, kv=kv, seed=seed, head_dim=head_dim)
     inp = dsgen.make_inputs(w)
     if key_range is not None:      # small integer index keys: block means exact in bf16
         inp.label = dsgen.uniform_int(tuple(inp.label.shape), -key_range, key_range, seed, 77)
@@ -114,13 +114,15 @@ BLOCK_CASES = [
     ("all_blocks", 2, 8, 2, [64 * 5 + 8, 64 * 2], 32, 9, "bf16"),     # kb above the block count: dense
     ("one_block", 2, 16, 2, [64 * 30, 4], 64, 1, "fp8_e4m3"),
     ("empty_row", 2, 8, 1, [0, 64 * 7 + 2], 16, 3, "bf16"),
+    ("qsa_d256_fp8", 2, 16, 2, [64 * 30 + 16, 64 * 9], 64, 5, "fp8_e4m3", 256),
 ]
 
 
 @pytest.mark.parametrize("case", BLOCK_CASES, ids=[c[0] for c in BLOCK_CASES])
 def test_block_decode_matches_the_oracle(case):
-    name, B, Hq, Hkv, T, C, kb, kv = case
-    w, inp = _inputs(name, B, Hq, Hkv, T, C, kv, 31, key_range=2)
+    name, B, Hq, Hkv, T, C, kb, kv = case[:8]
+    D = case[8] if len(case) > 8 else 128
+    w, inp = _inputs(name, B, Hq, Hkv, T, C, kv, 31, key_range=2, head_dim=D)
     bk = oracle.block_compress(inp.label, inp.page_table, inp.seq_lens, inp.num_pages)
     blocks, out, lse = _decode_blocks(inp, bk, kb)
     _, rblocks, rout, rlse = _reference(inp, bk, kb)
@@ -189,3 +191,42 @@ def test_block_decode_at_the_qsa_1m_shape_sampled():
     scores = oracle.block_score(inp.qp, bkc, inp.page_table, inp.seq_lens, w.num_kv_heads)
     rblocks = oracle.topk(scores, torch.tensor([w.seq_lens[0] // P], dtype=torch.int32), 32)
     _assert_valid_top_k(blocks, rblocks, scores)
+
+
+def test_block_decode_replays_in_a_cuda_graph_with_new_inputs():
+    # No host synchronisation and no allocation: the block-level step is captured once and replayed after
+    # the caches and queries change in place; each replay matches the oracle on the new contents.
+    ds = _ds()
+    kb = 6
+    wa, a = _inputs("graph", 2, 32, 4, [64 * 50, 64 * 21 + 8], 64, "bf16", 51, key_range=2)
+    _, b_ = _inputs("graph", 2, 32, 4, [64 * 50, 64 * 21 + 8], 64, "bf16", 52, key_range=2)
+    g = a.to(DEV)
+    shape = shape_of(a)
+    bk = torch.zeros((a.num_pages, 64), dtype=torch.bfloat16, device=DEV)
+    blocks = torch.empty((wa.batch, wa.num_kv_heads, kb), dtype=torch.int32, device=DEV)
+    out = torch.empty((wa.batch, wa.num_q_heads, 128), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((wa.batch, wa.num_q_heads), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ds.ds_block_decode_workspace_bytes(shape, kb), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+
+    def step():
+        ds.ds_block_compress(shape, g.label, g.page_table, g.seq_lens, bk, stream=stream)
+        ds.ds_sparse_decode_blocks(shape, g.q, g.qp, bk, g.k_cache, g.v_cache, None, None, g.page_table,
+                                   g.seq_lens, kb, blocks, out, lse, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()                       # warm-up outside the capture (sets kernel attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for src in (a, b_, a):
+        for name in ("q", "qp", "label", "k_cache", "v_cache", "page_table"):
+            getattr(g, name).copy_(getattr(src, name).to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        bkr = oracle.block_compress(src.label, src.page_table, src.seq_lens, src.num_pages)
+        assert torch.equal(bk.cpu().view(torch.int16), bkr.view(torch.int16))
+        _, rblocks, rout, rlse = _reference(src, bkr, kb)
+        assert torch.equal(blocks.cpu(), rblocks)
+        assert_close(out, rout, atol_for(wa), "graph replay out")
