@@ -105,3 +105,27 @@ def test_binding_exports_every_name_it_lists():
     import top_sparse_decode_label_gb300 as ds
     for n in ds.__all__:
         assert hasattr(ds, n), n
+
+
+def test_block_path_host_validation_without_a_gpu():
+    import top_sparse_decode_label_gb300 as ds
+    L = ds.lib()
+    P = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    shape = _shape(max_seq_len=256)
+    # Proxy width 24 is not implemented; null pointers are rejected.
+    assert L.ds_block_compress(ctypes.byref(shape), P, 24, P, P, 0, P, None) == -2
+    assert L.ds_block_compress(ctypes.byref(shape), None, 64, P, P, 0, P, None) == -1
+    assert L.ds_block_compress(ctypes.byref(shape), P, 64, P, P, 0, None, None) == -1
+    # The block decode: null args, negative kb, a workspace below the query's size.
+    assert L.ds_sparse_decode_blocks(ctypes.byref(shape), None, P, 1 << 20, None) == -1
+    a = ds.BlockDecodeArgs(q=16, qp=16, proxy_dim=64, block_keys=16, k_cache=16, v_cache=16, kv_dtype=0,
+                           page_table=16, seq_lens=16, kb=-1, sm_scale=0.1, blocks=16, out=16)
+    assert L.ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), P, 1 << 20, None) == -1
+    a.kb = 4
+    need = ds.ds_block_decode_workspace_bytes(shape, 4)
+    assert need > 0 and need % 256 == 0
+    assert need > ds.ds_block_decode_workspace_bytes(shape, 1)
+    ws = ctypes.c_void_p(256 * 1024)
+    assert L.ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), ws, need - 1, None) == -4
+    a.proxy_dim = 48
+    assert L.ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), ws, need, None) == -2
