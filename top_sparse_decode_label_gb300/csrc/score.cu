@@ -14,9 +14,9 @@
 // rows (HL*C*2 bytes each) of one request. A persistent grid takes the units
 // in chunks of consecutive units: with a work counter (chained call) each
 // CTA's first chunk is fixed and later ones are claimed with one atomicAdd, a
-// chunk ahead, so faster CTAs take more work and all CTAs finish together
-// (the last CTA to finish rearms the counter); without one each CTA takes a
-// contiguous range. In each CTA a producer warp loads the page ids of a
+// chunk ahead, so faster CTAs take more work; the last two units per CTA go
+// out one at a time, so all CTAs finish together (the last CTA to finish
+// rearms the counter); without a counter each CTA takes a contiguous range. In each CTA a producer warp loads the page ids of a
 // chunk's pages together, a chunk before they are needed, and streams the
 // units into a ring of shared-memory stages with bulk copies -- one per page
 // span -- that complete on the stage's mbarrier; eight consumer warps wait on
@@ -145,17 +145,17 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         su = e;
       }
     };
-    auto claim = [&]() -> int {   // dynamic: counter value (lane 0), resolved later
+    auto claim = [&](int sz) -> int {   // dynamic: counter value (lane 0), resolved later
       int base = 0;
-      if (p.work && lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(kChunkUnits)));
+      if (p.work && lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(sz)));
       return base;
     };
-    auto resolve = [&](int claimed, int& a, int& e) {
+    auto resolve = [&](int claimed, int sz, int& a, int& e) {
       if (p.work) {
         const long long base = static_cast<long long>(__shfl_sync(kFull, claimed, 0)) +
                                static_cast<long long>(gridDim.x) * kChunkUnits;
         a = static_cast<int>(base < p.units ? base : p.units);
-        e = min(p.units, a + kChunkUnits);
+        e = min(p.units, a + sz);
       } else {
         a = su;
         e = min(u1, su + kChunkUnits);
@@ -176,12 +176,17 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
     };
     int cu = 0, ce = 0, na = 0, ne = 0;
     first_chunk(cu, ce);
-    int claimed = claim();
+    // Near the end of the work, claims shrink to single units so that the
+    // CTAs finish together.
+    const int tail = 2 * static_cast<int>(gridDim.x);
+    int csz = kChunkUnits;
+    int claimed = claim(csz);
     int cpid = load_pids(cu, ce);
-    resolve(claimed, na, ne);
+    resolve(claimed, csz, na, ne);
     int npid = load_pids(na, ne);
     int ca = cu;          // first unit of the current chunk
-    claimed = claim();    // the chunk after next
+    csz = p.units - na > tail ? kChunkUnits : 1;
+    claimed = claim(csz);    // the chunk after next
     int s = 0;
     uint32_t fill = 0;  // how many times stage s has been filled before
     for (;;) {
@@ -192,9 +197,10 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         ce = ne;
         ca = cu;
         cpid = npid;
-        resolve(claimed, na, ne);
+        resolve(claimed, csz, na, ne);
         npid = load_pids(na, ne);
-        claimed = claim();
+        csz = p.units - na > tail ? kChunkUnits : 1;
+        claimed = claim(csz);
       }
       const int unit = cu < ce ? cu++ : -1;
       if (fill > 0 && !mbar_wait(&empty_bar[s], (fill - 1) & 1u, kWaitLimit) && lane == 0)
