@@ -341,7 +341,7 @@ typedef struct ds_block_decode_args {
   const int32_t* seq_lens;   /* int32 [B] */
   int kb;                    /* blocks kept per (request, KV head) */
   float sm_scale;
-  int32_t* blocks;           /* out: int32 [B, Hkv, kb] kept blocks, ascending, -1 padded */
+  int32_t* blocks;           /* out: int32 [B, Hkv, kb] kept blocks, ascending, -1 padded (NULL when kb = 0) */
   void* out;                 /* out: bf16 [B, Hq, D] */
   float* lse;                /* out: fp32 [B, Hq] (may be NULL) */
 } ds_block_decode_args;

@@ -230,3 +230,37 @@ def test_block_decode_replays_in_a_cuda_graph_with_new_inputs():
         _, rblocks, rout, rlse = _reference(src, bkr, kb)
         assert torch.equal(blocks.cpu(), rblocks)
         assert_close(out, rout, atol_for(wa), "graph replay out")
+
+
+def test_append_then_last_page_compress_equals_a_full_compress():
+    # The maintenance sequence a decoder runs per step: append each request's new token (its index key
+    # included), then refresh only the page that changed; the compressed cache must equal a full rebuild.
+    ds = _ds()
+    w, inp = _inputs("append_blocks", 3, 32, 4, [64 * 9 + 10, 64 * 3, 64 * 20 - 1], 64, "fp8_e4m3", 61)
+    g = inp.to(DEV)
+    shape = shape_of(inp)
+    bk = torch.zeros((inp.num_pages, 64), dtype=torch.bfloat16, device=DEV)
+    ds.ds_block_compress(shape, g.label, g.page_table, g.seq_lens, bk)
+    pos = torch.tensor([64 * 9 + 10, 64 * 3 - 1, 64 * 20 - 1], dtype=torch.int32)   # next token, last token, last
+    k_new = dsgen.normal((w.batch, w.num_kv_heads, 128), 61, 101)
+    v_new = dsgen.normal((w.batch, w.num_kv_heads, 128), 61, 102)
+    ikey = dsgen.uniform_int((w.batch, 64), -2, 2, 61, 103)
+    ds.ds_cache_append(shape, k_new.to(DEV), v_new.to(DEV), g.k_cache, g.v_cache, g.k_scale, g.v_scale,
+                       g.page_table, pos.to(DEV), label=g.label, index_key=ikey.to(DEV))
+    seq = torch.maximum(inp.seq_lens, pos + 1).to(torch.int32)
+    g.seq_lens.copy_(seq.to(DEV))
+    ds.ds_block_compress(shape, g.label, g.page_table, g.seq_lens, bk, last_page_only=True)
+    full = torch.zeros_like(bk)
+    ds.ds_block_compress(shape, g.label, g.page_table, g.seq_lens, full)
+    torch.cuda.synchronize()
+    assert torch.equal(bk.view(torch.int16), full.view(torch.int16))
+    ref = oracle.block_compress(g.label.cpu(), inp.page_table, seq, inp.num_pages)
+    assert torch.equal(bk.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_block_decode_with_no_kept_blocks_is_an_empty_attention():
+    w, inp = _inputs("kb0", 2, 8, 2, [64 * 4, 64 * 2], 32, "bf16", 71, key_range=2)
+    bk = oracle.block_compress(inp.label, inp.page_table, inp.seq_lens, inp.num_pages)
+    blocks, out, lse = _decode_blocks(inp, bk, 0)
+    assert blocks.numel() == 0
+    assert (out.float() == 0).all() and torch.isinf(lse).all() and (lse < 0).all()

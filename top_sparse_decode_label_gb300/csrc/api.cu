@@ -461,7 +461,8 @@ ds_status ds_sparse_decode_blocks(const ds_shape* shape, const ds_block_decode_a
   const int pd = args->proxy_dim;
   if (pd != 16 && pd != 32 && pd != 64) return DS_ERR_UNSUPPORTED;
   if (static_cast<long long>(args->kb) * shape->page_size > 0x7fffffffLL / 2) return DS_ERR_UNSUPPORTED;
-  if (!args->qp || !args->block_keys || !args->page_table || !args->seq_lens || !args->blocks || !args->out)
+  if (!args->qp || !args->block_keys || !args->page_table || !args->seq_lens || (args->kb > 0 && !args->blocks) ||
+      !args->out)
     return DS_ERR_INVALID_ARG;
   if (!aligned(args->qp, 4) || !aligned(args->block_keys, 16) || !aligned(args->blocks, 4)) return DS_ERR_INVALID_ARG;
   const BlockLayout L = block_layout(shape, args->kb, workspace);
