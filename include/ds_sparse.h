@@ -50,7 +50,7 @@ typedef struct CUstream_st* ds_stream_t;
 typedef enum {
   DS_OK = 0,
   DS_ERR_INVALID_ARG = -1,   /* null pointer, negative size, misaligned pointer, too-small buffer */
-  DS_ERR_UNSUPPORTED = -2,   /* a size this build does not implement (head_dim, page_size, group, ...) */
+  DS_ERR_UNSUPPORTED = -2,   /* a size this library does not implement (head_dim, page_size, group, ...) */
   DS_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
   DS_ERR_WORKSPACE = -4,     /* workspace too small (see the *_workspace_bytes queries) */
   DS_ERR_DEVICE_CHECK = -5   /* ds_device_errors found a flagged element */
@@ -75,9 +75,9 @@ typedef struct {
   int batch;             /* B, requests in the step (>= 0) */
   int num_q_heads;       /* Hq, a multiple of num_kv_heads; Hq / Hkv in {1, 2, 4, 8} */
   int num_kv_heads;      /* Hkv (>= 1) */
-  int head_dim;          /* D; this build supports 128 and 256 (the QSA model's shape on Blackwell,
+  int head_dim;          /* D; the library supports 128 and 256 (the QSA model's shape on Blackwell,
                             sglang PR #43527 review thread: BF16 queries, head dimension 256) */
-  int page_size;         /* P; this build supports 64 */
+  int page_size;         /* P; the library supports 64 */
   int max_pages_per_req; /* row stride of page_table (>= 1) */
   int num_pages;         /* physical pages in the pool; valid page ids are [0, num_pages) */
   int max_seq_len;       /* Tmax, row stride of the score buffer; every seq_lens[b] must be <= it */

@@ -107,7 +107,7 @@ const char* ds_error_string(ds_status status) {
   switch (status) {
     case DS_OK: return "DS_OK";
     case DS_ERR_INVALID_ARG: return "DS_ERR_INVALID_ARG: null, negative, misaligned or inconsistent argument";
-    case DS_ERR_UNSUPPORTED: return "DS_ERR_UNSUPPORTED: size not implemented by this build";
+    case DS_ERR_UNSUPPORTED: return "DS_ERR_UNSUPPORTED: size not implemented by this library";
     case DS_ERR_CUDA: return "DS_ERR_CUDA: a CUDA runtime call or kernel launch failed";
     case DS_ERR_WORKSPACE: return "DS_ERR_WORKSPACE: workspace too small or misaligned";
     case DS_ERR_DEVICE_CHECK: return "DS_ERR_DEVICE_CHECK: a kernel flagged an out-of-range element";
