@@ -8,6 +8,7 @@ import os
 import socket
 import sys
 
+import torch
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -63,3 +64,30 @@ def test_two_gloo_ranks_agree_on_the_slowest_time_and_only_rank0_prints():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["unit"] == "calls/s"
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["config"]["workload"] == "tiny_ds_b1_h4_t4096_c16_k256"
+
+
+def test_oracle_rows_on_several_threads_match_one_thread():
+    # The CPU baseline runs the oracle on (request, KV head) rows from several
+    # host threads at once: each row's result must not depend on that.
+    from concurrent.futures import ThreadPoolExecutor
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import dsgen
+    import oracle
+
+    w = dsgen.WORKLOADS[0].scaled(batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[700, 1500], top_k=64,
+                                  name="threads")
+    inp = dsgen.make_inputs(w, device="cpu")
+    masks = bench.row_masks(w)
+    assert len(masks) == 4 and all(int(m.sum()) == 1 for m in masks)
+    one = [oracle.decode(inp, row_mask=m) for m in masks]
+    with ThreadPoolExecutor(4) as ex:
+        many = list(ex.map(lambda m: oracle.decode(inp, row_mask=m), masks * 3))
+    for i, got in enumerate(many):
+        want = one[i % 4]
+        b, g = divmod(i % 4, 2)
+        assert torch.equal(got[1][b, g], want[1][b, g])
+        assert torch.equal(got[2][b, g * 4:(g + 1) * 4], want[2][b, g * 4:(g + 1) * 4])
+    rate, n = bench.oracle_rows(inp, 60.0, 3, max_rows=7)
+    assert n == 7 and rate > 0
