@@ -24,6 +24,9 @@
  *  - Calls are asynchronous on `stream` and never synchronise the host.
  *    Arguments are validated on the host before any launch; a call that
  *    returns an error has launched nothing.
+ *  - Make calls from one host thread at a time: the entry points set kernel
+ *    attributes and cache device queries (SM count, resident clusters) in
+ *    process-wide tables without a lock.
  *  - Problems the host cannot see (a seq_len, page id or token index outside
  *    its range) never cause an out-of-bounds access: the kernel skips the bad
  *    element and sets a bit in a sticky device error word, read back with
