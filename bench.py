@@ -108,6 +108,15 @@ def traffic_record(kernel_file: str, workload: str):
     return None
 
 
+def step_percentiles(step_ms) -> dict:
+    """Median and 10th / 90th percentiles (nearest rank) of this rank's event-timed steps, in µs."""
+    xs = sorted(step_ms)
+    if not xs:
+        return {"p10": None, "p50": None, "p90": None}
+    at = lambda q: xs[min(len(xs) - 1, max(0, math.ceil(q * len(xs)) - 1))] * 1e3
+    return {"p10": at(0.10), "p50": at(0.50), "p90": at(0.90)}
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -400,6 +409,7 @@ def run_ours(args):
     clocks = sampler.summary(t_wall0, t_wall1)
     if ds.ds_device_errors() != 0:
         raise RuntimeError("device error word set during the timed region")
+    step_spread = step_percentiles(step_ms)
 
     # ---- per-stage breakdown: the same chained call, with events recorded between its stages.
     S = ds.ds_decode_num_splits(shape, k)
@@ -604,7 +614,8 @@ def run_ours(args):
 
     line = {
         "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "step_us": step_spread, "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w, world, args.flush_mib),
         "tokens_per_s": calls_per_s * B, "scanned_tokens_per_s": calls_per_s * sum(w.seq_lens),

@@ -91,3 +91,12 @@ def test_oracle_rows_on_several_threads_match_one_thread():
         assert torch.equal(got[2][b, g * 4:(g + 1) * 4], want[2][b, g * 4:(g + 1) * 4])
     rate, n = bench.oracle_rows(inp, 60.0, 3, max_rows=7)
     assert n == 7 and rate > 0
+
+
+def test_step_percentiles_nearest_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    got = bench.step_percentiles([0.07, 0.05, 0.06, 0.052, 0.055])
+    assert got == {"p10": 50.0, "p50": 55.0, "p90": 70.0}
+    assert bench.step_percentiles([0.1]) == {"p10": 100.0, "p50": 100.0, "p90": 100.0}
+    assert bench.step_percentiles([])["p50"] is None
