@@ -22,7 +22,15 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/liboracle.so`` (no CUDA involved)."""
+    """Compile the oracle into ``oracle/liboracle.so`` (no CUDA involved).
+
+    With ``DS_ORACLE_LIB`` set, that prebuilt library is used instead: the
+    planted-mistake tests load a deliberately altered copy of the oracle this
+    way to show that the pins reject it.
+    """
+    override = os.environ.get("DS_ORACLE_LIB")
+    if override:
+        return override
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         cxx = os.environ.get("CXX", "g++")
         tmp = _LIB_PATH + f".tmp{os.getpid()}"

@@ -366,6 +366,44 @@ def test_merge_of_any_split_equals_the_unsplit_result(S, split_mode):
     assert torch.allclose(lse, lse1, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("S,split_mode", [(3, 0), (7, 0), (4, 1), (5, 1)])
+def test_each_split_chunk_is_attention_over_its_own_tokens(S, split_mode):
+    # Reading R6 fixes which selected tokens each chunk holds: contiguous
+    # splitting gives chunk j the positions [j n / S, (j + 1) n / S) of the n
+    # selected tokens, page-interleaved splitting the tokens whose logical page
+    # is j mod S. Each chunk's partial must be library attention over exactly
+    # those tokens, and a chunk without tokens has o = 0 and lse = -inf. (The
+    # merge test above cannot see a wrong assignment: any partition merges to
+    # the same result.)
+    w = _small_workload("bf16", T=(700, 45), k=90)
+    inp = dsgen.make_inputs(w)
+    _, idx, _, _ = oracle.decode(inp)
+    o, l = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
+                              inp.page_table, inp.seq_lens, idx, None, S, split_mode)
+    Kd = _dequant(inp, inp.k_cache, inp.k_scale)
+    Vd = _dequant(inp, inp.v_cache, inp.v_scale)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    empty = 0
+    for b in range(w.batch):
+        for h in range(w.num_q_heads):
+            g = h // w.group
+            sel = idx[b, g][idx[b, g] >= 0].long()
+            n = len(sel)
+            for j in range(S):
+                mine = sel[j * n // S:(j + 1) * n // S] if split_mode == 0 else sel[(sel // P) % S == j]
+                if len(mine) == 0:
+                    empty += 1
+                    assert torch.equal(o[j, b, h], torch.zeros_like(o[j, b, h]))
+                    assert math.isinf(float(l[j, b, h])) and float(l[j, b, h]) < 0
+                    continue
+                slots = inp.page_table[b, mine // P].long() * P + mine % P
+                o_ref, lse_ref = _sdpa_rows(inp.q[b, h].double(), Kd[slots, g], Vd[slots, g], scale)
+                assert torch.allclose(o[j, b, h], o_ref, rtol=0, atol=1e-12), (b, h, j)
+                assert abs(float(l[j, b, h]) - float(lse_ref)) < 1e-12, (b, h, j)
+    if split_mode == 1:
+        assert empty > 0          # the 45-token request has one page: every other chunk is empty
+
+
 def test_merge_closed_form_two_partials():
     # lse_1 = 0, lse_2 = ln 3: total lse = ln 4, weights 1/4 and 3/4.
     o = torch.tensor([[[1.0, 0.0]], [[0.0, 2.0]]], dtype=torch.float64)
