@@ -348,9 +348,12 @@ def _sample_rows(w, n=2):
     return rows
 
 
-@pytest.mark.parametrize("ci", [1, 2, 3, 4])
-def test_full_size_workload_sampled_rows(ci):
+@pytest.mark.parametrize("ci,D", [(1, 128), (2, 128), (3, 128), (4, 128), (1, 256), (3, 256)])
+def test_full_size_workload_sampled_rows(ci, D):
+    # Head dimension 256: the Llama-8B DS and QSA shapes as `bench.py --head-dim 256` times them.
     w = dsgen.WORKLOADS[ci]
+    if D != w.head_dim:
+        w = w.scaled(head_dim=D, name=f"{w.name}_d{D}")
     g = dsgen.make_inputs(w, device=DEV)
     shape = ds_shape = shape_of(g)
     idx, out, lse = run_decode(g, ds_shape, w.top_k)
@@ -382,7 +385,7 @@ def test_full_size_workload_sampled_rows(ci):
         # Split-KV over 4 and 16 chunks, merged, equals the unsplit result.
         ds = _ds()
         for S in (4, 16):
-            o_part = torch.empty((S, w.batch, w.num_q_heads, 128), device=DEV)
+            o_part = torch.empty((S, w.batch, w.num_q_heads, w.head_dim), device=DEV)
             l_part = torch.empty((S, w.batch, w.num_q_heads), device=DEV)
             ds.ds_sparse_decode_attn(shape, g.q, g.k_cache, g.v_cache, g.k_scale, g.v_scale, g.page_table,
                                      g.seq_lens, idx, num_splits=S, o_part=o_part, lse_part=l_part)
