@@ -278,7 +278,7 @@ def _fp8_pages(slots, H, D, scale, seed, tid, device, P):
     for s in range(0, slots, rows_per_chunk):
         e = min(slots, s + rows_per_chunk)
         x = _normal_at(seed, tid, s * H * D, (e - s, H, D), device)
-        sc =scale[torch.arange(s, e, device=device) // P].view(-1, 1, 1)
+        sc = scale[torch.arange(s, e, device=device) // P].view(-1, 1, 1)
         y = torch.clamp(x / sc, -448.0, 448.0)
         out[s:e] = y.to(torch.float8_e4m3fn).view(torch.uint8)
     return out
