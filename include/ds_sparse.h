@@ -21,7 +21,8 @@
  * Conventions for every entry point:
  *  - All pointers are DEVICE pointers on the current device unless stated.
  *    The caller owns all memory; the library never allocates or frees.
- *  - Calls are asynchronous on `stream` and never synchronise the host.
+ *  - Calls are asynchronous on `stream` and never synchronise the host
+ *    (ds_device_errors, the explicit check, is the one exception).
  *    Arguments are validated on the host before any launch; a call that
  *    returns an error has launched nothing.
  *  - Make calls from one host thread at a time: the entry points set kernel
