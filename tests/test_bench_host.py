@@ -100,3 +100,23 @@ def test_step_percentiles_nearest_rank():
     assert got == {"p10": 50.0, "p50": 55.0, "p90": 70.0}
     assert bench.step_percentiles([0.1]) == {"p10": 100.0, "p50": 100.0, "p90": 100.0}
     assert bench.step_percentiles([])["p50"] is None
+
+
+def test_algorithmic_bytes_are_the_workloads_byte_counts():
+    # Per call: the label / index rows scanned (B * T * label heads * C * 2) and the selected K and V rows
+    # (B * Hkv * k * D * element size * 2), worked out by hand from each workload's shape.
+    sys.path.insert(0, ROOT)
+    import bench
+    import dsgen
+    want = {
+        "llama8b_ds_b3_h32kv8_t60000_c32_k3000": (92_160_000, 36_864_000, 0),
+        "longchat7b_ds_b3_h32kv32_t20000_c16_k1024": (61_440_000, 50_331_648, 0),
+        "qsa_b8_h32kv4_t262144_idx64_k2048_fp8": (268_435_456, 16_777_216, 8 * 4 * 2048 * 8),
+        "qsa_1m_b1_h32kv4_t1048576_idx64_k2048_fp8": (134_217_728, 2_097_152, 1 * 4 * 2048 * 8),
+    }
+    for w in dsgen.WORKLOADS[1:]:
+        scan, kv, scales = want[w.name]
+        ab = bench.alg_bytes(w)
+        assert ab["scan"] == scan and ab["kv_rows"] == kv + scales, w.name
+        assert ab["page_table"] == w.batch * -(-w.seq_lens[0] // 64) * 4
+        assert ab["total"] == sum(v for key, v in ab.items() if key != "total")
