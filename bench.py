@@ -4,16 +4,19 @@
 A step is one call of the chained C entry point ds_sparse_decode (score every
 cached token -> exact top-k -> sparse GQA attention over the selected tokens ->
 log-sum-exp merge) over one batch of seeded synthetic inputs that are already
-resident in HBM. The default workload is the Llama-3.1-8B-shaped
-Double-Sparsity decode (batch 3, 32 query / 8 KV heads, 60000 tokens per
-request, 32 K-channel label cache, top-k 3000, bf16 KV); --config selects
-another one of dsgen.WORKLOADS.
+resident in HBM. The headline workload is the largest one, the QSA-shaped
+decode (batch 8, 32 query / 4 KV heads, 262,144 tokens per request, 64-wide
+index keys, top-k 2048, FP8 E4M3 paged KV); --config selects another one of
+dsgen.WORKLOADS. The Llama-3.1-8B- and longchat-7b-shaped Double-Sparsity
+workloads and the 1M-token QSA request (--also) are measured in the same run,
+with the same steps and warm-up, into `per_config`.
 
 Printed: one JSON line with calls/s (value), the achieved HBM bandwidth of the
-step and of its dominant kernel against the measured copy bandwidth, the
-end-to-end number through the C ABI with host<->device copies, the oracle's CPU
-time on a bounded sample, clocks sampled during the timed region, and the
-number of kernel launches.
+step against the nominal 8 TB/s and against the measured copy bandwidth, the
+dominant kernel's roofline, the end-to-end number through the C ABI with
+host<->device copies, the oracle's CPU time on a bounded sample, clocks
+sampled during the timed region, and the number of kernel launches; the same
+fields for every workload of `per_config`.
 
 Timing: W untimed warm-up steps, then exactly K timed steps; L2 is flushed
 before every timed step (a 256 MiB device write, then a 256 MiB read so the
@@ -49,6 +52,9 @@ import dsgen  # noqa: E402
 
 METRIC = "sparse-decode attn calls/s + achieved HBM GB/s vs ~8 TB/s roofline, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
+# The nominal HBM3e bandwidth of one GB300 that the decode step's roofline
+# fraction is stated against; the measured copy bandwidth is reported beside it.
+NOMINAL_HBM_GBS = 8000.0
 
 
 def parse_args():
@@ -57,7 +63,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, help="index into dsgen.WORKLOADS")
+    ap.add_argument("--config", type=int, default=3,
+                    help="headline workload, an index into dsgen.WORKLOADS (default: the QSA b8 x 262,144 "
+                         "FP8 workload, the largest)")
+    ap.add_argument("--also", default="1,2,4",
+                    help="comma-separated further workloads measured in the same run into `per_config` "
+                         "('' for none)")
     ap.add_argument("--head-dim", type=int, default=None, help="override the workload's head dimension (128, 256)")
     ap.add_argument("--flush-mib", type=int, default=256)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle time budget of the CPU baseline")
@@ -205,12 +216,17 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def workload_of(args) -> dsgen.Workload:
-    """The workload of --config, with --head-dim applied (its name then says so)."""
-    w = dsgen.WORKLOADS[args.config]
+def workload_of(args, config: int = None) -> dsgen.Workload:
+    """Workload `config` (default --config), with --head-dim applied (its name then says so)."""
+    w = dsgen.WORKLOADS[args.config if config is None else config]
     if args.head_dim is not None and args.head_dim != w.head_dim:
         w = w.scaled(head_dim=args.head_dim, name=f"{w.name}_d{args.head_dim}")
     return w
+
+
+def also_configs(args):
+    """The workload indices of --also."""
+    return [int(x) for x in args.also.split(",") if x.strip() != ""]
 
 
 def workload_config(w: dsgen.Workload, world: int, flush_mib: int) -> dict:
@@ -334,56 +350,59 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+class _Device:
+    """What every measured workload shares: the device, its stream, the L2 flush and the clock sampler."""
+
+    def __init__(self, args):
+        self.world, self.rank, local = dist_setup(args.gpus)
+        self.dev = torch.device("cuda", local)
+        torch.cuda.set_device(self.dev)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.flush_w = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=self.dev)
+        self.flush_r = torch.zeros(args.flush_mib << 20, dtype=torch.uint8, device=self.dev)
+        self.flush_sink = torch.empty((), dtype=torch.int64, device=self.dev)
+        props = torch.cuda.get_device_properties(self.dev)
+        gpu_id = "GPU-" + str(props.uuid) if getattr(props, "uuid", None) is not None else str(local)
+        self.sampler = ClockSampler(gpu_id)
+
+    def flush(self):
+        # Evicts L2: a write of flush_w, then a read of flush_r so that the
+        # dirty lines of the write are written back before the timed region.
+        self.flush_w.zero_()
+        torch.sum(self.flush_r, dim=0, dtype=torch.int64, out=self.flush_sink)
+
+
+def measure(d: _Device, w: dsgen.Workload, args, extras: bool) -> dict:
+    """Times the chained call on one workload; returns its fields of the JSON line."""
     import top_sparse_decode_label_gb300 as ds
 
-    world, rank, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = workload_of(args)
+    dev, stream, world = d.dev, d.stream, d.world
     inp = dsgen.make_inputs(w, device=dev)
     shape = ds.Shape(**dsgen.shape_kwargs(inp))
     k = w.top_k
     B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
-    stream = torch.cuda.current_stream(dev)
 
     idx = torch.empty((B, Hkv, k), dtype=torch.int32, device=dev)
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     ws = torch.zeros(ds.ds_decode_workspace_bytes(shape, w.proxy_dim, k), dtype=torch.uint8, device=dev)
-    flush_w = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
-    flush_r = torch.zeros(args.flush_mib << 20, dtype=torch.uint8, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
-
-    class _Flush:
-        # Evicts L2: a write of flush_w, then a read of flush_r so that the
-        # dirty lines of the write are written back before the timed region.
-        @staticmethod
-        def zero_():
-            flush_w.zero_()
-            torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
-
-    flush = _Flush()
 
     def step():
         ds.ds_sparse_decode(shape, inp.q, inp.qp, inp.label, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
                             inp.page_table, inp.seq_lens, k, idx, out, lse, ws, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        d.flush()
         step()
     torch.cuda.synchronize()
     if ds.ds_device_errors() != 0:
-        raise RuntimeError("device error word set during warm-up")
+        raise RuntimeError(f"{w.name}: device error word set during warm-up")
 
-    props = torch.cuda.get_device_properties(dev)
-    gpu_id = "GPU-" + str(props.uuid) if getattr(props, "uuid", None) is not None else str(local)
-    sampler = ClockSampler(gpu_id)
     # Untimed soak so that the clock record covers the timed region even when it is short.
     t_soak = time.time()
     while time.time() - t_soak < 1.0:
         for _ in range(50):
-            flush.zero_()
+            d.flush()
             step()
         torch.cuda.synchronize()
 
@@ -394,21 +413,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        d.flush()
         ev0[i].record(stream)
         step()
         ev1[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
-    sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
     calls_per_s = world * args.steps / total_s
     ms_per_step = total_s / args.steps * 1e3
-    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks = d.sampler.summary(t_wall0, t_wall1)
     if ds.ds_device_errors() != 0:
-        raise RuntimeError("device error word set during the timed region")
+        raise RuntimeError(f"{w.name}: device error word set during the timed region")
     step_spread = step_percentiles(step_ms)
 
     # ---- per-stage breakdown: the same chained call, with events recorded between its stages.
@@ -420,7 +438,7 @@ def run_ours(args):
             e.record(stream)  # creates the underlying event handles
     torch.cuda.synchronize()
     for i in range(nstage):
-        flush.zero_()
+        d.flush()
         ds.ds_sparse_decode(shape, inp.q, inp.qp, inp.label, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
                             inp.page_table, inp.seq_lens, k, idx, out, lse, ws, stream=stream, events=evs[i])
     torch.cuda.synchronize()
@@ -431,7 +449,9 @@ def run_ours(args):
     # A caller stages one step's inputs (q, qp, page table, sequence lengths)
     # in one pinned host buffer and the call's outputs (out, lse, idx) in one
     # device buffer, so each direction is a single copy; the library takes
-    # views into them like any other device pointers.
+    # views into them like any other device pointers. The read-back includes
+    # the selected indices (B * Hkv * k int32) as well as out and lse: a caller
+    # that needs only the attention output would copy less.
     def packed(tensors):
         nbytes = [t.numel() * t.element_size() for t in tensors]
         offs, o = [], 0
@@ -457,13 +477,12 @@ def run_ours(args):
         view(h_in, o, t).copy_(t.cpu())
     e_q, e_qp, e_pt, e_sl = (view(d_in, o, t) for t, o in zip(in_src, in_offs))
     e_out, e_lse, e_idx = (view(d_out, o, t) for t, o in zip(out_src, out_offs))
-    h2d, d2h = in_bytes, out_bytes
     ee0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ee1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.zero_()
+        d.flush()
         ee0[i].record(stream)
         d_in.copy_(h_in, non_blocking=True)
         ds.ds_sparse_decode(shape, e_q, e_qp, inp.label, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
@@ -475,8 +494,84 @@ def run_ours(args):
     e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(ee0, ee1)) / 1e3, world)
     e2e_value = world * args.steps / e2e_s
     if not torch.equal(view(h_out, out_offs[2], idx), idx.cpu()):
-        raise RuntimeError("the end-to-end call's indices differ from the device-resident call's")
+        raise RuntimeError(f"{w.name}: the end-to-end call's indices differ from the device-resident call's")
 
+    rec = {}
+    if extras:
+        rec.update(measure_extras(d, w, inp, shape, args))
+
+    # ---- roofline: the step against HBM, and its dominant kernel
+    peak, peak_src = measured_peak()
+    ab = alg_bytes(w)
+    step_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
+    dominant = max(stage_us, key=stage_us.get)
+    dom_bytes, dom_file = stage_bytes(w, dominant)
+    dom_gbs = dom_bytes / (stage_us[dominant] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                "frac": dom_gbs / peak, "frac_of_8000_gbs": dom_gbs / NOMINAL_HBM_GBS,
+                "traffic": traffic_record(dom_file, w.name),
+                "alg_bytes_per_launch": dom_bytes, "avg_launch_us": stage_us[dominant], "peak_source": peak_src}
+
+    rec.update({
+        "value": calls_per_s, "unit": "calls/s", "ms_per_step": ms_per_step, "step_us": step_spread,
+        "config": workload_config(w, world, args.flush_mib),
+        "tokens_per_s": calls_per_s * B, "scanned_tokens_per_s": calls_per_s * sum(w.seq_lens),
+        "step_hbm": {"alg_bytes_per_call": ab["total"], "bytes_breakdown": ab, "achieved_gbs": step_gbs,
+                     "frac_of_8000_gbs": step_gbs / NOMINAL_HBM_GBS,
+                     "frac_of_measured_copy": step_gbs / peak, "measured_copy_gbs": peak},
+        "stage_us": stage_us, "internal_splits": S,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out_bytes,
+                "what": "one H2D copy of q, qp, page_table, seq_lens staged in one pinned buffer; the chained "
+                        "call on views of it; one D2H copy of out, lse and the selected indices; KV and label "
+                        "caches stay resident"},
+        "clocks": clocks,
+        "gpu_launches": args.steps * ds.ds_decode_kernel_launches(shape, k),
+    })
+    if d.rank == 0 and world == 1 and not args.no_cpu_baseline:
+        budget = args.cpu_budget_s if extras else args.cpu_budget_s / 2
+        rec["cpu_baseline"] = cpu_baseline(inp, args, budget)
+    return rec
+
+
+def stage_bytes(w: dsgen.Workload, stage: str):
+    """Algorithmic bytes one launch of a stage's kernel moves, and its source file."""
+    ab = alg_bytes(w)
+    if stage == "index_score":
+        return ab["scan"] + ab["page_table"] + w.batch * w.num_q_heads * w.proxy_dim * 2, "score.cu"
+    if stage == "sparse_attn":
+        return ab["kv_rows"] + ab["q"] + w.batch * w.num_kv_heads * w.top_k * 4, "attn.cu"
+    # the top-k reads the row scores once and writes the indices
+    return sum(T * 4 for T in w.seq_lens) * w.num_kv_heads + w.batch * w.num_kv_heads * w.top_k * 4, "topk.cu"
+
+
+def cpu_baseline(inp, args, budget_s: float) -> dict:
+    """The oracle on whole (request, KV head) rows of the call, on the host cores, scaled to calls/s."""
+    w = inp.w
+    rows_per_call = w.batch * w.num_kv_heads
+    cpu = inp.to("cpu")
+    threads = args.oracle_threads or host_threads()
+    rate1, n1 = oracle_rows(cpu, budget_s / 3, 1)
+    rate, n = oracle_rows(cpu, budget_s * 2 / 3, threads)
+    what = (f"(request, KV head) rows of the {rows_per_call}-row call, each scored, top-k selected and "
+            f"attended by the oracle")
+    return {
+        "value": rate / rows_per_call, "unit": "calls/s", "cores": threads, "kind": "oracle",
+        "sample": f"{n} {what}, {threads} rows at a time on {threads} host threads",
+        "single_thread": {"value": rate1 / rows_per_call, "unit": "calls/s", "cores": 1,
+                          "sample": f"{n1} {what}, one at a time; {1e3 / rate1:.1f} ms per row"},
+    }
+
+
+def measure_extras(d: _Device, w: dsgen.Workload, inp, shape, args) -> dict:
+    """Beside the headline, outside its timed region: the cache append, the shard-emulated top-k and
+    (shared index keys only) the block-compressed selection."""
+    import top_sparse_decode_label_gb300 as ds
+
+    dev, stream = d.dev, d.stream
+    k = w.top_k
+    B, Hkv, D = w.batch, w.num_kv_heads, w.head_dim
     # ---- the step before the path: appending each request's new token (its
     # last position is rewritten with fresh rows; launch-latency-bound).
     append_us = None
@@ -491,6 +586,7 @@ def run_ours(args):
         else:
             channels = None
             index_key = torch.randn((B, w.proxy_dim), generator=gen).to(torch.bfloat16).to(dev)
+
         def append():
             ds.ds_cache_append(shape, k_new, v_new, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
                                inp.page_table, pos, label=inp.label, channels=channels, index_key=index_key)
@@ -546,6 +642,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             times[name] = e0.elapsed_time(e1) * 1e3 / 50
         sharded = {"topk_us": times, "equal": bool(torch.equal(idx1, idx2))}
+        del scores, ws1, ws2
     except Exception as e:
         sharded = f"failed: {e}"
 
@@ -558,7 +655,7 @@ def run_ours(args):
             kb = k // 64
             bk = torch.empty((inp.num_pages, w.proxy_dim), dtype=torch.bfloat16, device=dev)
             ec = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            flush.zero_()
+            d.flush()
             ec[0].record(stream)
             ds.ds_block_compress(shape, inp.label, inp.page_table, inp.seq_lens, bk, stream=stream)
             ec[1].record(stream)
@@ -575,7 +672,7 @@ def run_ours(args):
             eb0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_b)]
             eb1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_b)]
             for i in range(n_b):
-                flush.zero_()
+                d.flush()
                 eb0[i].record(stream)
                 bcall()
                 eb1[i].record(stream)
@@ -591,63 +688,44 @@ def run_ours(args):
                                   "the whole cache, once (a cache-maintenance step, not part of the call)"}
         except Exception as e:  # reported, never hides the main measurement
             blocks_rec = f"failed: {e}"
+    return {"cache_append_us": append_us, "sharded_topk": sharded, "block_select": blocks_rec}
 
-    # ---- roofline
-    peak, peak_src = measured_peak()
-    ab = alg_bytes(w)
-    step_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
-    dominant = max(stage_us, key=stage_us.get)
-    if dominant == "index_score":
-        dom_bytes = ab["scan"] + ab["page_table"] + w.batch * w.num_q_heads * w.proxy_dim * 2
-        dom_file = "score.cu"
-    elif dominant == "sparse_attn":
-        dom_bytes = ab["kv_rows"] + ab["q"] + w.batch * w.num_kv_heads * w.top_k * 4
-        dom_file = "attn.cu"
-    else:
-        # the top-k reads the row scores once and writes the indices
-        dom_bytes = sum(T * 4 for T in w.seq_lens) * w.num_kv_heads + w.batch * w.num_kv_heads * w.top_k * 4
-        dom_file = "topk.cu"
-    dom_gbs = dom_bytes / (stage_us[dominant] * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
-                "frac": dom_gbs / peak, "traffic": traffic_record(dom_file, w.name),
-                "alg_bytes_per_launch": dom_bytes, "avg_launch_us": stage_us[dominant], "peak_source": peak_src}
 
-    line = {
-        "metric": METRIC, "value": calls_per_s, "unit": "calls/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "step_us": step_spread, "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, world, args.flush_mib),
-        "tokens_per_s": calls_per_s * B, "scanned_tokens_per_s": calls_per_s * sum(w.seq_lens),
-        "step_hbm": {"alg_bytes_per_call": ab["total"], "bytes_breakdown": ab, "achieved_gbs": step_gbs,
-                     "frac_of_peak": step_gbs / peak},
-        "stage_us": stage_us, "internal_splits": S, "block_select": blocks_rec,
-        "cache_append_us": append_us,
-        "sharded_topk": sharded,
-        "roofline": roofline,
-        "e2e": {"value": e2e_value, "unit": "calls/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "what": "one H2D copy of q, qp, page_table, seq_lens staged in one pinned buffer; the chained "
-                        "call on views of it; one D2H copy of out, lse, idx; KV and label caches stay resident"},
-        "clocks": clocks,
-        "gpu_launches": args.steps * ds.ds_decode_kernel_launches(shape, k),
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows_per_call = B * Hkv
-        cpu = inp.to("cpu")
-        threads = args.oracle_threads or host_threads()
-        rate1, n1 = oracle_rows(cpu, args.cpu_budget_s / 3, 1)
-        rate, n = oracle_rows(cpu, args.cpu_budget_s * 2 / 3, threads)
-        what = (f"(request, KV head) rows of the {rows_per_call}-row call, each scored, top-k selected and "
-                f"attended by the oracle")
-        line["cpu_baseline"] = {
-            "value": rate / rows_per_call, "unit": "calls/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} {what}, {threads} rows at a time on {threads} host threads",
-            "single_thread": {"value": rate1 / rows_per_call, "unit": "calls/s", "cores": 1,
-                              "sample": f"{n1} {what}, one at a time; {1e3 / rate1:.1f} ms per row"},
-        }
-    if rank == 0:
+# Keys of a workload's record that describe only that workload (the rest of the line is shared).
+PER_CONFIG_KEYS = ("value", "unit", "ms_per_step", "step_us", "config", "tokens_per_s", "scanned_tokens_per_s",
+                   "step_hbm", "stage_us", "internal_splits", "roofline", "e2e", "clocks", "gpu_launches",
+                   "cpu_baseline")
+
+
+def run_ours(args):
+    import top_sparse_decode_label_gb300  # noqa: F401  (fails loudly when the library is missing)
+
+    d = _Device(args)
+    head = workload_of(args)
+    others = [c for c in also_configs(args) if c != args.config]
+    try:
+        rec = measure(d, head, args, extras=True)
+        torch.cuda.empty_cache()
+        per_config = []
+        for c in others:
+            wc = workload_of(args, c)
+            rc = measure(d, wc, args, extras=False)
+            per_config.append({key: rc[key] for key in PER_CONFIG_KEYS if key in rc})
+            torch.cuda.empty_cache()
+    finally:
+        d.sampler.stop()
+
+    line = {"metric": METRIC, "value": rec["value"], "unit": "calls/s", "n_gpus": d.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "step_us": rec["step_us"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic"}
+    for key in PER_CONFIG_KEYS + ("block_select", "cache_append_us", "sharded_topk"):
+        if key in rec and key not in line:
+            line[key] = rec[key]
+    line["per_config"] = per_config
+    if d.rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
+    if d.world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0

@@ -135,21 +135,22 @@ ds_status ds_topk_select(const ds_shape* shape, const float* scores, const int32
 /*
  * ds_topk_select without a workspace argument, for callers that cannot
  * allocate device memory: a plugin whose host framework owns every device
- * allocation and passes in only the call's tensors, code running while a CUDA
- * graph is being captured around it (where entering an allocator is not
- * allowed), or a latency-critical serving thread that must not wait on an
- * allocator lock. The pages describe no such entry point; it exists for
- * these callers only. Same arguments and results as ds_topk_select.
+ * allocation and hands it only the tensors of the call, or a latency-critical
+ * serving thread that must not wait on an allocator's lock. The pages
+ * describe no such entry point; it exists for these callers only. Same
+ * arguments and results as ds_topk_select, and nothing is allocated or freed.
  *
  * Scratch comes from an array of DS_TOPK_STATIC_SCRATCH_BYTES (16 MiB)
  * compiled into the library; each GPU that loads the library holds one until
  * the process exits. A (shape, k) needing more scratch than that (see
  * ds_topk_workspace_bytes) returns DS_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. All calls share the one array, so calls whose work overlaps on the
- * GPU (other streams, other host threads) race and corrupt each other's
- * results: serialise them. Nothing is allocated or freed.
+ * device, with that device current) and caches it; make that first call
+ * before any stream capture, and note that cudaDeviceReset invalidates the
+ * cached address. All calls share the one array, so calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and corrupt
+ * each other's results: serialise them. The array needs no clearing: the
+ * top-k only spills candidate lists there, writing before it reads.
  */
 #define DS_TOPK_STATIC_SCRATCH_BYTES (16u << 20)
 ds_status ds_topk_select_static(const ds_shape* shape, const float* scores, const int32_t* seq_lens, int k,

@@ -69,3 +69,51 @@ def run_decode(inp_gpu, shape, k):
 
 def default_scale(w):
     return 1.0 / math.sqrt(w.head_dim)
+
+
+def host_threads() -> int:
+    import os
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_every_row(inp, k=None, num_splits: int = 1, split_mode: int = 0):
+    """The oracle's (idx, out, lse) for every (request, KV head) row of a CPU ``dsgen.Inputs``.
+
+    Each row is the oracle's four stages run on that row alone (its row mask); the rows are spread over
+    the host cores (the C oracle releases the interpreter lock while it computes) and their results are
+    assembled into full-size tensors: idx int32 [B, Hkv, k], out float64 [B, Hq, D], lse float64 [B, Hq].
+    """
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    w = inp.w
+    k = w.top_k if k is None else k
+    B, Hkv, G = w.batch, w.num_kv_heads, w.group
+    oracle.lib()
+    idx = torch.full((B, Hkv, k), -1, dtype=torch.int32)
+    out = torch.zeros((B, w.num_q_heads, w.head_dim), dtype=torch.float64)
+    lse = torch.zeros((B, w.num_q_heads), dtype=torch.float64)
+
+    def one(bg):
+        b, g = bg
+        m = torch.zeros((B, Hkv), dtype=torch.uint8)
+        m[b, g] = 1
+        _, ri, ro, rl = oracle.decode(inp, k=k, num_splits=num_splits, split_mode=split_mode, row_mask=m)
+        hs = slice(g * G, (g + 1) * G)
+        return b, g, ri[b, g].clone(), ro[b, hs].clone(), rl[b, hs].clone()
+
+    rows = [(b, g) for b in range(B) for g in range(Hkv)]
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        with ThreadPoolExecutor(min(len(rows), host_threads())) as ex:
+            for b, g, ri, ro, rl in ex.map(one, rows):
+                idx[b, g] = ri
+                out[b, g * G:(g + 1) * G] = ro
+                lse[b, g * G:(g + 1) * G] = rl
+    finally:
+        torch.set_num_threads(prev)
+    return idx, out, lse

@@ -129,3 +129,17 @@ def test_block_path_host_validation_without_a_gpu():
     assert L.ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), ws, need - 1, None) == -4
     a.proxy_dim = 48
     assert L.ds_sparse_decode_blocks(ctypes.byref(shape), ctypes.byref(a), ws, need, None) == -2
+
+
+def test_library_is_built_as_whole_program_device_code():
+    # The library is compiled without relocatable device code: every kernel's
+    # code is generated from its own translation unit (a relocatable timing
+    # build of the same sources is the one configuration on record that faulted).
+    import importlib.util
+    path = os.path.join(ROOT, "top_sparse_decode_label_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_dssparse_build_flags", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    flags = mod.ARCH + mod.FLAGS
+    assert not any(f.startswith("-rdc") or f in ("-dc", "--relocatable-device-code=true", "-dlink") for f in flags)
+    assert mod.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

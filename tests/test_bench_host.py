@@ -120,3 +120,22 @@ def test_algorithmic_bytes_are_the_workloads_byte_counts():
         assert ab["scan"] == scan and ab["kv_rows"] == kv + scales, w.name
         assert ab["page_table"] == w.batch * -(-w.seq_lens[0] // 64) * 4
         assert ab["total"] == sum(v for key, v in ab.items() if key != "total")
+
+
+def test_default_headline_is_the_largest_workload_and_the_others_ride_along():
+    # The headline is the workload with the most algorithmic bytes per call (the QSA b8 x 262,144 decode);
+    # the Llama-8B DS, longchat DS and 1M-token QSA workloads are measured in the same run.
+    sys.path.insert(0, ROOT)
+    import bench
+    import dsgen
+    old = sys.argv
+    sys.argv = ["bench.py"]
+    try:
+        args = bench.parse_args()
+    finally:
+        sys.argv = old
+    largest = max(range(len(dsgen.WORKLOADS)), key=lambda i: bench.alg_bytes(dsgen.WORKLOADS[i])["total"])
+    assert args.config == largest == 3
+    assert bench.workload_of(args).name == "qsa_b8_h32kv4_t262144_idx64_k2048_fp8"
+    assert sorted(bench.also_configs(args)) == [1, 2, 4]
+    assert bench.NOMINAL_HBM_GBS == 8000.0

@@ -167,7 +167,7 @@ def test_block_decode_on_real_valued_keys_keeps_a_valid_top_k():
     assert_lse_close(lse, rlse, "block decode lse")
 
 
-def test_block_decode_at_the_qsa_1m_shape_sampled():
+def test_block_decode_at_the_qsa_1m_shape():
     # One request of 1,048,576 tokens (16,384 blocks), 32 of them kept (2048 tokens), FP8 cache.
     w = dsgen.WORKLOADS[4]
     g = dsgen.make_inputs(w, device=DEV)
@@ -178,19 +178,22 @@ def test_block_decode_at_the_qsa_1m_shape_sampled():
     blocks, out, lse = _decode_blocks(g, bk, 32)
     inp = g.to("cpu")
     bkc = bk.cpu()
-    # Block keys of a sample of pages, exactly.
-    pages = inp.page_table[0, :: 997].long()
-    keys = inp.label.view(-1, P, w.proxy_dim)[pages].double().mean(1)
-    ref_keys = oracle.block_compress(inp.label, inp.page_table[:, :64].contiguous(),
-                                     torch.tensor([64 * 64], dtype=torch.int32), inp.num_pages)
-    assert torch.equal(bkc[inp.page_table[0, :64].long()].view(torch.int16),
-                       ref_keys[inp.page_table[0, :64].long()].view(torch.int16))
-    assert torch.allclose(bkc[pages].double(), keys, rtol=1e-2, atol=1e-2)
+    # Every block key of the request, bit for bit.
+    ref_keys = oracle.block_compress(inp.label, inp.page_table, inp.seq_lens, inp.num_pages)
+    used = inp.page_table[0, : w.seq_lens[0] // P].long()
+    assert torch.equal(bkc[used].view(torch.int16), ref_keys[used].view(torch.int16))
     # The kept blocks are the oracle's top 32 of the block scores (up to score rounding: the keys' means
     # are not exact in bf16 here).
     scores = oracle.block_score(inp.qp, bkc, inp.page_table, inp.seq_lens, w.num_kv_heads)
     rblocks = oracle.topk(scores, torch.tensor([w.seq_lens[0] // P], dtype=torch.int32), 32)
     _assert_valid_top_k(blocks, rblocks, scores)
+    # The attention over the tokens of the blocks the GPU kept, against the oracle's attention over them.
+    idx = oracle.block_expand(blocks, inp.seq_lens)
+    o, l = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale, inp.page_table,
+                              inp.seq_lens, idx)
+    rout, rlse = oracle.lse_merge(o, l)
+    assert_close(out, rout, atol_for(w), "out over the kept blocks")
+    assert_lse_close(lse, rlse, "lse over the kept blocks")
 
 
 def test_block_decode_replays_in_a_cuda_graph_with_new_inputs():

@@ -13,7 +13,7 @@ import torch
 import dsgen
 import oracle
 from gpu_helpers import (ATOL_BF16, ATOL_FP8, assert_close, assert_lse_close, atol_for, default_scale,
-                         run_decode, shape_of, workload)
+                         oracle_every_row, run_decode, shape_of, workload)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -338,51 +338,30 @@ def test_bad_page_id_is_flagged_not_read():
     assert flags & 2
 
 
-# --------------------------------------------------------------------- full size, sampled
-
-def _sample_rows(w, n=2):
-    rows = torch.zeros((w.batch, w.num_kv_heads), dtype=torch.uint8)
-    picks = [(0, 0), (w.batch - 1, w.num_kv_heads - 1)][:n]
-    for b, g in picks:
-        rows[b, g] = 1
-    return rows
-
+# --------------------------------------------------------------------- full size, every row
 
 @pytest.mark.parametrize("ci,D", [(1, 128), (2, 128), (3, 128), (4, 128), (1, 256), (3, 256)])
-def test_full_size_workload_sampled_rows(ci, D):
-    # Head dimension 256: the Llama-8B DS and QSA shapes as `bench.py --head-dim 256` times them.
+def test_full_size_workload_every_row(ci, D):
+    # The four full-size workloads through the chained call the bench times, every (request, KV head) row
+    # against the oracle (indices bit-exact, out and lse element by element); head dimension 256 for the
+    # Llama-8B DS and QSA shapes as `bench.py --head-dim 256` times them.
     w = dsgen.WORKLOADS[ci]
     if D != w.head_dim:
         w = w.scaled(head_dim=D, name=f"{w.name}_d{D}")
     g = dsgen.make_inputs(w, device=DEV)
-    shape = ds_shape = shape_of(g)
-    idx, out, lse = run_decode(g, ds_shape, w.top_k)
+    shape = shape_of(g)
+    idx, out, lse = run_decode(g, shape, w.top_k)
     torch.cuda.synchronize()
     inp = g.to("cpu")
-    mask = _sample_rows(w)
-    scores = oracle.index_score(inp.qp, inp.label, inp.page_table, inp.seq_lens, w.num_kv_heads, w.max_seq_len,
-                                row_mask=mask)
-    ridx = oracle.topk(scores, inp.seq_lens, w.top_k, row_mask=mask)
-    o, l = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale, inp.page_table,
-                              inp.seq_lens, ridx, row_mask=mask)
-    rout, rlse = oracle.lse_merge(o, l)
-    gi, go, gl = idx.cpu(), out.cpu(), lse.cpu()
-    G = w.group
-    for b, gg in mask.nonzero().tolist():
-        assert torch.equal(gi[b, gg], ridx[b, gg]), (b, gg)
-        hs = slice(gg * G, (gg + 1) * G)
-        assert_close(go[b, hs], rout[b, hs], atol_for(w), f"out b{b} g{gg}")
-        assert_lse_close(gl[b, hs], rlse[b, hs], f"lse b{b} g{gg}")
-    # Every row: ascending, distinct, in range, exactly min(k, T) entries.
+    ridx, rout, rlse = oracle_every_row(inp)
+    gi = idx.cpu()
     for b in range(w.batch):
-        T = w.seq_lens[b]
-        keff = min(w.top_k, T)
-        r = gi[b]
-        assert (r[:, keff:] == -1).all()
-        v = r[:, :keff]
-        assert (v >= 0).all() and (v < T).all() and (v[:, 1:] > v[:, :-1]).all()
+        for gg in range(w.num_kv_heads):
+            assert torch.equal(gi[b, gg], ridx[b, gg]), f"indices of row (b{b}, g{gg})"
+    assert_close(out, rout, atol_for(w), "out")
+    assert_lse_close(lse, rlse, "lse")
     if ci == 4:
-        # Split-KV over 4 and 16 chunks, merged, equals the unsplit result.
+        # Split-KV over 4 and 16 chunks, merged, equals the unsplit result and the oracle's split merge.
         ds = _ds()
         for S in (4, 16):
             o_part = torch.empty((S, w.batch, w.num_q_heads, w.head_dim), device=DEV)
@@ -395,7 +374,24 @@ def test_full_size_workload_sampled_rows(ci, D):
             assert_close(mo, out.float(), ATOL_FP8, f"merged S={S} vs unsplit")
             assert_lse_close(ml, lse.double(), f"merged lse S={S}")
             os_, ls_ = oracle.sparse_attn(inp.q, inp.k_cache, inp.v_cache, inp.k_scale, inp.v_scale,
-                                          inp.page_table, inp.seq_lens, ridx, None, S, 0, row_mask=mask)
+                                          inp.page_table, inp.seq_lens, ridx, None, S, 0)
             mo2, ml2 = oracle.lse_merge(os_, ls_)
-            b, gg = 0, 0
-            assert_close(mo[b, :G], mo2[b, :G], ATOL_FP8, f"merged S={S} vs oracle")
+            assert_close(mo, mo2, ATOL_FP8, f"merged S={S} vs the oracle's split merge")
+            assert_lse_close(ml, ml2, f"merged lse S={S} vs the oracle's")
+
+
+def test_k_equal_to_seq_len_is_dense_attention_at_the_longchat_size():
+    # The longchat workload's own size (3 requests x 20000 tokens, 32 KV heads) with k = T = 20000: every
+    # token is kept, so the call is dense softmax attention over the whole cache, split and merged inside
+    # the attention's clusters at that size.
+    w = dsgen.WORKLOADS[2]
+    T = w.max_seq_len
+    g = dsgen.make_inputs(w, device=DEV)
+    idx, out, lse = run_decode(g, shape_of(g), T)
+    torch.cuda.synchronize()
+    inp = g.to("cpu")
+    ridx, rout, rlse = oracle_every_row(inp, k=T)
+    assert torch.equal(idx.cpu(), ridx)
+    assert idx.cpu().eq(torch.arange(T, dtype=torch.int32)).all()
+    assert_close(out, rout, ATOL_BF16, "dense out")
+    assert_lse_close(lse, rlse, "dense lse")

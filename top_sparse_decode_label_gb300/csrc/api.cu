@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "ds_sparse.h"
@@ -26,17 +27,20 @@ int current_device() {
   return dev;
 }
 
-// Device address of the error word on the current device (resolved once).
+// Device address of the error word on the current device (looked up once per
+// device; concurrent first lookups store the same address).
 unsigned* error_word() {
-  static unsigned* ptrs[kMaxDevices] = {};
+  static std::atomic<unsigned*> ptrs[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0) return nullptr;
-  if (!ptrs[dev]) {
+  unsigned* w = ptrs[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ds_device_errors) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned*>(p);
+    w = static_cast<unsigned*>(p);
+    ptrs[dev].store(w, std::memory_order_release);
   }
-  return ptrs[dev];
+  return w;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

@@ -3,17 +3,18 @@
 //
 // Some callers of a decode step have no way to obtain a workspace: a plugin
 // that runs inside a host framework which owns every device allocation and
-// hands out only the tensors of the call, code that runs while another layer
-// is capturing a CUDA graph and must not enter the allocator, or a real-time
-// serving thread that may not block on an allocator lock. For them this entry
-// point takes its scratch from a fixed array compiled into the library
-// instead of from a caller-provided workspace.
+// hands it only the tensors of the call, or a real-time serving thread that
+// may not block on an allocator's lock. For them this entry point takes its
+// scratch from a fixed array compiled into the library instead of from a
+// caller-provided workspace, and allocates nothing.
 //
 // The array lives in device global memory on every GPU that loads the
 // library, for as long as the process runs. Its size caps the problem: a
 // (shape, k) whose top-k scratch exceeds DS_TOPK_STATIC_SCRATCH_BYTES is
 // rejected with DS_ERR_WORKSPACE before anything is launched.
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "ds_sparse.h"
 
@@ -26,18 +27,21 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the scratch array on the current device, resolved on the
-// first call made with that device current (nullptr on failure).
+// Device address of the scratch array on the current device, looked up on the
+// first call made with that device current (nullptr on failure). Two threads
+// that make their first call at once both look it up and store the same
+// address; the atomics make that well defined. A cudaDeviceReset invalidates
+// the cached address (the header says so).
 void* static_scratch() {
-  static void* ptrs[kMaxDevices] = {};
+  static std::atomic<void*> ptrs[kMaxDevices] = {};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!ptrs[dev]) {
-    void* p = nullptr;
+  void* p = ptrs[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_topk_static_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
+    ptrs[dev].store(p, std::memory_order_release);
   }
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace
