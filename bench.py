@@ -68,7 +68,7 @@ def parse_args():
                          "FP8 workload, the largest)")
     ap.add_argument("--also", default="1,2,4",
                     help="comma-separated further workloads measured in the same run into `per_config` "
-                         "('' for none)")
+                         "('none' for none)")
     ap.add_argument("--head-dim", type=int, default=None, help="override the workload's head dimension (128, 256)")
     ap.add_argument("--flush-mib", type=int, default=256)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0, help="oracle time budget of the CPU baseline")
@@ -225,7 +225,9 @@ def workload_of(args, config: int = None) -> dsgen.Workload:
 
 
 def also_configs(args):
-    """The workload indices of --also."""
+    """The workload indices of --also ('none' or '' for none)."""
+    if args.also.strip().lower() == "none":
+        return []
     return [int(x) for x in args.also.split(",") if x.strip() != ""]
 
 

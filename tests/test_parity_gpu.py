@@ -277,6 +277,8 @@ CHAIN_CASES = [
     ("qsa_1m_small", dsgen.WORKLOADS[4].scaled(seq_lens=[40000], top_k=2048)),
     ("qsa_d256_small", dsgen.WORKLOADS[3].scaled(batch=2, seq_lens=[9000, 4097], top_k=512, head_dim=256)),
     ("llama_ds_d256_small", dsgen.WORKLOADS[1].scaled(batch=2, seq_lens=[5000, 77], top_k=300, head_dim=256)),
+    # Rows of one call whose k is small, large and equal against their length.
+    ("mixed_rows", dsgen.WORKLOADS[1].scaled(seq_lens=[6000, 1000, 300], top_k=300)),
 ]
 
 
@@ -289,6 +291,82 @@ def test_chained_decode_matches_oracle(name, w):
     assert torch.equal(idx.cpu(), ridx)
     assert_close(out, rout, atol_for(w), "out")
     assert_lse_close(lse, rlse, "lse")
+
+
+def _one_token_per_page(T):
+    """One token of every 64-token page of a row of T tokens, at an offset that varies from page to page (the
+    page's first token when that offset lies past T)."""
+    out = []
+    for i in range(-(-T // 64)):
+        t = i * 64 + ((i * 37 + 11) & 63)
+        out.append(t if t < T else i * 64)
+    return out
+
+
+@pytest.mark.parametrize("layout", ["per_head_label", "shared_index_key"])
+def test_chained_decode_with_a_few_high_tokens_and_ties_below_them(layout):
+    # Only one token per page scores high (all equally), every other token scores 0: the top-k keeps the high
+    # tokens and then the lowest-index tokens of score 0, through the chained call on both label layouts.
+    T, k = 20000, 1000
+    if layout == "per_head_label":
+        w = workload("sparse_high_ds", 1, 8, 2, [T], 32, 2, k)
+    else:
+        w = workload("sparse_high_qsa", 1, 16, 2, [T], 64, 1, k, kv="fp8_e4m3", from_q=False)
+    inp = dsgen.make_inputs(w)
+    inp.qp = torch.ones_like(inp.qp)
+    lab = torch.zeros_like(inp.label)
+    pt = inp.page_table[0].long()
+    high = _one_token_per_page(T)
+    for t in high:
+        lab[pt[t // 64] * 64 + t % 64] = 8
+    inp.label = lab
+    g = inp.to(DEV)
+    idx, out, lse = run_decode(g, shape_of(inp), k)
+    _, ridx, rout, rlse = oracle.decode(inp)
+    assert torch.equal(idx.cpu(), ridx)
+    assert set(high) <= set(ridx[0, 0].tolist()) and len(high) < k
+    assert_close(out, rout, atol_for(w), "out")
+    assert_lse_close(lse, rlse, "lse")
+
+
+def test_chained_decode_is_exact_when_every_score_ties():
+    # A zero proxy query: every score is 0 and the top-k keeps the lowest token indices, on a long and a short
+    # row of one call.
+    w = dsgen.WORKLOADS[1].scaled(batch=2, seq_lens=[20000, 5000], top_k=600)
+    inp = dsgen.make_inputs(w)
+    inp.qp = torch.zeros_like(inp.qp)
+    g = inp.to(DEV)
+    idx, out, lse = run_decode(g, shape_of(inp), w.top_k)
+    _, ridx, rout, rlse = oracle.decode(inp)
+    assert torch.equal(idx.cpu(), ridx)
+    assert idx.cpu().eq(torch.arange(600, dtype=torch.int32)).all()
+    assert_close(out, rout, ATOL_BF16, "out")
+    assert_lse_close(lse, rlse, "lse")
+
+
+def test_chained_decode_on_long_rows_reuses_its_workspace():
+    # Rows of 200,000 and 150,001 tokens, two calls with different inputs on one workspace: the second call must
+    # not see the first one's state.
+    w = dsgen.WORKLOADS[3].scaled(batch=2, seq_lens=[200000, 150001], top_k=2048)
+    a = dsgen.make_inputs(w, seed=31)
+    b = dsgen.make_inputs(w, seed=32)
+    g = a.to(DEV)
+    shape = shape_of(a)
+    ds = _ds()
+    ws = torch.zeros(ds.ds_decode_workspace_bytes(shape, w.proxy_dim, w.top_k), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((w.batch, w.num_kv_heads, w.top_k), dtype=torch.int32, device=DEV)
+    out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((w.batch, w.num_q_heads), device=DEV)
+    for src in (a, b):
+        for name in ("q", "qp", "label", "k_cache", "v_cache", "k_scale", "v_scale", "page_table"):
+            getattr(g, name).copy_(getattr(src, name).to(DEV))
+        ds.ds_sparse_decode(shape, g.q, g.qp, g.label, g.k_cache, g.v_cache, g.k_scale, g.v_scale, g.page_table,
+                            g.seq_lens, w.top_k, idx, out, lse, ws)
+        torch.cuda.synchronize()
+        ridx, rout, rlse = oracle_every_row(src)
+        assert torch.equal(idx.cpu(), ridx)
+        assert_close(out, rout, ATOL_FP8, "out")
+        assert_lse_close(lse, rlse, "lse")
 
 
 def test_k_at_least_seq_len_is_dense_attention():
