@@ -329,6 +329,61 @@ def test_chained_decode_with_a_few_high_tokens_and_ties_below_them(layout):
     assert_lse_close(lse, rlse, "lse")
 
 
+@pytest.mark.parametrize("pattern", ["iid", "high_per_page", "negative", "all_tied"])
+def test_chained_decode_with_the_block_maxima_filter(pattern):
+    # Shared 64-wide index keys, rows long enough and k small enough (at most 1/128 of the row) for the top-k to
+    # bound its threshold with the scan's 16-token block maxima and read only the blocks that can hold a kept
+    # token; the second request is ragged (a partial last block). Patterns: iid scores; one high token per
+    # page, all equal and more of them than k (ties at the threshold); every score negative; every score tied
+    # (the candidates overflow and the exact two-pass selection takes over).
+    T, k = [300001, 280003], 2048
+    w = workload("bm_" + pattern, 2, 16, 2, T, 64, 1, k, kv="fp8_e4m3", from_q=False)
+    inp = dsgen.make_inputs(w)
+    if pattern == "high_per_page":
+        inp.qp = torch.ones_like(inp.qp)
+        lab = torch.zeros_like(inp.label)
+        for b in range(2):
+            pt = inp.page_table[b].long()
+            for t in _one_token_per_page(T[b]):
+                lab[pt[t // 64] * 64 + t % 64] = 8
+        inp.label = lab
+    elif pattern == "negative":
+        inp.qp = -inp.qp.abs()
+        inp.label = inp.label.abs()
+    elif pattern == "all_tied":
+        inp.qp = torch.zeros_like(inp.qp)
+    g = inp.to(DEV)
+    idx, out, lse = run_decode(g, shape_of(inp), k)
+    ridx, rout, rlse = oracle_every_row(inp)
+    assert torch.equal(idx.cpu(), ridx)
+    if pattern == "high_per_page":
+        assert all(ridx[b, h].tolist() == _one_token_per_page(T[b])[:k] for b in range(2) for h in range(2))
+    if pattern == "all_tied":
+        assert ridx.eq(torch.arange(k, dtype=torch.int32)).all()
+    assert_close(out, rout, ATOL_FP8, "out")
+    assert_lse_close(lse, rlse, "lse")
+
+
+@pytest.mark.parametrize("pattern", ["iid", "all_tied"])
+def test_chained_decode_long_rows_with_a_per_head_label(pattern):
+    # The same long rows and small k with a per-head label cache (no block maxima from that scan): the top-k
+    # guesses its filter bin from a sample of the scores; with every score tied the guess fails and the exact
+    # two-pass selection takes over.
+    T, k = [300001, 280003], 2048
+    w = workload("long_ds_" + pattern, 2, 8, 2, T, 32, 2, k)
+    inp = dsgen.make_inputs(w)
+    if pattern == "all_tied":
+        inp.qp = torch.zeros_like(inp.qp)
+    g = inp.to(DEV)
+    idx, out, lse = run_decode(g, shape_of(inp), k)
+    ridx, rout, rlse = oracle_every_row(inp)
+    assert torch.equal(idx.cpu(), ridx)
+    if pattern == "all_tied":
+        assert ridx.eq(torch.arange(k, dtype=torch.int32)).all()
+    assert_close(out, rout, ATOL_BF16, "out")
+    assert_lse_close(lse, rlse, "lse")
+
+
 def test_chained_decode_is_exact_when_every_score_ties():
     # A zero proxy query: every score is 0 and the top-k keeps the lowest token indices, on a long and a short
     # row of one call.

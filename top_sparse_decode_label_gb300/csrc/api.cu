@@ -285,11 +285,12 @@ ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* 
 namespace {
 
 // Workspace of the chained call: the scan's unit counters (zero before the
-// first call, left zero by every call), the scores, the top-k overflow lists
-// and the physical slots of the selection.
+// first call, left zero by every call), the scores and their 16-token block
+// maxima, the top-k overflow lists and the physical slots of the selection.
 struct DecodeLayout {
   unsigned* work;   // [2]
   float* scores;
+  float* bmax;      // [B, Hkv, ceil(max_seq_len / 16)]
   TopkLayout topk;
   int32_t* slots;   // [B, Hkv, k]
   float2* sscale;   // [B, Hkv, k] (K, V) page scales of the kept tokens (FP8 caches)
@@ -305,6 +306,9 @@ DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
   off = align256(off + 2 * sizeof(unsigned));
   L.scores = reinterpret_cast<float*>(p + off);
   off = align256(off + static_cast<size_t>(R) * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
+  L.bmax = reinterpret_cast<float*>(p + off);
+  const size_t nbr = static_cast<size_t>((s->max_seq_len > 0 ? s->max_seq_len : 1) + kMaxBlock - 1) / kMaxBlock;
+  off = align256(off + static_cast<size_t>(R) * nbr * 4);
   L.topk = topk_layout(p + off, R, s->max_seq_len);
   off = align256(off + L.topk.bytes);
   L.slots = reinterpret_cast<int32_t*>(p + off);
@@ -373,7 +377,7 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (shape->max_seq_len > 0) {
     ScoreArgs sa{args->qp, args->label, args->page_table, args->seq_lens, L.scores, err, shape->batch,
                  shape->num_q_heads, shape->num_kv_heads, args->label_heads, pd, shape->max_pages_per_req,
-                 shape->num_pages, shape->max_seq_len, L.work};
+                 shape->num_pages, shape->max_seq_len, L.work, L.bmax};
     st = from_cuda(launch_index_score(sa, s));
     if (st != DS_OK) return st;
   }
@@ -383,7 +387,10 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
     TopkArgs ta{L.scores, args->seq_lens, args->idx, err, shape->batch, shape->num_kv_heads, shape->max_seq_len,
                 shape->max_pages_per_req * shape->page_size, k, L.topk, L.slots, args->page_table,
                 fp8 ? args->k_scale : nullptr, fp8 ? args->v_scale : nullptr, fp8 ? L.sscale : nullptr,
-                shape->max_pages_per_req, shape->num_pages, shape->max_seq_len > 0 ? 1 : 0};
+                shape->max_pages_per_req, shape->num_pages, shape->max_seq_len > 0 ? 1 : 0,
+                (shape->max_seq_len > 0 && index_score_block_maxima(pd, args->label_heads, shape->num_kv_heads))
+                    ? L.bmax
+                    : nullptr};
     st = from_cuda(launch_topk(ta, s));
     if (st != DS_OK) return st;
   }

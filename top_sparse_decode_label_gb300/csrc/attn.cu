@@ -68,6 +68,14 @@ struct AttnParams {
   float qscale;        // sm_scale * log2(e)
 };
 
+// Stores 4 consecutive bf16 outputs (x, y, z, w) * scale as two bf16 pairs
+// (the output row offset is a multiple of 4 elements; rows are 4-byte aligned).
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v, float scale) {
+  __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(dst);
+  d2[0] = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+  d2[1] = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+}
+
 template <bool FP8, int D>
 struct Cfg {
   static constexpr int ROWB = FP8 ? D : D * 2;   // bytes per K or V row
@@ -92,7 +100,9 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   int* sl = reinterpret_cast<int*>(smem + C::RING);                 // [kSeg] slots
   float2* sc = reinterpret_cast<float2*>(sl + kSeg);                // [kSeg] (k scale, v scale)
   __shared__ float wm[kWarps][8], wl[kWarps][8];
+  __shared__ float cw[kWarps][8];          // each warp's weight per head in the combine
   __shared__ float cm[8], cl[8];
+  __shared__ float mw[16][8], mm[8], ml[8];   // each split's normalised weight per head in the merge
   __shared__ unsigned sh_scan[33];
   __shared__ unsigned sh_cnt[kWarps];
 
@@ -434,78 +444,106 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   }
   __syncthreads();
 
-  // ---- combine the warps: state (M, L, O unnormalised) per (head, dim)
+  // ---- combine the warps: state (M, L, O unnormalised) per (head, dim); each
+  // warp's weight per head is computed once, and the outputs go 4 dims at a time
   float* co = wo + kWarps * G * D;   // [G][D]
   if (tid < G) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][tid]);
     float L = 0.f;
-    if (M != -INFINITY)
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) L += (wm[w][tid] == -INFINITY) ? 0.f : exp2f(wm[w][tid] - M) * wl[w][tid];
+    for (int w = 0; w < kWarps; ++w) {
+      const float wt = (M == -INFINITY || wm[w][tid] == -INFINITY) ? 0.f : exp2f(wm[w][tid] - M);
+      cw[w][tid] = wt;
+      L += wt * wl[w][tid];
+    }
     cm[tid] = M;
     cl[tid] = L;
   }
   __syncthreads();
-  for (int e = tid; e < G * D; e += kThreads) {
+  for (int e = 4 * tid; e < G * D; e += 4 * kThreads) {
     const int h = e / D;
     const int d = e % D;
-    const float M = cm[h];
-    float acc_o = 0.f;
-    if (M != -INFINITY)
+    float4 acc_o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        acc_o += (wm[w][h] == -INFINITY) ? 0.f : exp2f(wm[w][h] - M) * wo[(w * G + h) * D + d];
+    for (int w = 0; w < kWarps; ++w) {
+      const float wt = cw[w][h];
+      const float4 v = *reinterpret_cast<const float4*>(wo + (w * G + h) * D + d);
+      acc_o.x += wt * v.x;
+      acc_o.y += wt * v.y;
+      acc_o.z += wt * v.z;
+      acc_o.w += wt * v.w;
+    }
+    const float M = cm[h];
     const float L = cl[h];
     const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
     if (p.cluster_merge) {
-      co[e] = acc_o;
+      *reinterpret_cast<float4*>(co + e) = acc_o;
     } else if (p.S == 1) {
-      p.out[qrow * D + d] = __float2bfloat16_rn(L > 0.f ? acc_o / L : 0.f);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      store_bf16x4(p.out + qrow * D + d, acc_o, inv);
       if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     } else {
       const long long prow = static_cast<long long>(j) * p.B * p.Hq + qrow;
-      p.o_part[prow * D + d] = L > 0.f ? acc_o / L : 0.f;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      float* op = p.o_part + prow * D + d;
+      op[0] = acc_o.x * inv;
+      op[1] = acc_o.y * inv;
+      op[2] = acc_o.z * inv;
+      op[3] = acc_o.w * inv;
       if (d == 0) p.lse_part[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
   }
   if (!p.cluster_merge) return;
 
-  // ---- merge the cluster's S splits: CTA j finishes elements [e0, e1)
+  // ---- merge the cluster's S splits. Every CTA reads each split's (M, L) per
+  // head once and turns them into normalised weights; CTA j then finishes
+  // elements [e0, e1) of G x D, 4 at a time, from every split's partial.
   cluster_sync();
-  const int E = G * D;
-  const int e0 = j * E / p.S, e1 = (j + 1) * E / p.S;
-  for (int e = e0 + tid; e < e1; e += kThreads) {
-    const int h = e / D;
-    const int d = e % D;
-    float Ms[16], Ls[16], Os[16];
+  if (tid < G) {
+    float Ms[16], Ls[16];
+    float M = -INFINITY;
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       if (s < p.S) {
-        Ms[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cm + h), s)));
-        Ls[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cl + h), s)));
-        Os[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(co + e), s)));
+        Ms[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cm + tid), s)));
+        Ls[s] = __uint_as_float(cluster_ld(cluster_map(smem_u32(cl + tid), s)));
+        M = fmaxf(M, Ms[s]);
       }
     }
-    float M = -INFINITY;
+    float L = 0.f;
 #pragma unroll
     for (int s = 0; s < 16; ++s)
-      if (s < p.S) M = fmaxf(M, Ms[s]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+      if (s < p.S && M != -INFINITY && Ms[s] != -INFINITY) L += exp2f(Ms[s] - M) * Ls[s];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        if (s < p.S && Ms[s] != -INFINITY) {
-          const float w = exp2f(Ms[s] - M);
-          L += w * Ls[s];
-          O += w * Os[s];
-        }
+    for (int s = 0; s < 16; ++s)
+      if (s < p.S) mw[s][tid] = (L > 0.f && Ms[s] != -INFINITY) ? exp2f(Ms[s] - M) / L : 0.f;
+    mm[tid] = M;
+    ml[tid] = L;
+  }
+  __syncthreads();
+  const int E = G * D;
+  const int e0 = j * E / p.S, e1 = (j + 1) * E / p.S;   // multiples of 4 (E and S powers of two, E / S >= 8)
+  for (int e = e0 + 4 * tid; e < e1; e += 4 * kThreads) {
+    const int h = e / D;
+    const int d = e % D;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s < p.S) {
+        const uint4 u = cluster_ld4(cluster_map(smem_u32(co + e), s));
+        const float wt = mw[s][h];
+        o.x += wt * __uint_as_float(u.x);
+        o.y += wt * __uint_as_float(u.y);
+        o.z += wt * __uint_as_float(u.z);
+        o.w += wt * __uint_as_float(u.w);
       }
     }
     const long long qrow = static_cast<long long>(b) * p.Hq + g * G + h;
-    p.out[qrow * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-    if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    store_bf16x4(p.out + qrow * D + d, o, 1.f);
+    const float L = ml[h];
+    if (d == 0 && p.lse) p.lse[qrow] = L > 0.f ? (mm[h] + log2f(L)) * kLn2 : -INFINITY;
   }
   cluster_sync();   // keep this CTA's shared memory until every CTA has read it
 }
@@ -562,7 +600,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (!fn) return cudaErrorNotSupported;
   const long long blocks = static_cast<long long>(a.B) * a.Hkv * a.S;
   if (blocks == 0) return cudaSuccess;
-  if (a.cluster_merge && (a.S > 16 || a.split_mode != 0)) return cudaErrorInvalidValue;
+  // The merge hands each CTA G * D / S outputs, 4 at a time: S a power of two up to 16.
+  if (a.cluster_merge && (a.S > 16 || (a.S & (a.S - 1)) || a.split_mode != 0)) return cudaErrorInvalidValue;
   AttnParams p{};
   p.q = static_cast<const uint16_t*>(a.q);
   p.kc = static_cast<const uint8_t*>(a.k_cache);

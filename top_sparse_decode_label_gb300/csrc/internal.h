@@ -34,10 +34,15 @@ struct ScoreArgs {
   unsigned* err;
   int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
   unsigned* work;          // [2] zeroed unit counters (left zero): dynamic unit scheduling; null: static
+  float* bmax;             // [B, Hkv, ceil(Tmax / 16)] largest score of each 16-token block, or null
+                           // (written only by kernels for which index_score_block_maxima is true)
 };
 // Returns a cudaError_t; cudaErrorNotSupported for shapes without a kernel.
 cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream);
 bool index_score_supported(int C, int HL, int Hkv, int G);
+// Whether the scan for this shape also writes the 16-token block maxima.
+bool index_score_block_maxima(int C, int HL, int Hkv);
+constexpr int kMaxBlock = 16;   // tokens per block of the block maxima
 
 struct TopkArgs {
   const float* scores;     // [B, Hkv, Tmax]
@@ -56,6 +61,10 @@ struct TopkArgs {
   float2* sscale;          // [B, Hkv, k]
   int maxp, num_pages;
   int pre_wait;            // inputs may be read before the previous kernel completes
+  // Largest score of each 16-token block of each row ([B, Hkv, ceil(Tmax / 16)],
+  // exactly the maxima of `scores`), or null. Long rows with a small k use
+  // them to read only the blocks that can hold a kept token.
+  const float* bmax;
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 

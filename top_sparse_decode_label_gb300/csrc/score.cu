@@ -10,9 +10,11 @@
 // lane first adds its group's proxy queries (fp32) and then needs one dot
 // product per (token, group).
 //
-// HBM-bound scan. The label cache is cut into 16 KB units of whole token
-// rows (HL*C*2 bytes each) of one request. A persistent grid takes the units
-// in chunks of consecutive units: with a work counter (chained call) each
+// HBM-bound scan. The label rows are read once, with an evict-first L2
+// policy; the scores are written with an evict-last one, so that the top-k
+// after the scan reads them from L2. The label cache is cut into 16 KB units
+// of whole token rows (HL*C*2 bytes each) of one request. A persistent grid
+// takes the units in chunks of consecutive units: with a work counter (chained call) each
 // CTA's first chunk is fixed and later ones are claimed with one atomicAdd, a
 // chunk ahead, so faster CTAs take more work; the last two units per CTA go
 // out one at a time, so all CTAs finish together (the last CTA to finish
@@ -34,8 +36,11 @@
 // whole 64-token pages with tiled tensor copies that swizzle 16-byte chunks
 // by row, each consumer warp forms the scores of 16 tokens for every group
 // with ldmatrix and mma.sync (bf16 in, fp32 accumulate) against the group
-// queries held in registers. Every mbarrier wait is bounded: on timeout it
-// sets DS_DEVERR_TIMEOUT and carries on.
+// queries held in registers. These warps also write the largest score of
+// each 16-token block per group (three shuffles over the fragment rows), from
+// which the top-k bounds its threshold without reading every score. Every
+// mbarrier wait is bounded: on timeout it sets DS_DEVERR_TIMEOUT and carries
+// on.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -68,6 +73,8 @@ struct ScoreParams {
   int units;        // B * upb (< 2^31, checked on the host)
   int upb;          // units per request
   int nst;          // ring stages
+  float* bmax;      // tensor-core path: [B, Hkv, nbr] maxima of 16-token blocks, or null
+  int nbr;          // blocks per row of bmax: ceil(Tmax / 16)
 };
 
 __device__ __forceinline__ int clamp_len(const ScoreParams& p, int b) {
@@ -100,6 +107,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ int stage_unit[kMaxStages];   // unit held by each ring stage, -1: no more units
+  __shared__ int stage_req[kMaxStages];    // and its request (the producer's quotient, for the consumers)
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -118,6 +126,10 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
   grid_dependency_wait();
   grid_launch_dependents();
 
+  // The label rows stream through once and go first from L2; the scores and
+  // block maxima stay there for the top-k, which reads them next.
+  const uint64_t stream_pol = l2_evict_first();
+  const uint64_t keep_pol = l2_evict_last();
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
     // Units come in chunks of kChunkUnits consecutive units. The page ids of
@@ -241,10 +253,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
         if (lane == 0) {
           stage_unit[s] = unit;
+          stage_req[s] = b;
           mbar_arrive_expect_tx(&full_bar[s], total);
         }
         __syncwarp();
-        if (nbytes) tensor_g2s_2d(dst + dst_off, &p.tmap, 0, pid * kPage, &full_bar[s]);
+        if (nbytes) tensor_g2s_2d_hint(dst + dst_off, &p.tmap, 0, pid * kPage, &full_bar[s], stream_pol);
         if (++s == p.nst) {
           s = 0;
           ++fill;
@@ -271,10 +284,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
       for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
       if (lane == 0) {
         stage_unit[s] = unit;
+        stage_req[s] = b;
         mbar_arrive_expect_tx(&full_bar[s], total);
       }
       __syncwarp();
-      if (nbytes) bulk_g2s(dst + dst_off, src, nbytes, &full_bar[s]);
+      if (nbytes) bulk_g2s_hint(dst + dst_off, src, nbytes, &full_bar[s], stream_pol);
       if (++s == p.nst) {
         s = 0;
         ++fill;
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         if (!ok && lane == 0) flag_error(p.err, 8u);
         const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
         if (unit < 0) break;
-        const int ub = unit / p.upb;
+        const int ub = stage_req[s];
         const int ui = unit - ub * p.upb;
         if (ub != cur) {
           cur = ub;
@@ -343,6 +357,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
           }
         }
         const int tw = ui * TPU + 16 * warp;   // this warp's first token
+        bool released = false;
         if (ok && tw < T) {
           const int row0 = (16 * warp) & (kPage - 1);
           const uint32_t tile = smem_u32(ring + s * kUnitBytes + ((16 * warp) >> 6) * 8192);
@@ -360,19 +375,43 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
           }
+          // The stage has been read into registers: hand it back to the
+          // producer before the scores are written.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
+          released = true;
           const int t_lo = tw + gr, t_hi = tw + gr + 8;
+          const bool full = tw + 16 <= T;   // the warp's 16 tokens all lie inside the sequence
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const int g = nt * 4 + qc;
+            const float s_lo = acc[nt][0] + acc[nt][1];
+            const float s_hi = acc[nt][2] + acc[nt][3];
             if (g < NGR) {
               float* srow = p.scores + (static_cast<long long>(b) * p.Hkv + g) * p.Tmax;
-              if (t_lo < T) srow[t_lo] = acc[nt][0] + acc[nt][1];
-              if (t_hi < T) srow[t_hi] = acc[nt][2] + acc[nt][3];
+              if (full || t_lo < T) st_hint(srow + t_lo, s_lo, keep_pol);
+              if (full || t_hi < T) st_hint(srow + t_hi, s_hi, keep_pol);
+            }
+            if (p.bmax) {
+              // The largest of the warp's 16 scores of group g (lanes with
+              // this qc, rows gr and gr + 8): the very values stored above,
+              // combined with fmaxf, which passes over NaN and positions
+              // past the sequence (NaN here) as the top-k's keys rank NaN
+              // lowest.
+              const float nan = __int_as_float(0x7fffffff);
+              float m = full ? fmaxf(s_lo, s_hi) : fmaxf(t_lo < T ? s_lo : nan, t_hi < T ? s_hi : nan);
+              m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+              m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+              m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
+              if (gr == 0 && g < NGR)
+                st_hint(p.bmax + (static_cast<long long>(b) * p.Hkv + g) * p.nbr + (tw >> 4), m, keep_pol);
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (!released) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
         if (++s == p.nst) {
           s = 0;
           ++fill;
@@ -398,7 +437,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
       if (!ok && lane == 0) flag_error(p.err, 8u);
       const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
       if (unit < 0) break;
-      const int ub = unit / p.upb;
+      const int ub = stage_req[s];
       const int ui = unit - ub * p.upb;
       if (ub != cur) {
         cur = ub;
@@ -425,6 +464,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
       }
 
       const int tbase = ui * TPU;
+      bool released = false;
       if (ok && tbase < T) {
         const unsigned char* src = ring + s * kUnitBytes + (warp * U) * 512 + lane * 16;
         float acc[V];
@@ -445,6 +485,11 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
             acc[uu * NGR + n] = a.x + a.y;
           }
         }
+        // The stage has been read into registers: hand it back to the
+        // producer before the sums are combined and written.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        released = true;
         transposed_reduce<LPR, V>(acc);
 #pragma unroll
         for (int kk = 0; kk < PER; ++kk) {
@@ -454,11 +499,13 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
           const int n = v % NGR;
           const int t = tbase + ((warp * U + uu) / PPT) * TPI + tok_off;
           const int g = (NGR == 1) ? head_of(uu) : n;
-          if (writer && t < T) p.scores[(static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t] = acc[kk];
+          if (writer && t < T) st_hint(p.scores + (static_cast<long long>(b) * p.Hkv + g) * p.Tmax + t, acc[kk], keep_pol);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (!released) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
       if (++s == p.nst) {
         s = 0;
         ++fill;
@@ -588,6 +635,12 @@ cudaError_t allow_smem(KernelFn fn, int bytes) {
 
 }  // namespace
 
+bool index_score_block_maxima(int C, int HL, int Hkv) {
+  int tpi = 0;
+  bool mma = false;
+  return select_kernel(C, HL, Hkv, &tpi, &mma) != nullptr && mma;
+}
+
 bool index_score_supported(int C, int HL, int Hkv, int G) {
   (void)G;
   int tpi = 0;
@@ -625,6 +678,8 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (mma) {
     const cudaError_t te = key_tensor_map(&p.tmap, a.label, static_cast<long long>(a.num_pages) * kPage);
     if (te != cudaSuccess) return te;
+    p.bmax = a.bmax;
+    p.nbr = (a.Tmax + kMaxBlock - 1) / kMaxBlock;
   }
   // Two CTAs per SM, each with a ring of 7 x 16 KB stages (6 on the
   // tensor-core path, which aligns the ring to 1024 bytes).

@@ -54,6 +54,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPerF = 32;                     // scores per lane per step of the filtered pass
 constexpr int kStep = 32 * kPerF;             // keys of one warp step of the filtered pass
 constexpr int kWarpCap = kListCap / kWarps;   // (key, token) pairs one warp keeps in the filtered pass
+constexpr int kBmPer = 8;                     // block maxima per thread (block-maxima filter)
+constexpr int kBmCap = kThreads * kBmPer;     // 16-token blocks of a CTA slice that takes the block-maxima filter
+constexpr int kGatherPer = 2;                 // candidate blocks per thread read in one round trip
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -74,6 +77,8 @@ struct TopkParams {
   float2* sscale;  // [R, k]
   int maxp, num_pages;
   int pre_wait;    // inputs may be read before the previous kernel completes
+  const float* bmax;   // [R, nbr] maxima of the rows' 16-token blocks, or null
+  int nbr;
 };
 
 struct __align__(16) Smem {
@@ -94,6 +99,21 @@ struct __align__(16) Smem {
   uint2 list[kListCap];
 };
 constexpr int kZeroWords = 4 * kBins1 + 2 * kBins3;   // h1 .. t3
+
+// Shared memory the filtered variant adds after Smem: the block-maxima filter.
+struct __align__(16) FiltX {
+  unsigned hm[kBins1];              // first-digit histogram of this CTA's block maxima, bin b at hslot(b)
+  unsigned tm[kBins1];              // row totals of the maxima bins this CTA owns, bin b at b
+  unsigned short cblk[kBmCap];      // the slice's candidate blocks, in token order
+};
+
+// The smallest score whose key is `key` (a multiple of 2^21). For the keys of
+// bins 1..3 that float is a NaN bit pattern, while every score but NaN has a
+// key in bin 3 or above (-inf's key is 0x007fffff): those bins, like bin 0,
+// take every key.
+__device__ __forceinline__ float key_floor(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
 // Keys of one thread's share of a tile of NT threads x N scores starting at
 // token `base` of a row: group i (4 consecutive scores) of thread r is tokens
@@ -245,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
   {
     uint4* z = reinterpret_cast<uint4*>(S.h1);
     for (int i = tid; i < kZeroWords / 4; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (FILT) {
+      uint4* zx = reinterpret_cast<uint4*>(dsm + sizeof(Smem));   // FiltX::hm and ::tm
+      for (int i = tid; i < 2 * kBins1 / 4; i += kThreads) zx[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (tid == 0) {
       S.lmax = 0u;
       S.res[0] = 0u;
@@ -306,136 +330,246 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
   if (FILT && filtered_row(SLr, keff, T)) {
     const int warp = tid >> 5, lane = tid & 31;
     const int len = s1 - s0;
-    // Warp w owns the contiguous token range [w0, w1) of the slice, in tiles
-    // of kStep keys (kPerF per lane), so each warp appends its candidates in
-    // token order without block-wide barriers.
-    const int SW = ((len + kWarps - 1) / kWarps + kStep - 1) / kStep * kStep;
-    const int w0 = min(s1, s0 + warp * SW), w1 = min(s1, w0 + SW);
-    const int nst = (w1 - w0 + kStep - 1) / kStep;
-    // The tiles stay raw floats: order_key is monotone, so key >= lb is
-    // compared as score >= the float of key lb, and only candidates are
-    // converted.
-    float4 raw[kPerF / 4];
-    float cur[kPerF];
-    auto tile_floats = [&]() {
+    // With the scan's block maxima (slices of at most kBmCap blocks), the
+    // filter bin is exact instead of guessed: the first-digit bin where the
+    // row's block maxima, counted from the top, reach K_eff. Each of those
+    // blocks holds its maximum, so at least K_eff keys lie in that bin or
+    // above and so does the threshold; only blocks whose maximum reaches the
+    // bin can hold a kept key, and only they are read.
+    const bool bm_path = p.bmax != nullptr && SLr <= kMaxBlock * kBmCap;
+    uint2* sub = S.list + warp * kWarpCap;   // sample path: this warp's candidates, in token order
+    unsigned n = 0;    // sample path: this warp's candidates so far (only the first kWarpCap are kept)
+    unsigned mc = 0;   // block-maxima path: the CTA's candidates (only the first kListCap are kept)
+    unsigned lbin = 0;
+    if (bm_path) {
+      FiltX& X = *reinterpret_cast<FiltX*>(dsm + sizeof(Smem));
+      const int nbk = (len + kMaxBlock - 1) / kMaxBlock;   // s0 is a multiple of 16
+      const float* bm = p.bmax + static_cast<long long>(row) * p.nbr + s0 / kMaxBlock;
+      uint32_t mk[kBmPer];
 #pragma unroll
-      for (int i = 0; i < kPerF / 4; ++i) {
-        cur[4 * i] = raw[i].x;
-        cur[4 * i + 1] = raw[i].y;
-        cur[4 * i + 2] = raw[i].z;
-        cur[4 * i + 3] = raw[i].w;
+      for (int i = 0; i < kBmPer; ++i) {
+        const int blk = tid * kBmPer + i;
+        mk[i] = blk < nbk ? order_key(__ldcg(bm + blk)) : 0u;
+        warp_hist_add_grouped(X.hm, mk[i] >> 21, blk < nbk);
       }
-    };
-    if (nst > 0) load_tile<kPerF / 4, 32>(s, w0, lane, w1, raw);
-    tile_floats();
-    // Sample: the largest key of each lane's share of the first tile. The filter bin
-    // is where the sampled maxima, counted from the top, reach twice this
-    // slice's share of K_eff scaled to a pass of kBatch keys (0, no filter,
-    // when they never do). Fewer maxima than keys lie above any bin, so the
-    // guess errs low.
-    {
-      float mx = __int_as_float(0x7fffffff);   // NaN: fmaxf keeps the other operand
-      bool any = false;
+      __syncthreads();
+      cluster_wait();
+      push_bins<kBins1>(X.hm, X.tm, cs);
+      cluster_sync();
+      {
+        unsigned c[4];
+        read_totals<kBins1, 4>(X.tm, cs, c);
+        find_crossing<kBins1, 4>(c, static_cast<unsigned>(keff), S);   // the row has at least 8 K_eff blocks
+      }
+      lbin = S.res[0];
+      cluster_arrive();   // no more reads of the maxima totals; paired with the wait before the next push
+      // The candidate blocks (maximum in the bin or above), in token order.
+      const uint32_t lb = lbin << 21;
+      unsigned cnt = 0;
 #pragma unroll
-      for (int i = 0; i < kPerF; ++i) {
-        if (tile_token<32>(w0, lane, i) < w1) {
-          mx = fmaxf(mx, cur[i]);
-          any = true;
+      for (int i = 0; i < kBmPer; ++i) cnt += (tid * kBmPer + i < nbk && mk[i] >= lb) ? 1u : 0u;
+      unsigned nc;
+      unsigned pos = block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &nc);
+#pragma unroll
+      for (int i = 0; i < kBmPer; ++i)
+        if (tid * kBmPer + i < nbk && mk[i] >= lb) X.cblk[pos++] = static_cast<unsigned short>(tid * kBmPer + i);
+      __syncthreads();
+      // Their keys in the bin or above, appended in token order.
+      const float flb = key_floor(lb);
+      const bool take_all = lbin < 4u;
+      const bool al = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
+      // The 16 scores of the block at token tb (none past s1) and the mask of its candidates.
+      auto load_block = [&](int tb, float (&v)[kMaxBlock]) {
+        if (al && tb + kMaxBlock <= s1) {
+#pragma unroll
+          for (int j = 0; j < kMaxBlock / 4; ++j) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(s + tb) + j);
+            v[4 * j] = f.x;
+            v[4 * j + 1] = f.y;
+            v[4 * j + 2] = f.z;
+            v[4 * j + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kMaxBlock; ++j) v[j] = tb + j < s1 ? __ldcg(s + tb + j) : 0.f;
         }
-      }
-      warp_hist_add(S.h2, order_key(mx) >> 21, any);
-    }
-    __syncthreads();
-    const unsigned want =
-        len > 0 ? static_cast<unsigned>((2LL * keff * kThreads * kPerF + static_cast<long long>(cs) * len - 1) /
-                                        (static_cast<long long>(cs) * len))
-                : 0u;
-    {
-      const int hi = kBins1 - 4 * tid;
-      unsigned c[4], sum = 0;
+      };
+      auto block_mask = [&](int tb, const float (&v)[kMaxBlock]) {
+        unsigned m = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        c[j] = S.h2[hslot(hi - 1 - j)];
-        sum += c[j];
+        for (int j = 0; j < kMaxBlock; ++j)
+          if ((take_all || v[j] >= flb) && tb + j < s1) m |= 1u << j;
+        return m;
+      };
+      auto append = [&](int tb, const float (&v)[kMaxBlock], unsigned m, unsigned& q) {
+#pragma unroll
+        for (int j = 0; j < kMaxBlock; ++j) {
+          if ((m >> j) & 1u) {
+            if (q < static_cast<unsigned>(kListCap)) S.list[q] = make_uint2(order_key(v[j]), static_cast<unsigned>(tb + j));
+            ++q;
+          }
+        }
+      };
+      // Batches of up to kGatherPer * kThreads candidate blocks: in a batch
+      // thread t owns a run of at most kGatherPer consecutive blocks and
+      // issues all their loads before using any, one round trip per batch.
+      for (int cb = 0; cb < static_cast<int>(nc); cb += kGatherPer * kThreads) {
+        const int nb_ = min(static_cast<int>(nc) - cb, kGatherPer * kThreads);
+        const int per = (nb_ + kThreads - 1) / kThreads;
+        const int c0 = cb + min(nb_, tid * per), c1 = cb + min(nb_, tid * per + per);
+        float v[kGatherPer][kMaxBlock];
+        int tb[kGatherPer];
+#pragma unroll
+        for (int u = 0; u < kGatherPer; ++u) {
+          tb[u] = c0 + u < c1 ? s0 + kMaxBlock * static_cast<int>(X.cblk[c0 + u]) : s1;   // s1: nothing to load
+          load_block(tb[u], v[u]);
+        }
+        unsigned m[kGatherPer], cnt = 0;
+#pragma unroll
+        for (int u = 0; u < kGatherPer; ++u) {
+          m[u] = block_mask(tb[u], v[u]);
+          cnt += static_cast<unsigned>(__popc(m[u]));
+        }
+        unsigned tot;
+        unsigned q = mc + block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &tot);
+#pragma unroll
+        for (int u = 0; u < kGatherPer; ++u) append(tb[u], v[u], m[u], q);
+        mc += tot;
       }
-      unsigned tot;
-      unsigned run = block_excl_scan(sum, reinterpret_cast<unsigned*>(S.scan), &tot);
-      if (want > 0 && run < want && run + sum >= want) {
+      __syncthreads();
+      // Digit-1 histogram of the candidates (an overflowing list is not used);
+      // most of them share a bin or two.
+      const unsigned lim = min(mc, static_cast<unsigned>(kListCap));
+      for (unsigned e0 = 0; e0 < lim; e0 += kThreads) {
+        const unsigned e = e0 + static_cast<unsigned>(tid);
+        warp_hist_add_grouped(S.h1, e < lim ? S.list[e].x >> 21 : 0u, e < lim);
+      }
+    } else {
+      // Warp w owns the contiguous token range [w0, w1) of the slice, in tiles
+      // of kStep keys (kPerF per lane), so each warp appends its candidates in
+      // token order without block-wide barriers.
+      const int SW = ((len + kWarps - 1) / kWarps + kStep - 1) / kStep * kStep;
+      const int w0 = min(s1, s0 + warp * SW), w1 = min(s1, w0 + SW);
+      const int nst = (w1 - w0 + kStep - 1) / kStep;
+      // The tiles stay raw floats: order_key is monotone, so key >= lb is
+      // compared as score >= the float of key lb, and only candidates are
+      // converted.
+      float4 raw[kPerF / 4];
+      float cur[kPerF];
+      auto tile_floats = [&]() {
+#pragma unroll
+        for (int i = 0; i < kPerF / 4; ++i) {
+          cur[4 * i] = raw[i].x;
+          cur[4 * i + 1] = raw[i].y;
+          cur[4 * i + 2] = raw[i].z;
+          cur[4 * i + 3] = raw[i].w;
+        }
+      };
+      if (nst > 0) load_tile<kPerF / 4, 32>(s, w0, lane, w1, raw);
+      tile_floats();
+      // Sample: the largest key of each lane's share of the first tile. The filter bin
+      // is where the sampled maxima, counted from the top, reach twice this
+      // slice's share of K_eff scaled to a pass of kBatch keys (0, no filter,
+      // when they never do). Fewer maxima than keys lie above any bin, so the
+      // guess errs low.
+      {
+        float mx = __int_as_float(0x7fffffff);   // NaN: fmaxf keeps the other operand
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < kPerF; ++i) {
+          if (tile_token<32>(w0, lane, i) < w1) {
+            mx = fmaxf(mx, cur[i]);
+            any = true;
+          }
+        }
+        warp_hist_add(S.h2, order_key(mx) >> 21, any);
+      }
+      __syncthreads();
+      const unsigned want =
+          len > 0 ? static_cast<unsigned>((2LL * keff * kThreads * kPerF + static_cast<long long>(cs) * len - 1) /
+                                          (static_cast<long long>(cs) * len))
+                  : 0u;
+      {
+        const int hi = kBins1 - 4 * tid;
+        unsigned c[4], sum = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (run + c[j] >= want) {
-            S.res[0] = static_cast<unsigned>(hi - 1 - j);
-            break;
-          }
-          run += c[j];
+          c[j] = S.h2[hslot(hi - 1 - j)];
+          sum += c[j];
         }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) S.h2[hslot(hi - 1 - j)] = 0u;   // digit 2 starts from zero
-    }
-    __syncthreads();
-    const unsigned lbin = S.res[0];
-    const uint32_t lb = lbin << 21;
-    // The smallest score whose key is lb. For bins 1..3 that float is a NaN
-    // bit pattern, while every score but NaN has a key in bin 3 or above
-    // (-inf's key is 0x007fffff): those bins, like bin 0 (no filter), take
-    // every key.
-    const float flb = __uint_as_float((lb & 0x80000000u) ? (lb & 0x7fffffffu) : ~lb);
-    const bool take_all = lbin < 4u;
-    // ---- the filtered pass: the candidate list of the keys >= lb, then their digit-1 histogram
-    uint2* sub = S.list + warp * kWarpCap;
-    unsigned n = 0;   // this warp's candidates so far (only the first kWarpCap are kept)
-    for (int st = 0; st < nst; ++st) {
-      const int tb = w0 + st * kStep;
-      if (st > 0) tile_floats();
-      if (st + 1 < nst) load_tile<kPerF / 4, 32>(s, tb + kStep, lane, w1, raw);
-      // Group g of the tile (4 keys per lane) is 128 contiguous tokens, lane
-      // by lane: a warp ballot per key index gives every lane the number of
-      // candidates before its own, and groups without any are skipped.
-      const bool full = tb + kStep <= w1;
-#pragma unroll
-      for (int g = 0; g < kPerF / 4; ++g) {
-        bool tk[4];
-        unsigned bal[4], any = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tk[j] = (take_all || cur[4 * g + j] >= flb) && (full || tile_token<32>(tb, lane, 4 * g + j) < w1);
-          bal[j] = __ballot_sync(kFull, tk[j]);
-          any |= bal[j];
-        }
-        if (any) {
-          const unsigned lt = (1u << lane) - 1u;
-          unsigned q = n, tot = 0;
+        unsigned tot;
+        unsigned run = block_excl_scan(sum, reinterpret_cast<unsigned*>(S.scan), &tot);
+        if (want > 0 && run < want && run + sum >= want) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            q += __popc(bal[j] & lt);
-            tot += __popc(bal[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (tk[j]) {
-              if (q < static_cast<unsigned>(kWarpCap))
-                sub[q] = make_uint2(order_key(cur[4 * g + j]),
-                                    static_cast<unsigned>(tile_token<32>(tb, lane, 4 * g + j)));
-              ++q;
+            if (run + c[j] >= want) {
+              S.res[0] = static_cast<unsigned>(hi - 1 - j);
+              break;
             }
+            run += c[j];
           }
-          n += tot;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) S.h2[hslot(hi - 1 - j)] = 0u;   // digit 2 starts from zero
+      }
+      __syncthreads();
+      lbin = S.res[0];
+      const float flb = key_floor(lbin << 21);
+      const bool take_all = lbin < 4u;
+      // ---- the filtered pass: the candidate list of the keys >= lb, then their digit-1 histogram
+      for (int st = 0; st < nst; ++st) {
+        const int tb = w0 + st * kStep;
+        if (st > 0) tile_floats();
+        if (st + 1 < nst) load_tile<kPerF / 4, 32>(s, tb + kStep, lane, w1, raw);
+        // Group g of the tile (4 keys per lane) is 128 contiguous tokens, lane
+        // by lane: a warp ballot per key index gives every lane the number of
+        // candidates before its own, and groups without any are skipped.
+        const bool full = tb + kStep <= w1;
+#pragma unroll
+        for (int g = 0; g < kPerF / 4; ++g) {
+          bool tk[4];
+          unsigned bal[4], any = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tk[j] = (take_all || cur[4 * g + j] >= flb) && (full || tile_token<32>(tb, lane, 4 * g + j) < w1);
+            bal[j] = __ballot_sync(kFull, tk[j]);
+            any |= bal[j];
+          }
+          if (any) {
+            const unsigned lt = (1u << lane) - 1u;
+            unsigned q = n, tot = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              q += __popc(bal[j] & lt);
+              tot += __popc(bal[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (tk[j]) {
+                if (q < static_cast<unsigned>(kWarpCap))
+                  sub[q] = make_uint2(order_key(cur[4 * g + j]),
+                                      static_cast<unsigned>(tile_token<32>(tb, lane, 4 * g + j)));
+                ++q;
+              }
+            }
+            n += tot;
+          }
         }
       }
+      // Digit-1 histogram of the candidates (an overflowing list is not used).
+      for (unsigned e = static_cast<unsigned>(lane); e < min(n, static_cast<unsigned>(kWarpCap)); e += 32)
+        atomicAdd(S.h1 + hslot(static_cast<int>(sub[e].x >> 21)), 1u);
+      if (lane == 0) S.wcnt[warp] = n;
     }
-    // Digit-1 histogram of the candidates (an overflowing list is not used).
-    for (unsigned e = static_cast<unsigned>(lane); e < min(n, static_cast<unsigned>(kWarpCap)); e += 32)
-      atomicAdd(S.h1 + hslot(static_cast<int>(sub[e].x >> 21)), 1u);
-    if (lane == 0) S.wcnt[warp] = n;
     __syncthreads();
     cluster_wait();
     push_bins<kBins1>(S.h1, S.t1, cs);
     if (tid == 0) {
-      // This CTA's filter bin into rank 0's maximum; a warp list that
-      // overflowed posts one past the last bin, which fails the check.
-      bool over = false;
-      for (int w = 0; w < kWarps; ++w) over |= S.wcnt[w] > static_cast<unsigned>(kWarpCap);
+      // This CTA's filter bin into rank 0's maximum; a list that overflowed
+      // posts one past the last bin, which fails the check.
+      bool over = mc > static_cast<unsigned>(kListCap);
+      if (!bm_path)
+        for (int w = 0; w < kWarps; ++w) over |= S.wcnt[w] > static_cast<unsigned>(kWarpCap);
       cluster_red_max(cluster_map(smem_u32(&S.lmax), 0u), over ? static_cast<unsigned>(kBins1) : lbin);
       S.res[0] = 0xffffffffu;   // no crossing yet
     }
@@ -452,7 +586,16 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     // totals are exact from lmax up; a crossing there is the true one, and
     // every list holds all keys of its slice whose first digit reaches it.
     filtered = b1 != 0xffffffffu && b1 >= lmax;
-    if (filtered) {
+    if (filtered && bm_path) {
+      // One token-ordered list already; its entries below b1 fail every
+      // later test (digit 2 and 3 match on the higher digits, the output
+      // compares with the threshold), so it is used as it is.
+      M = mc;
+      for (int e = tid; e < static_cast<int>(M); e += kThreads) {
+        const uint32_t key = S.list[e].x;
+        warp_hist_add(S.h2, (key >> 10) & 2047u, (key >> 21) == b1);
+      }
+    } else if (filtered) {
       // The warps' lists, concatenated in warp (= token) order, keeping only
       // the entries whose first digit reaches b1 (the filter bin may lie
       // below it). In place, through registers: a warp's destination may
@@ -757,7 +900,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.maxp = a.maxp;
   p.num_pages = a.num_pages;
   p.pre_wait = a.pre_wait;
+  p.bmax = a.bmax;
+  p.nbr = (a.Tmax + kMaxBlock - 1) / kMaxBlock;
   const int smem = static_cast<int>(sizeof(Smem));
+  const int smem_f = static_cast<int>(sizeof(Smem) + sizeof(FiltX));   // the filtered variant
   // Cluster size: one pass of kBatch scores per CTA where possible, but no
   // more clusters than the device keeps resident at once (a second wave would
   // double the latency-bound selection). The occupancy query assumes an empty
@@ -777,8 +923,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   bool filt = false;
   int cs = 1;
   const long long keff_max = a.k < a.Tmax ? a.k : a.Tmax;
-  if (filtered_row(2 * kBatch, keff_max, a.Tmax) && resident_clusters<true>(1, smem) > 0) {
-    cs = cluster_size([&](int c) { return resident_clusters<true>(c, smem); });
+  if (filtered_row(2 * kBatch, keff_max, a.Tmax) && resident_clusters<true>(1, smem_f) > 0) {
+    cs = cluster_size([&](int c) { return resident_clusters<true>(c, smem_f); });
     filt = filtered_row(((a.Tmax + cs - 1) / cs + 15) & ~15, keff_max, a.Tmax);
   }
   if (!filt) {
@@ -789,7 +935,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(R * cs));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = filt ? smem_f : smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
