@@ -280,15 +280,11 @@ typedef struct {
  * The whole decode step: ds_index_score -> ds_topk_select ->
  * ds_sparse_decode_attn (internal split-KV chosen for occupancy) ->
  * ds_lse_merge, on one stream, with scores in `workspace`
- * (at least ds_decode_workspace_bytes bytes, 256-byte aligned). The
- * workspace holds the scan's work counters, which must be zero before its
- * first use (e.g. cudaMemsetAsync(workspace, 0, bytes) once); every call
- * leaves them zero again, so it is reused without clearing. The splits of
- * each (request, KV head) run as one thread-block cluster and merge in
- * on-chip shared memory. Calls sharing one workspace must not overlap on the
- * GPU. No host synchronisation
- * and no allocation, so the call can be captured in a CUDA graph and replayed
- * with new input contents.
+ * (at least ds_decode_workspace_bytes bytes, 256-byte aligned; its contents
+ * need no initialisation). The splits of each (request, KV head) run as one
+ * thread-block cluster and merge in on-chip shared memory. Calls sharing one
+ * workspace must not overlap on the GPU. No host synchronisation and no
+ * allocation.
  */
 size_t ds_decode_workspace_bytes(const ds_shape* shape, int proxy_dim, int k);
 ds_status ds_sparse_decode(const ds_shape* shape, const ds_decode_args* args, void* workspace,

@@ -60,7 +60,8 @@ def run_decode(inp_gpu, shape, k):
     idx = torch.full((w.batch, w.num_kv_heads, k), -7, dtype=torch.int32, device=dev)
     out = torch.full((w.batch, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.bfloat16, device=dev)
     lse = torch.full((w.batch, w.num_q_heads), float("nan"), dtype=torch.float32, device=dev)
-    ws = torch.zeros(ds.ds_decode_workspace_bytes(shape, w.proxy_dim, k), dtype=torch.uint8, device=dev)
+    # Stale bytes: the chained call needs no initialised workspace.
+    ws = torch.full((ds.ds_decode_workspace_bytes(shape, w.proxy_dim, k),), 0xA5, dtype=torch.uint8, device=dev)
     ds.ds_sparse_decode(shape, inp_gpu.q, inp_gpu.qp, inp_gpu.label, inp_gpu.k_cache, inp_gpu.v_cache,
                         inp_gpu.k_scale, inp_gpu.v_scale, inp_gpu.page_table, inp_gpu.seq_lens, k, idx, out, lse,
                         ws)

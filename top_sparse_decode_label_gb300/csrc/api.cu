@@ -284,11 +284,9 @@ ds_status ds_cache_append(const ds_shape* shape, const void* k_new, const void* 
 
 namespace {
 
-// Workspace of the chained call: the scan's unit counters (zero before the
-// first call, left zero by every call), the scores and their 16-token block
-// maxima, the top-k overflow lists and the physical slots of the selection.
+// Workspace of the chained call: the scores and their 16-token block maxima,
+// the top-k overflow lists and the physical slots of the selection.
 struct DecodeLayout {
-  unsigned* work;   // [2]
   float* scores;
   float* bmax;      // [B, Hkv, ceil(max_seq_len / 16)]
   TopkLayout topk;
@@ -302,8 +300,6 @@ DecodeLayout decode_layout(const ds_shape* s, int k, void* base) {
   char* p = static_cast<char*>(base);
   const int R = s->batch * s->num_kv_heads;
   size_t off = 0;
-  L.work = reinterpret_cast<unsigned*>(p + off);
-  off = align256(off + 2 * sizeof(unsigned));
   L.scores = reinterpret_cast<float*>(p + off);
   off = align256(off + static_cast<size_t>(R) * (s->max_seq_len > 0 ? s->max_seq_len : 1) * 4);
   L.bmax = reinterpret_cast<float*>(p + off);
@@ -377,7 +373,7 @@ static ds_status decode_impl(const ds_shape* shape, const ds_decode_args* args, 
   if (shape->max_seq_len > 0) {
     ScoreArgs sa{args->qp, args->label, args->page_table, args->seq_lens, L.scores, err, shape->batch,
                  shape->num_q_heads, shape->num_kv_heads, args->label_heads, pd, shape->max_pages_per_req,
-                 shape->num_pages, shape->max_seq_len, L.work, L.bmax};
+                 shape->num_pages, shape->max_seq_len, L.bmax};
     st = from_cuda(launch_index_score(sa, s));
     if (st != DS_OK) return st;
   }

@@ -33,7 +33,6 @@ struct ScoreArgs {
   float* scores;           // [B, Hkv, Tmax]
   unsigned* err;
   int B, Hq, Hkv, HL, C, maxp, num_pages, Tmax;
-  unsigned* work;          // [2] zeroed unit counters (left zero): dynamic unit scheduling; null: static
   float* bmax;             // [B, Hkv, ceil(Tmax / 16)] largest score of each 16-token block, or null
                            // (written only by kernels for which index_score_block_maxima is true)
 };

@@ -13,18 +13,18 @@
 // HBM-bound scan. The label rows are read once, with an evict-first L2
 // policy; the scores are written with an evict-last one, so that the top-k
 // after the scan reads them from L2. The label cache is cut into 16 KB units
-// of whole token rows (HL*C*2 bytes each) of one request. A persistent grid
-// takes the units in chunks of consecutive units: with a work counter (chained call) each
-// CTA's first chunk is fixed and later ones are claimed with one atomicAdd, a
-// chunk ahead, so faster CTAs take more work; the last two units per CTA go
-// out one at a time, so all CTAs finish together (the last CTA to finish
-// rearms the counter); without a counter each CTA takes a contiguous range. In each CTA a producer warp loads the page ids of a
-// chunk's pages together, a chunk before they are needed, and streams the
-// units into a ring of shared-memory stages with bulk copies -- one per page
-// span -- that complete on the stage's mbarrier; eight consumer warps wait on
-// it, compute, and release the stage through a second mbarrier, so copies run
-// ahead by the ring depth with no CTA-wide barrier per unit; each stage
-// carries its unit number, and a stage marked -1 ends the consumers.
+// of whole token rows (HL*C*2 bytes each) of one request; only units that
+// hold tokens of a sequence count. A persistent grid splits them evenly: CTA
+// c takes a contiguous range of them in request order (a shared counter with
+// dynamic claims was measured slower: its returning atomics queue at one L2
+// address). In each CTA a producer warp loads the page ids of a chunk's pages
+// together, a chunk before they are needed, and streams the units into a
+// ring of shared-memory stages with bulk copies -- one per page span -- that
+// complete on the stage's mbarrier; eight consumer warps wait on it, read it
+// into registers, release it through a second mbarrier and then compute, so
+// copies run ahead by the ring depth with no CTA-wide barrier per unit; each
+// stage carries its unit's request and index, and a stage marked -1 ends the
+// consumers.
 //
 // CUDA-core consumers: each warp reads 4 consecutive 512-byte pieces of a
 // unit; C/8 lanes hold one C-wide row (one head of one token), every lane
@@ -58,7 +58,7 @@ constexpr int kScoreThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kUnitBytes = 16384;                     // 32 pieces of 512 B
 constexpr int kMaxStages = 12;
 constexpr uint32_t kWaitLimit = 1u << 22;             // bounded mbarrier polls
-constexpr int kChunkUnits = 4;                        // units a CTA takes per dynamic fetch
+constexpr int kChunkUnits = 4;                        // units whose page ids are loaded together
 
 struct ScoreParams {
   CUtensorMap tmap;   // tensor-core path: the key cache as [slots, 64] bf16 rows, 64 x 64 boxes, 128-byte swizzle
@@ -69,9 +69,6 @@ struct ScoreParams {
   float* scores;
   unsigned* err;
   int B, Hq, Hkv, HL, maxp, num_pages, Tmax;
-  unsigned* work;   // [2]: next unit, finished CTAs (zero between calls); null: static unit ranges
-  int units;        // B * upb (< 2^31, checked on the host)
-  int upb;          // units per request
   int nst;          // ring stages
   float* bmax;      // tensor-core path: [B, Hkv, nbr] maxima of 16-token blocks, or null
   int nbr;          // blocks per row of bmax: ceil(Tmax / 16)
@@ -112,8 +109,6 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.units / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.units / gridDim.x);
 
   if (tid == 0) {
     for (int s = 0; s < p.nst; ++s) {
@@ -132,87 +127,77 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
   const uint64_t keep_pol = l2_evict_last();
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
-    // Units come in chunks of kChunkUnits consecutive units. The page ids of
-    // a chunk's pages are loaded together, one lane per page, one chunk
-    // before the chunk is copied, and dynamic chunk claims are also issued a
-    // chunk ahead, so no global round trip sits on the per-unit path; the
-    // ring of stages covers the one round trip per chunk that remains.
+    // The work is the valid units of all requests in request order (a
+    // request of T tokens has ceil(T / TPU) of them) and this CTA takes an
+    // equal contiguous share: no global counter, no units past a sequence.
+    // The units come in chunks of kChunkUnits; the page ids of a chunk's
+    // pages are loaded together, one lane per page, a chunk before the chunk
+    // is copied, so no global round trip sits on the per-unit path.
     constexpr int PPU = TPU >= kPage ? TPU / kPage : 1;   // pages per unit
     static_assert(PPU * kChunkUnits <= 32, "one lane per page of a chunk");
-    // Sequence lengths of up to 32 requests, one per lane (clamped).
-    const int Tl = lane < p.B ? clamp_len(p, lane) : 0;
-    auto seq_len = [&](int b) { return p.B <= 32 ? __shfl_sync(kFull, Tl, b & 31) : clamp_len(p, b); };
-    // Chunk ranges: static -- the CTA's own range [u0, u1) cut in chunks;
-    // dynamic -- each CTA's first chunk is fixed, later ones come from the
-    // counter (offset past the fixed ones).
-    int su = u0;
-    auto first_chunk = [&](int& a, int& e) {
-      if (p.work) {
-        a = blockIdx.x * kChunkUnits;
-        e = min(p.units, a + kChunkUnits);
-        if (a > e) a = e;
-      } else {
-        a = su;
-        e = min(u1, su + kChunkUnits);
-        su = e;
+    // upre[b]: valid units of the requests before b (upre[B]: all of them);
+    // ulen[b]: request b's length, clamped.
+    int* upre = reinterpret_cast<int*>(smem + p.nst * kUnitBytes + (MMA ? 1024 : 0));
+    int* ulen = upre + p.B + 1;
+    int carry = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int rb = b0 + lane;
+      const int T = rb < p.B ? clamp_len(p, rb) : 0;
+      const int nv = (T + TPU - 1) / TPU;
+      const int inc = static_cast<int>(warp_incl_scan(static_cast<unsigned>(nv)));
+      if (rb < p.B) {
+        upre[rb] = carry + inc - nv;
+        ulen[rb] = T;
       }
-    };
-    auto claim = [&](int sz) -> int {   // dynamic: counter value (lane 0), resolved later
-      int base = 0;
-      if (p.work && lane == 0) base = static_cast<int>(atomicAdd(p.work, static_cast<unsigned>(sz)));
-      return base;
-    };
-    auto resolve = [&](int claimed, int sz, int& a, int& e) {
-      if (p.work) {
-        const long long base = static_cast<long long>(__shfl_sync(kFull, claimed, 0)) +
-                               static_cast<long long>(gridDim.x) * kChunkUnits;
-        a = static_cast<int>(base < p.units ? base : p.units);
-        e = min(p.units, a + sz);
-      } else {
-        a = su;
-        e = min(u1, su + kChunkUnits);
-        su = e;
-      }
-    };
-    // Page id for lane l: page l % PPU of unit a + l / PPU (-1 past the sequence).
-    auto load_pids = [&](int a, int e) -> int {
-      const int u = a + lane / PPU;
-      const int b = u / p.upb;
-      const int T = seq_len(u < e ? b : 0);
+      carry += __shfl_sync(kFull, inc, 31);
+    }
+    if (lane == 0) upre[p.B] = carry;
+    __syncwarp();
+    const int v0 = static_cast<int>(static_cast<long long>(blockIdx.x) * carry / gridDim.x);
+    const int v1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * carry / gridDim.x);
+    // Lane l's unit of chunk [a, e) is a + l / PPU: its request rb (the last
+    // one with upre[rb] <= unit), its index rui in the request and the id of
+    // its page l % PPU (-1 past the sequence or the chunk).
+    auto load_chunk = [&](int a, int e, int& rb, int& rui) -> int {
+      const int v = a + lane / PPU;
       int pid = -1;
-      if (u < e) {
-        const int pg = (((u - b * p.upb) * TPU) >> 6) + lane % PPU;
-        if (pg * kPage < T) pid = __ldg(p.page_table + b * p.maxp + pg);
+      rb = 0;
+      rui = 0;
+      if (v < e) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (upre[mid] <= v) lo = mid;
+          else hi = mid - 1;
+        }
+        rb = lo;
+        rui = v - upre[lo];
+        const int pg = ((rui * TPU) >> 6) + lane % PPU;
+        if (pg * kPage < ulen[lo]) pid = __ldg(p.page_table + static_cast<long long>(lo) * p.maxp + pg);
       }
       return pid;
     };
-    int cu = 0, ce = 0, na = 0, ne = 0;
-    first_chunk(cu, ce);
-    // Near the end of the work, claims shrink to single units so that the
-    // CTAs finish together.
-    const int tail = 2 * static_cast<int>(gridDim.x);
-    int csz = kChunkUnits;
-    int claimed = claim(csz);
-    int cpid = load_pids(cu, ce);
-    resolve(claimed, csz, na, ne);
-    int npid = load_pids(na, ne);
+    int cu = v0, ce = min(v1, v0 + kChunkUnits);
+    int cb, cui, nb, nui;
+    int cpid = load_chunk(cu, ce, cb, cui);
+    int na = ce, ne = min(v1, na + kChunkUnits);
+    int npid = load_chunk(na, ne, nb, nui);
     int ca = cu;          // first unit of the current chunk
-    csz = p.units - na > tail ? kChunkUnits : 1;
-    claimed = claim(csz);    // the chunk after next
     int s = 0;
     uint32_t fill = 0;  // how many times stage s has been filled before
     for (;;) {
       if (cu >= ce && na < ne) {
         // Next chunk: its page ids were loaded a chunk ago; start loading the
-        // one after it, and claim another.
+        // one after it.
         cu = na;
         ce = ne;
         ca = cu;
         cpid = npid;
-        resolve(claimed, csz, na, ne);
-        npid = load_pids(na, ne);
-        csz = p.units - na > tail ? kChunkUnits : 1;
-        claimed = claim(csz);
+        cb = nb;
+        cui = nui;
+        na = ce;
+        ne = min(v1, na + kChunkUnits);
+        npid = load_chunk(na, ne, nb, nui);
       }
       const int unit = cu < ce ? cu++ : -1;
       if (fill > 0 && !mbar_wait(&empty_bar[s], (fill - 1) & 1u, kWaitLimit) && lane == 0)
@@ -225,12 +210,13 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         }
         break;
       }
-      const int b = unit / p.upb;
-      const int ui = unit - b * p.upb;
-      const int T = seq_len(b);
+      const int lane0 = (unit - ca) * PPU;   // lane of this unit's first page id
+      const int b = __shfl_sync(kFull, cb, lane0);
+      const int ui = __shfl_sync(kFull, cui, lane0);
+      const int T = ulen[b];
       const int t0 = ui * TPU;
       const int t1 = min(T, t0 + TPU);
-      const int pbase = (unit - ca) * PPU;   // lane of this unit's first page id
+      const int pbase = lane0;
       unsigned char* dst = ring + s * kUnitBytes;
       uint32_t nbytes = 0;
       const uint8_t* src = p.label;
@@ -252,7 +238,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
 #pragma unroll
         for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
         if (lane == 0) {
-          stage_unit[s] = unit;
+          stage_unit[s] = ui;
           stage_req[s] = b;
           mbar_arrive_expect_tx(&full_bar[s], total);
         }
@@ -283,7 +269,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
 #pragma unroll
       for (int o = 16; o; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
       if (lane == 0) {
-        stage_unit[s] = unit;
+        stage_unit[s] = ui;
         stage_req[s] = b;
         mbar_arrive_expect_tx(&full_bar[s], total);
       }
@@ -317,7 +303,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
         if (unit < 0) break;
         const int ub = stage_req[s];
-        const int ui = unit - ub * p.upb;
+        const int ui = unit;
         if (ub != cur) {
           cur = ub;
           b = ub;
@@ -438,7 +424,7 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
       const int unit = ok ? stage_unit[s] : -1;   // a wait that ran out stops this warp
       if (unit < 0) break;
       const int ub = stage_req[s];
-      const int ui = unit - ub * p.upb;
+      const int ui = unit;
       if (ub != cur) {
         cur = ub;
         b = ub;
@@ -511,16 +497,6 @@ __global__ void __launch_bounds__(kScoreThreads, (NGR >= 8 && !MMA) ? 1 : 2)
         ++fill;
       }
     }
-    }
-  }
-  __syncthreads();
-  if (p.work && tid == 0) {
-    // Every unit has been handed out; the last CTA to finish rearms the
-    // counters for the next call.
-    __threadfence();
-    if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
-      atomicExch(p.work, 0u);
-      atomicExch(p.work + 1, 0u);
     }
   }
 }
@@ -669,12 +645,10 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   p.maxp = a.maxp;
   p.num_pages = a.num_pages;
   p.Tmax = a.Tmax;
-  p.work = a.work;
+  // Units of all requests at their longest: their count must fit an int.
   const long long upb = (static_cast<long long>(a.maxp) * kPage + tpu - 1) / tpu;
   const long long units = static_cast<long long>(a.B) * upb;
   if (units >= (1LL << 31) || static_cast<long long>(a.B) * a.maxp >= (1LL << 31)) return cudaErrorNotSupported;
-  p.upb = static_cast<int>(upb);
-  p.units = static_cast<int>(units);
   if (mma) {
     const cudaError_t te = key_tensor_map(&p.tmap, a.label, static_cast<long long>(a.num_pages) * kPage);
     if (te != cudaSuccess) return te;
@@ -682,9 +656,10 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
     p.nbr = (a.Tmax + kMaxBlock - 1) / kMaxBlock;
   }
   // Two CTAs per SM, each with a ring of 7 x 16 KB stages (6 on the
-  // tensor-core path, which aligns the ring to 1024 bytes).
+  // tensor-core path, which aligns the ring to 1024 bytes), and the
+  // producer's per-request unit prefix and lengths after it.
   p.nst = mma ? 6 : 7;
-  const int smem = p.nst * kUnitBytes + (mma ? 1024 : 0);
+  const int smem = p.nst * kUnitBytes + (mma ? 1024 : 0) + 8 * (a.B + 1);
   cudaError_t e = allow_smem(fn, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -692,7 +667,7 @@ cudaError_t launch_index_score(const ScoreArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   long long blocks = static_cast<long long>(sm_count()) * per_sm;
-  if (p.units < blocks) blocks = p.units;
+  if (units < blocks) blocks = units;
   e = launch_pdl(fn, dim3(static_cast<unsigned>(blocks)), dim3(kScoreThreads), smem, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
