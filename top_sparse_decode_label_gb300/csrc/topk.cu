@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       for (int i = 0; i < kBmPer; ++i) {
         const int blk = tid * kBmPer + i;
         mk[i] = blk < nbk ? order_key(__ldcg(bm + blk)) : 0u;
-        warp_hist_add_grouped(X.hm, mk[i] >> 21, blk < nbk);
+        warp_hist_add(X.hm, mk[i] >> 21, blk < nbk);
       }
       __syncthreads();
       cluster_wait();
@@ -437,13 +437,9 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
         mc += tot;
       }
       __syncthreads();
-      // Digit-1 histogram of the candidates (an overflowing list is not used);
-      // most of them share a bin or two.
-      const unsigned lim = min(mc, static_cast<unsigned>(kListCap));
-      for (unsigned e0 = 0; e0 < lim; e0 += kThreads) {
-        const unsigned e = e0 + static_cast<unsigned>(tid);
-        warp_hist_add_grouped(S.h1, e < lim ? S.list[e].x >> 21 : 0u, e < lim);
-      }
+      // Digit-1 histogram of the candidates (an overflowing list is not used).
+      for (unsigned e = static_cast<unsigned>(tid); e < min(mc, static_cast<unsigned>(kListCap)); e += kThreads)
+        warp_hist_add(S.h1, S.list[e].x >> 21, true);
     } else {
       // Warp w owns the contiguous token range [w0, w1) of the slice, in tiles
       // of kStep keys (kPerF per lane), so each warp appends its candidates in

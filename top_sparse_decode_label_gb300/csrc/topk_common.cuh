@@ -22,15 +22,6 @@ __device__ __forceinline__ void warp_hist_add(unsigned* h, unsigned bin, bool pr
   if (pred) atomicAdd(h + hslot(static_cast<int>(bin)), 1u);
 }
 
-// The same for histograms whose keys crowd into a few bins: lanes with equal
-// bins are grouped first and one atomic per distinct bin adds the group's
-// size. Every lane of the warp must call it.
-__device__ __forceinline__ void warp_hist_add_grouped(unsigned* h, unsigned bin, bool pred) {
-  const unsigned peers = __match_any_sync(0xffffffffu, pred ? bin : 0xffffffffu);
-  if (pred && __ffs(peers) - 1 == static_cast<int>(threadIdx.x & 31))
-    atomicAdd(h + hslot(static_cast<int>(bin)), static_cast<unsigned>(__popc(peers)));
-}
-
 // Rows that need a selection at all: 0 < K_eff < T.
 __device__ __forceinline__ bool needs_selection(int k, int T) { return k > 0 && k < T; }
 
