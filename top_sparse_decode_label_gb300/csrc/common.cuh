@@ -347,6 +347,9 @@ __device__ __forceinline__ void cluster_red_add(uint32_t addr, unsigned v) {
 __device__ __forceinline__ void cluster_red_max(uint32_t addr, unsigned v) {
   asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void cluster_red_min(uint32_t addr, unsigned v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned cluster_ld(uint32_t addr) {
   unsigned v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");

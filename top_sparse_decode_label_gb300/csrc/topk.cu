@@ -24,18 +24,20 @@
 // token order is below r; the counts of the CTAs before it give its output
 // offset. No global atomics, no completion counters, nothing to clear.
 //
-// Long rows with a small k (slices of two passes or more, K_eff <= T/128) try
-// one filtered pass first (a kernel variant with one CTA per SM, launched
-// when full-length rows qualify). Each CTA samples the largest of each lane's
-// first 32 keys and takes as its filter bin the first-digit bin where those maxima,
-// counted from the top, reach twice its share of K_eff scaled to the sample;
-// each warp then streams its own contiguous part of the slice once, adding to
-// the digit-1 histogram and to its token-ordered candidate list only the keys
-// whose first digit reaches the filter bin. The histogram is exact from the
-// highest filter bin of the cluster up, so a crossing found there is the true
-// digit 1 and the lists hold every key that can be kept; otherwise (or when a
-// warp's list overflows) the cluster clears its histograms and takes the two
-// passes above.
+// Rows with slices of two passes or more and K_eff <= T/128 first try a
+// filtered pass (a kernel variant with one CTA per SM, launched when
+// full-length rows qualify): a filter key that all CTAs of the cluster share
+// lets only the keys at or above it into the candidate lists and their
+// digit-1 histogram. The filter key comes from the scan's 16-token block
+// maxima when there are any (the first-digit bin where the row's block maxima
+// reach K_eff, an exact lower bound; only blocks whose maximum reaches it are
+// read), otherwise from a sample of the keys (the key where the sample, counted from
+// the top, reaches the kept fraction plus three standard deviations; the
+// cluster takes its CTAs' smallest). Either way every key at or above the
+// filter is a candidate, so a digit-1 crossing in the candidates' totals is
+// the true one and the lists hold every key that can be kept; when there is
+// none (too few keys passed) or a list overflows, the cluster clears its
+// histograms and takes the two passes above.
 #include "common.cuh"
 #include "internal.h"
 #include "topk_common.cuh"
@@ -92,6 +94,7 @@ struct __align__(16) Smem {
   unsigned cnt[2];       // this CTA's keys above the threshold, equal to it
   unsigned res[4];
   unsigned lmax;         // filtered pass: the highest filter bin of the cluster (rank 0's copy)
+  unsigned lmin;         // sampled filter: the smallest filter key of the cluster (rank 0's copy)
   unsigned wcnt[kThreads / 32];   // filtered pass: candidates of each warp's token range
   unsigned woff[kThreads / 32];
   int pt[kPtCap];        // page-table entries of this CTA's slice (chained call)
@@ -155,10 +158,14 @@ __device__ __forceinline__ int tile_token(int base, int r, int q) {
 }
 
 // Rows that try the filtered pass: CTA slices of two passes or more, and at
-// most 1/128 of the row kept.
+// most 1/128 of the row kept (with more kept, the two passes of the other
+// variant, two CTAs per SM, were measured faster on GB300).
 __host__ __device__ __forceinline__ bool filtered_row(int slice, long long keff, int T) {
   return slice >= 2 * kBatch && keff * 128 <= T;
 }
+// Filtered rows that bound the threshold with the scan's block maxima:
+// slices of at most kBmCap blocks.
+__host__ __device__ __forceinline__ bool block_maxima_row(int slice) { return slice <= kMaxBlock * kBmCap; }
 
 // Adds this CTA's histogram h (nbins bins, slots hslot) into the owners'
 // totals t: bin b belongs to cluster rank b / (nbins / cs).
@@ -271,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     }
     if (tid == 0) {
       S.lmax = 0u;
+      S.lmin = 0xffffffffu;
       S.res[0] = 0u;
     }
   }
@@ -320,23 +328,21 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
   unsigned b1 = 0, above1 = 0, M = 0;
   uint2* lst = S.list;
   bool filtered = false;
-  // Rows whose CTA slices span two passes or more and that keep at most
-  // 1/128 of their tokens first try one filtered pass: a lower bound on the
-  // threshold's first digit, guessed from a sample, lets only the keys at or
-  // above it into the histogram and the candidate list. The guess is checked
-  // exactly afterwards; when it fails every CTA of the cluster falls back to
-  // the two passes below.
+  // Filtered rows (see the top of the file): a shared filter key lets only
+  // the keys at or above it into the candidate lists; when too few pass, or a
+  // list overflows, every CTA of the cluster falls back to the two passes
+  // below.
   const int SLr = ((T + static_cast<int>(cs) - 1) / static_cast<int>(cs) + 15) & ~15;
   if (FILT && filtered_row(SLr, keff, T)) {
     const int warp = tid >> 5, lane = tid & 31;
     const int len = s1 - s0;
-    // With the scan's block maxima (slices of at most kBmCap blocks), the
-    // filter bin is exact instead of guessed: the first-digit bin where the
+    // With the scan's block maxima (block_maxima_row), the filter bin is
+    // exact instead of sampled: the first-digit bin where the
     // row's block maxima, counted from the top, reach K_eff. Each of those
     // blocks holds its maximum, so at least K_eff keys lie in that bin or
     // above and so does the threshold; only blocks whose maximum reaches the
     // bin can hold a kept key, and only they are read.
-    const bool bm_path = p.bmax != nullptr && SLr <= kMaxBlock * kBmCap;
+    const bool bm_path = p.bmax != nullptr && block_maxima_row(SLr);
     uint2* sub = S.list + warp * kWarpCap;   // sample path: this warp's candidates, in token order
     unsigned n = 0;    // sample path: this warp's candidates so far (only the first kWarpCap are kept)
     unsigned mc = 0;   // block-maxima path: the CTA's candidates (only the first kListCap are kept)
@@ -463,57 +469,63 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       };
       if (nst > 0) load_tile<kPerF / 4, 32>(s, w0, lane, w1, raw);
       tile_floats();
-      // Sample: the largest key of each lane's share of the first tile. The filter bin
-      // is where the sampled maxima, counted from the top, reach twice this
-      // slice's share of K_eff scaled to a pass of kBatch keys (0, no filter,
-      // when they never do). Fewer maxima than keys lie above any bin, so the
-      // guess errs low.
+      // Sample: two keys of each lane's first tile (up to 1024 per CTA,
+      // spread over the warps' token ranges). The CTA's filter key is where
+      // the sampled keys, counted from the top, reach the row's kept
+      // fraction of the sample plus three standard deviations plus two --
+      // found on the sample digit by digit (11 bits, then 11 more inside that
+      // bin) -- and the cluster filters with the smallest of its CTAs' keys.
+      // A sample whose kept share rounds to all of it gives key 0: no filter.
+      uint32_t lb = 0;
       {
-        float mx = __int_as_float(0x7fffffff);   // NaN: fmaxf keeps the other operand
-        bool any = false;
+        FiltX& X = *reinterpret_cast<FiltX*>(dsm + sizeof(Smem));
+        constexpr int kSamp[2] = {0, kPerF / 2};
+        uint32_t sk[2];
+        bool sv[2];
 #pragma unroll
-        for (int i = 0; i < kPerF; ++i) {
-          if (tile_token<32>(w0, lane, i) < w1) {
-            mx = fmaxf(mx, cur[i]);
-            any = true;
-          }
+        for (int j = 0; j < 2; ++j) {
+          sv[j] = nst > 0 && tile_token<32>(w0, lane, kSamp[j]) < w1;
+          sk[j] = order_key(cur[kSamp[j]]);
+          warp_hist_add(S.h2, sk[j] >> 21, sv[j]);
         }
-        warp_hist_add(S.h2, order_key(mx) >> 21, any);
-      }
-      __syncthreads();
-      const unsigned want =
-          len > 0 ? static_cast<unsigned>((2LL * keff * kThreads * kPerF + static_cast<long long>(cs) * len - 1) /
-                                          (static_cast<long long>(cs) * len))
-                  : 0u;
-      {
+        if (tid == 0) S.res[0] = 0xffffffffu;
+        unsigned ns;
+        block_excl_scan(static_cast<unsigned>(sv[0]) + static_cast<unsigned>(sv[1]),
+                        reinterpret_cast<unsigned*>(S.scan), &ns);
+        const float mu = static_cast<float>(keff) / static_cast<float>(T) * static_cast<float>(ns);
+        const unsigned m = static_cast<unsigned>(ceilf(mu + 3.f * sqrtf(mu) + 2.f));
         const int hi = kBins1 - 4 * tid;
-        unsigned c[4], sum = 0;
+        unsigned c[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          c[j] = S.h2[hslot(hi - 1 - j)];
-          sum += c[j];
-        }
-        unsigned tot;
-        unsigned run = block_excl_scan(sum, reinterpret_cast<unsigned*>(S.scan), &tot);
-        if (want > 0 && run < want && run + sum >= want) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (run + c[j] >= want) {
-              S.res[0] = static_cast<unsigned>(hi - 1 - j);
-              break;
-            }
-            run += c[j];
-          }
-        }
+        for (int j = 0; j < 4; ++j) c[j] = S.h2[hslot(hi - 1 - j)];
+        if (m < ns) find_crossing<kBins1, 4>(c, m, S);
+        const unsigned bs = S.res[0], above = S.res[1];
 #pragma unroll
         for (int j = 0; j < 4; ++j) S.h2[hslot(hi - 1 - j)] = 0u;   // digit 2 starts from zero
+        if (bs != 0xffffffffu) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) warp_hist_add(X.hm, (sk[j] >> 10) & 2047u, sv[j] && (sk[j] >> 21) == bs);
+          __syncthreads();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            c[j] = X.hm[hslot(hi - 1 - j)];
+            X.hm[hslot(hi - 1 - j)] = 0u;
+          }
+          find_crossing<kBins1, 4>(c, m - above, S);   // the bin holds the m-th sample
+          lb = (bs << 21) | (S.res[0] << 10);
+        }
       }
-      __syncthreads();
-      lbin = S.res[0];
-      const float flb = key_floor(lbin << 21);
-      const bool take_all = lbin < 4u;
+      cluster_wait();   // every CTA has set up its shared memory
+      cluster_red_min(cluster_map(smem_u32(&S.lmin), 0u), lb);
+      cluster_sync();
+      lb = cluster_ld(cluster_map(smem_u32(&S.lmin), 0u));
+      cluster_arrive();   // no more reads of rank 0's filter key; paired with the wait before the next push
+      lbin = lb >> 21;
+      // Keys below -inf's are NaN patterns: such a filter takes every key.
+      const float flb = key_floor(lb);
+      const bool take_all = lb < (4u << 21);
       // ---- the filtered pass: the candidate list of the keys >= lb, then their digit-1 histogram
-      for (int st = 0; st < nst; ++st) {
+      for (int st = 0; st < (lb != 0 ? nst : 0); ++st) {
         const int tb = w0 + st * kStep;
         if (st > 0) tile_floats();
         if (st + 1 < nst) load_tile<kPerF / 4, 32>(s, tb + kStep, lane, w1, raw);
