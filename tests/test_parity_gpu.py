@@ -279,6 +279,8 @@ CHAIN_CASES = [
     ("llama_ds_d256_small", dsgen.WORKLOADS[1].scaled(batch=2, seq_lens=[5000, 77], top_k=300, head_dim=256)),
     # Rows of one call whose k is small, large and equal against their length.
     ("mixed_rows", dsgen.WORKLOADS[1].scaled(seq_lens=[6000, 1000, 300], top_k=300)),
+    # 96 rows of up to 20,000 tokens: two-CTA clusters whose full slices take one pass of 20 keys per thread.
+    ("longchat_one_wide_pass", dsgen.WORKLOADS[2].scaled(seq_lens=[20000, 17001, 9000], top_k=1024)),
 ]
 
 

@@ -260,9 +260,13 @@ __device__ __forceinline__ void emit(const TopkParams& p, const Smem& S, int row
 
 // FILT: the variant that tries the filtered pass first (one CTA per SM, so
 // that its deeper loads keep their registers); the other one runs two CTAs
-// per SM.
-template <bool FILT>
+// per SM. KPER: keys per thread per pass of the two passes (16, or 20 so that
+// slices of up to 10,240 keys take one pass and the second pass reuses the
+// keys still in registers).
+template <bool FILT, int KPER = kPer>
 __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(const TopkParams p) {
+  constexpr int PASS = kThreads * KPER;            // keys per CTA pass
+  constexpr int FB = KPER / 4 <= 4 ? 16 : 12;      // bits per group count in the packed scan
   extern __shared__ __align__(16) unsigned char dsm[];
   Smem& S = *reinterpret_cast<Smem*>(dsm);
   const int tid = threadIdx.x;
@@ -658,17 +662,17 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
 
   if (!filtered) {
     // ---- digit 1 (key bits 21..31) over the slice
-    const int nb = (s1 - s0 + kBatch - 1) / kBatch;
+    const int nb = (s1 - s0 + PASS - 1) / PASS;
     // Passes over the slice with the next pass's loads in flight.
-    float4 raw[kPer / 4];
-    uint32_t cur[kPer];
-    if (nb > 0) load_tile<kPer / 4, kThreads>(s, s0, tid, s1, raw);
+    float4 raw[KPER / 4];
+    uint32_t cur[KPER];
+    if (nb > 0) load_tile<KPER / 4, kThreads>(s, s0, tid, s1, raw);
     for (int bt = 0; bt < nb; ++bt) {
-      const int tb = s0 + bt * kBatch;
+      const int tb = s0 + bt * PASS;
       tile_keys(raw, cur);
-      if (bt + 1 < nb) load_tile<kPer / 4, kThreads>(s, tb + kBatch, tid, s1, raw);
+      if (bt + 1 < nb) load_tile<KPER / 4, kThreads>(s, tb + PASS, tid, s1, raw);
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) warp_hist_add(S.h1, cur[i] >> 21, tile_token<kThreads>(tb, tid, i) < s1);
+      for (int i = 0; i < KPER; ++i) warp_hist_add(S.h1, cur[i] >> 21, tile_token<kThreads>(tb, tid, i) < s1);
     }
     __syncthreads();
     cluster_wait();
@@ -714,22 +718,22 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
     lst = (M <= static_cast<unsigned>(kListCap)) ? S.list : p.list + static_cast<size_t>(row) * p.Tmax + s0;
     unsigned base = 0;
     // (with one pass, raw still holds it)
-    if (nb > 1) load_tile<kPer / 4, kThreads>(s, s0, tid, s1, raw);
+    if (nb > 1) load_tile<KPER / 4, kThreads>(s, s0, tid, s1, raw);
     for (int bt = 0; bt < nb; ++bt) {
-      const int tb = s0 + bt * kBatch;
+      const int tb = s0 + bt * PASS;
       tile_keys(raw, cur);
-      if (bt + 1 < nb) load_tile<kPer / 4, kThreads>(s, tb + kBatch, tid, s1, raw);
+      if (bt + 1 < nb) load_tile<KPER / 4, kThreads>(s, tb + PASS, tid, s1, raw);
       // Candidates per group of 4 (group g = 2048 contiguous tokens of the
-      // pass), packed 16 bits per group: one block scan orders them.
+      // pass), packed FB bits per group: one block scan orders them.
       unsigned flags = 0;
       unsigned long long packed = 0;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
+      for (int i = 0; i < KPER; ++i) {
         const bool valid = tile_token<kThreads>(tb, tid, i) < s1;
         const unsigned d1 = cur[i] >> 21;
         if (valid && d1 >= b1) {
           flags |= 1u << i;
-          packed += 1ull << (16 * (i >> 2));
+          packed += 1ull << (FB * (i >> 2));
         }
         warp_hist_add(S.h2, (cur[i] >> 10) & 2047u, valid && d1 == b1);
       }
@@ -737,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       const unsigned long long ex = block_excl_scan64(packed, S.scan, &tot);
       unsigned gbase = base;
 #pragma unroll
-      for (int g = 0; g < kPer / 4; ++g) {
-        unsigned pos = gbase + static_cast<unsigned>((ex >> (16 * g)) & 65535u);
+      for (int g = 0; g < KPER / 4; ++g) {
+        unsigned pos = gbase + static_cast<unsigned>((ex >> (FB * g)) & ((1u << FB) - 1u));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = 4 * g + j;
           if ((flags >> i) & 1u) lst[pos++] = make_uint2(cur[i], static_cast<unsigned>(tile_token<kThreads>(tb, tid, i)));
         }
-        gbase += static_cast<unsigned>((tot >> (16 * g)) & 65535u);
+        gbase += static_cast<unsigned>((tot >> (FB * g)) & ((1u << FB) - 1u));
       }
       base = gbase;
     }
@@ -841,17 +845,17 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
 
 // Clusters of `cs` CTAs of variant FILT the current device keeps resident at
 // once (cached per device; 0 if unknown). Also sets the kernel's attributes.
-template <bool FILT>
+template <bool FILT, int KPER = kPer>
 int resident_clusters(int cs, int smem) {
   static int cache[64][5] = {};
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT, KPER>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return 0;
-    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+    if (cudaFuncSetAttribute(topk_cluster_kernel<FILT, KPER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
         cudaSuccess)
       cudaGetLastError();
     attr_done[dev] = true;
@@ -871,7 +875,7 @@ int resident_clusters(int cs, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<FILT>, &cfg) != cudaSuccess || n < 0) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<FILT, KPER>, &cfg) != cudaSuccess || n < 0) n = 0;
   cudaGetLastError();
   c = n > 0 ? n : -1;
   return n;
@@ -935,9 +939,14 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     cs = cluster_size([&](int c) { return resident_clusters<true>(c, smem_f); });
     filt = filtered_row(((a.Tmax + cs - 1) / cs + 15) & ~15, keff_max, a.Tmax);
   }
+  bool wide = false;   // the two-pass variant with 20 keys per thread per pass
   if (!filt) {
     if (resident_clusters<false>(1, smem) <= 0) return cudaErrorNotSupported;
     cs = cluster_size([&](int c) { return resident_clusters<false>(c, smem); });
+    // Full-length slices of one pass at 20 keys per thread but two at 16:
+    // the wider pass, whose second pass reuses the keys in registers.
+    const int slice = ((a.Tmax + cs - 1) / cs + 15) & ~15;
+    wide = slice > kBatch && slice <= kThreads * 20 && resident_clusters<false, 20>(cs, smem) >= R;
   }
   if (static_cast<long long>(R) * cs > 0x7fffffffLL) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
@@ -954,8 +963,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = filt ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, p)
-                       : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, p);
+  cudaError_t e = filt   ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, p)
+                  : wide ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false, 20>, p)
+                         : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
