@@ -356,11 +356,30 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       const int nbk = (len + kMaxBlock - 1) / kMaxBlock;   // s0 is a multiple of 16
       const float* bm = p.bmax + static_cast<long long>(row) * p.nbr + s0 / kMaxBlock;
       uint32_t mk[kBmPer];
+      {
+        // Thread t's kBmPer maxima, as two 16-byte loads where they are whole
+        // and aligned (a quarter of the sectors the scalar loads request).
+        float mf[kBmPer];
+        const int blk0 = tid * kBmPer;
+        if ((reinterpret_cast<uintptr_t>(bm + blk0) & 15u) == 0 && blk0 + kBmPer <= nbk) {
 #pragma unroll
-      for (int i = 0; i < kBmPer; ++i) {
-        const int blk = tid * kBmPer + i;
-        mk[i] = blk < nbk ? order_key(__ldcg(bm + blk)) : 0u;
-        warp_hist_add(X.hm, mk[i] >> 21, blk < nbk);
+          for (int i = 0; i < kBmPer / 4; ++i) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(bm + blk0) + i);
+            mf[4 * i] = f.x;
+            mf[4 * i + 1] = f.y;
+            mf[4 * i + 2] = f.z;
+            mf[4 * i + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBmPer; ++i) mf[i] = blk0 + i < nbk ? __ldcg(bm + blk0 + i) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBmPer; ++i) {
+          const int blk = blk0 + i;
+          mk[i] = blk < nbk ? order_key(mf[i]) : 0u;
+          warp_hist_add(X.hm, mk[i] >> 21, blk < nbk);
+        }
       }
       __syncthreads();
       cluster_wait();
