@@ -58,7 +58,7 @@ constexpr int kStep = 32 * kPerF;             // keys of one warp step of the fi
 constexpr int kWarpCap = kListCap / kWarps;   // (key, token) pairs one warp keeps in the filtered pass
 constexpr int kBmPer = 8;                     // block maxima per thread (block-maxima filter)
 constexpr int kBmCap = kThreads * kBmPer;     // 16-token blocks of a CTA slice that takes the block-maxima filter
-constexpr int kGatherPer = 2;                 // candidate blocks per thread read in one round trip
+constexpr int kGatherRounds = 4;              // rounds of kThreads / 4 candidate blocks read in one round trip
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -407,63 +407,58 @@ __global__ void __launch_bounds__(kThreads, FILT ? 1 : 2) topk_cluster_kernel(co
       const float flb = key_floor(lb);
       const bool take_all = lbin < 4u;
       const bool al = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
-      // The 16 scores of the block at token tb (none past s1) and the mask of its candidates.
-      auto load_block = [&](int tb, float (&v)[kMaxBlock]) {
-        if (al && tb + kMaxBlock <= s1) {
+      // Batches of kGatherRounds x kThreads / 4 candidate blocks. In round u
+      // thread t reads the 16-byte quarter t % 4 of block
+      // cb + u kThreads / 4 + t / 4, so each warp load covers 8 whole blocks
+      // (whole 32-byte sectors); all rounds' loads are issued before any is
+      // used, and one block scan of per-round counts (16 bits each) orders
+      // the batch: token order is round, then thread order.
+      constexpr int BPR = kThreads / 4;   // blocks per round
+      for (int cb = 0; cb < static_cast<int>(nc); cb += kGatherRounds * BPR) {
+        float4 v[kGatherRounds];
+        int tb[kGatherRounds];
 #pragma unroll
-          for (int j = 0; j < kMaxBlock / 4; ++j) {
-            const float4 f = __ldcg(reinterpret_cast<const float4*>(s + tb) + j);
-            v[4 * j] = f.x;
-            v[4 * j + 1] = f.y;
-            v[4 * j + 2] = f.z;
-            v[4 * j + 3] = f.w;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < kMaxBlock; ++j) v[j] = tb + j < s1 ? __ldcg(s + tb + j) : 0.f;
-        }
-      };
-      auto block_mask = [&](int tb, const float (&v)[kMaxBlock]) {
-        unsigned m = 0;
-#pragma unroll
-        for (int j = 0; j < kMaxBlock; ++j)
-          if ((take_all || v[j] >= flb) && tb + j < s1) m |= 1u << j;
-        return m;
-      };
-      auto append = [&](int tb, const float (&v)[kMaxBlock], unsigned m, unsigned& q) {
-#pragma unroll
-        for (int j = 0; j < kMaxBlock; ++j) {
-          if ((m >> j) & 1u) {
-            if (q < static_cast<unsigned>(kListCap)) S.list[q] = make_uint2(order_key(v[j]), static_cast<unsigned>(tb + j));
-            ++q;
+        for (int u = 0; u < kGatherRounds; ++u) {
+          const int ci = cb + u * BPR + (tid >> 2);
+          tb[u] = ci < static_cast<int>(nc) ? s0 + kMaxBlock * static_cast<int>(X.cblk[ci]) + 4 * (tid & 3) : s1;
+          if (al && tb[u] + 4 <= s1) {
+            v[u] = __ldcg(reinterpret_cast<const float4*>(s + tb[u]));
+          } else {
+            v[u].x = tb[u] < s1 ? __ldcg(s + tb[u]) : 0.f;
+            v[u].y = tb[u] + 1 < s1 ? __ldcg(s + tb[u] + 1) : 0.f;
+            v[u].z = tb[u] + 2 < s1 ? __ldcg(s + tb[u] + 2) : 0.f;
+            v[u].w = tb[u] + 3 < s1 ? __ldcg(s + tb[u] + 3) : 0.f;
           }
         }
-      };
-      // Batches of up to kGatherPer * kThreads candidate blocks: in a batch
-      // thread t owns a run of at most kGatherPer consecutive blocks and
-      // issues all their loads before using any, one round trip per batch.
-      for (int cb = 0; cb < static_cast<int>(nc); cb += kGatherPer * kThreads) {
-        const int nb_ = min(static_cast<int>(nc) - cb, kGatherPer * kThreads);
-        const int per = (nb_ + kThreads - 1) / kThreads;
-        const int c0 = cb + min(nb_, tid * per), c1 = cb + min(nb_, tid * per + per);
-        float v[kGatherPer][kMaxBlock];
-        int tb[kGatherPer];
+        unsigned m[kGatherRounds];
+        unsigned long long packed = 0;
 #pragma unroll
-        for (int u = 0; u < kGatherPer; ++u) {
-          tb[u] = c0 + u < c1 ? s0 + kMaxBlock * static_cast<int>(X.cblk[c0 + u]) : s1;   // s1: nothing to load
-          load_block(tb[u], v[u]);
+        for (int u = 0; u < kGatherRounds; ++u) {
+          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          m[u] = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if ((take_all || x[j] >= flb) && tb[u] + j < s1) m[u] |= 1u << j;
+          packed += static_cast<unsigned long long>(__popc(m[u])) << (16 * u);
         }
-        unsigned m[kGatherPer], cnt = 0;
+        unsigned long long tot;
+        const unsigned long long ex = block_excl_scan64(packed, S.scan, &tot);
+        unsigned base = mc;
 #pragma unroll
-        for (int u = 0; u < kGatherPer; ++u) {
-          m[u] = block_mask(tb[u], v[u]);
-          cnt += static_cast<unsigned>(__popc(m[u]));
+        for (int u = 0; u < kGatherRounds; ++u) {
+          unsigned q = base + static_cast<unsigned>((ex >> (16 * u)) & 65535u);
+          const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if ((m[u] >> j) & 1u) {
+              if (q < static_cast<unsigned>(kListCap))
+                S.list[q] = make_uint2(order_key(x[j]), static_cast<unsigned>(tb[u] + j));
+              ++q;
+            }
+          }
+          base += static_cast<unsigned>((tot >> (16 * u)) & 65535u);
         }
-        unsigned tot;
-        unsigned q = mc + block_excl_scan(cnt, reinterpret_cast<unsigned*>(S.scan), &tot);
-#pragma unroll
-        for (int u = 0; u < kGatherPer; ++u) append(tb[u], v[u], m[u], q);
-        mc += tot;
+        mc = base;
       }
       __syncthreads();
       // Digit-1 histogram of the candidates (an overflowing list is not used).
