@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
   __shared__ float cw[kWarps][8];          // each warp's weight per head in the combine
   __shared__ float cm[8], cl[8];
   __shared__ float mw[16][8], mm[8], ml[8];   // each split's normalised weight per head in the merge
-  __shared__ unsigned sh_scan[33];
+  __shared__ unsigned long long sh_scan[33];
   __shared__ unsigned sh_cnt[kWarps];
 
   const int tid = threadIdx.x;
@@ -206,14 +206,17 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
 
   for (int sb = p0; sb < p1; sb += kSeg) {
     const int se = min(p1, sb + kSeg);
-    // ---- resolve the slots of this segment, in order
+    // ---- resolve the slots of this segment, in order: in round i thread t
+    // takes position sb + i kThreads + t (coalesced loads), and one scan of
+    // the rounds' counts (16 bits each) orders them, round by round.
     constexpr int PPT = kSeg / kThreads;
+    static_assert(PPT <= 4, "four 16-bit round counts in the scan");
     int slot_v[PPT];
     float2 sc_v[PPT];
-    unsigned cnt = 0;
+    unsigned long long packed = 0;
 #pragma unroll
     for (int i = 0; i < PPT; ++i) {
-      const int pos = sb + tid * PPT + i;
+      const int pos = sb + i * kThreads + tid;
       slot_v[i] = -1;
       sc_v[i] = make_float2(1.f, 1.f);
       if (pos < se && p.slots) {
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
         if (sv >= 0) {
           slot_v[i] = sv;
           if (FP8) sc_v[i] = p.sscale ? given : make_float2(__ldg(p.ks + sv / kPage), __ldg(p.vs + sv / kPage));
-          ++cnt;
+          packed += 1ull << (16 * i);
         }
       } else if (pos < se) {
         const int t = row[pos];
@@ -241,20 +244,22 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const AttnParams 
           } else {
             slot_v[i] = pid * kPage + (t & (kPage - 1));
             if (FP8) sc_v[i] = make_float2(__ldg(p.ks + pid), __ldg(p.vs + pid));
-            ++cnt;
+            packed += 1ull << (16 * i);
           }
         }
       }
     }
-    unsigned nseg_u;
-    unsigned wpos = block_excl_scan(cnt, sh_scan, &nseg_u);
+    unsigned long long tot;
+    const unsigned long long ex = block_excl_scan64(packed, sh_scan, &tot);
+    unsigned nseg_u = 0;
 #pragma unroll
     for (int i = 0; i < PPT; ++i) {
       if (slot_v[i] >= 0) {
+        const unsigned wpos = nseg_u + static_cast<unsigned>((ex >> (16 * i)) & 65535u);
         sl[wpos] = slot_v[i];
         if (FP8) sc[wpos] = sc_v[i];
-        ++wpos;
       }
+      nseg_u += static_cast<unsigned>((tot >> (16 * i)) & 65535u);
     }
     __syncthreads();
     const int nseg = static_cast<int>(nseg_u);
