@@ -106,3 +106,16 @@ def test_long_row_threshold_inside_a_tie_class():
     seq = torch.tensor([T], dtype=torch.int32)
     for k in (1000, 2000, 4000):
         assert torch.equal(_topk_gpu(s, seq, k), oracle.topk(s, seq, k)), k
+
+
+def test_long_row_tie_class_inside_one_slice():
+    # 2500 consecutive tokens share one value in the threshold's first-digit bin (scores 3 to 3.5), all
+    # inside one CTA's slice: one CTA of the cluster holds nearly all of the keys that digits 2 and 3 and
+    # the tie rule decide on. k = 1000 (the filtered variant) and k = 2500 (the two-pass variant) both put
+    # the threshold inside the tie class.
+    T = 300000
+    s = dsgen.normal((1, 1, T), 19, 5, dtype=torch.float32)
+    s[0, 0, 5000:7500] = 3.25
+    seq = torch.tensor([T], dtype=torch.int32)
+    for k in (1000, 2500):
+        assert torch.equal(_topk_gpu(s, seq, k), oracle.topk(s, seq, k)), k
