@@ -79,7 +79,9 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v, float
 template <bool FP8, int D>
 struct Cfg {
   static constexpr int ROWB = FP8 ? D : D * 2;   // bytes per K or V row
-  static constexpr int NST = FP8 ? 4 : 2;                       // ring stages per warp
+  // Ring stages per warp. At D = 256 half as many (a 64 KB ring, three CTAs
+  // per SM), so that twice the splits stay resident in one wave.
+  static constexpr int NST = D == 128 ? (FP8 ? 4 : 2) : (FP8 ? 2 : 1);
   static constexpr int STAGE = 2 * kTok * ROWB;                 // K tile then V tile
   static constexpr int RING = kWarps * NST * STAGE;
   static constexpr int SMEM = RING + kSeg * 4 + (FP8 ? kSeg * 8 : 0);
