@@ -574,18 +574,9 @@ KernelFn pick(int G, int fp8, int D) {
   return nullptr;
 }
 
-// Dynamic shared memory of a launch. e4m3 at D = 128 asks for at least
-// 80 KB, so that no more than two CTAs share an SM: left at three, the
-// clusters of a launch were packed onto the first free SMs (8 requests of
-// 262,144 tokens with 4 KV heads: 256 CTAs on 120 of 152 SMs), and CTAs
-// sharing an SM with two others finished their tiles about 2.4 us later than
-// CTAs alone. That call took 1.5 us less with the cap; the bf16 shapes were
-// unchanged or slower with it.
 int smem_bytes(int fp8, int D) {
   if (D == 256) return fp8 ? Cfg<true, 256>::SMEM : Cfg<false, 256>::SMEM;
-  if (!fp8) return Cfg<false, 128>::SMEM;
-  constexpr int kMinFp8 = 80 << 10;
-  return Cfg<true, 128>::SMEM < kMinFp8 ? kMinFp8 : Cfg<true, 128>::SMEM;
+  return fp8 ? Cfg<true, 128>::SMEM : Cfg<false, 128>::SMEM;
 }
 
 cudaError_t prepare(KernelFn fn, int bytes) {
