@@ -363,15 +363,19 @@ ds_status ds_sparse_decode_blocks(const ds_shape* shape, const ds_block_decode_a
                                   size_t workspace_bytes, ds_stream_t stream);
 
 /*
- * Kernel launches one ds_sparse_decode call makes for this shape and k (not
- * counting the one cudaMemsetAsync of the top-k counters); 0 when the
- * arguments are invalid or there is nothing to do. Host-only query.
+ * Kernel launches one ds_sparse_decode call makes for this shape and k (it
+ * issues no other device work: no copies, no memsets); 0 when the arguments
+ * are invalid or there is nothing to do. Host-only query.
  */
 int ds_decode_kernel_launches(const ds_shape* shape, int k);
 
 /*
  * Split-KV count the chained call uses internally for this shape and k (so a
- * caller running the four stages one by one can reproduce it). Host-only.
+ * caller running the four stages one by one can reproduce it): the largest
+ * power of two up to 16 with at most one split per started 64 selected
+ * tokens and at most 456 (request, KV head, split) CTAs, lowered on a device
+ * until every cluster of splits is resident at once. 0 for an invalid shape.
+ * Host-only.
  */
 int ds_decode_num_splits(const ds_shape* shape, int k);
 

@@ -95,6 +95,36 @@ def test_workspace_queries_are_host_only_and_grow_with_the_problem():
     assert ds.ds_topk_workspace_bytes(_shape(head_dim=64), 16) == 0
 
 
+def test_split_and_launch_queries_follow_their_rules():
+    # The chained call's split count is a power of two up to 16, at most one split per started 64 selected
+    # tokens, and keeps the (request, KV head, split) CTAs at or under 456 (three per SM); on a device it is
+    # lowered further until every cluster of splits is resident at once. Without a device the count is the
+    # rule alone.
+    import torch
+    import top_sparse_decode_label_gb300 as ds
+    cases = [  # batch, Hq, Hkv, T, k, count from the rule alone
+        (3, 32, 8, 60000, 3000, 16),
+        (3, 32, 32, 20000, 1024, 4),
+        (8, 32, 4, 262144, 2048, 8),
+        (1, 32, 4, 1048576, 2048, 16),
+        (2, 8, 2, 4096, 64, 1),
+        (2, 8, 2, 4096, 100, 2),
+    ]
+    for B, Hq, Hkv, T, k, rule in cases:
+        pages = -(-T // 64)
+        sh = _shape(batch=B, num_q_heads=Hq, num_kv_heads=Hkv, max_seq_len=T, max_pages_per_req=pages,
+                    num_pages=B * pages)
+        S = ds.ds_decode_num_splits(sh, k)
+        assert 1 <= S <= rule and S & (S - 1) == 0, (B, Hkv, T, k, S)
+        assert S == 1 or (S <= -(-k // 64) and B * Hkv * S <= 456)
+        if not torch.cuda.is_available():
+            assert S == rule, (B, Hkv, T, k, S)
+        # One kernel per stage: scoring, top-k, attention with its merge.
+        assert ds.ds_decode_kernel_launches(sh, k) == 3
+        assert ds.ds_decode_kernel_launches(sh, 0) == 2
+    assert ds.ds_decode_num_splits(_shape(batch=-1), 100) == 0
+
+
 def test_error_strings():
     import top_sparse_decode_label_gb300 as ds
     for st in (0, -1, -2, -3, -4, -5):

@@ -84,8 +84,8 @@ int sm_count() {
 // Internal split count of the chained call: the largest power of two up to
 // 16 (the splits of a (request, KV head) form one thread-block cluster) that
 // keeps the (request, KV head, split) CTAs within about three per SM, with at
-// least 64 selected tokens per split -- and, when the device can be queried,
-// with every cluster resident at once (no second wave).
+// most one split per started 64 selected tokens -- and, when the device can
+// be queried, with every cluster resident at once (no second wave).
 int decode_splits(const ds_shape* s, int k) {
   const long long rows = static_cast<long long>(s->batch) * s->num_kv_heads;
   if (rows <= 0 || k <= 64) return 1;
